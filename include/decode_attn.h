@@ -1,0 +1,216 @@
+/*
+ * decode_attn.h — C ABI of the GB300 decode-attention library
+ * (libdecode_attn.so, built from quantized_kv_decode_paged_gb300/csrc).
+ *
+ * The operation: single-token (decode) grouped-query attention over a KV
+ * cache whose pages are reached through a per-sequence block table, with an
+ * optional int8 cold tier and an f16 hot ring.  For every sequence b and
+ * query head h (kv head = h / (Hq/Hkv)) the library computes
+ *
+ *     s_t   = scale * <Q[b,h,:], K_t>           (optionally  cap*tanh(s_t/cap))
+ *     out   = sum_t softmax(s)_t * V_t           over the visible keys t
+ *     lse   = max_t s_t + ln sum_t exp(s_t - max_t s_t)     (natural log)
+ *
+ * Definitions followed:
+ *   - paged layout, block_table indirection and the LSE output:
+ *       boostr "paged_attention.wgsl", paged_attention_fwd_f32 (both passes
+ *       and the lse store);
+ *   - GQA head map, causal and sliding-window masks, softcap after scale,
+ *     zero-sum guard: @simulatte/doppler 0.1.0 "attention_f16kv.wgsl",
+ *     get_kv_head_idx / is_masked / the online-softmax block loop;
+ *   - int8 cold tier (4 values per u32, little-endian byte lane d%4, sign
+ *     extended, times one f16 scale per (token, kv head)) and the f16 hot
+ *     ring (slot = (hot_start + j) % hot_window):
+ *       @simulatte/doppler 0.1.0 "attention_decode_tiered_int8_f16kv.wgsl",
+ *       read_cold_k / read_cold_v / get_hot_pos / main;
+ *   - merge of two partial softmax states (m, d):
+ *       com.microsoft.SparseAttention "sparse-attention.wgsl.jinja",
+ *       combine_partials.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument that names a tensor is a DEVICE pointer of the
+ *     current CUDA device, owned by the caller.  The library never frees or
+ *     keeps them.  f16 data is passed as uint16_t (IEEE binary16 bits).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous on that stream and never
+ *     synchronises the host; the library allocates no device memory.
+ *   - Host-detectable errors return a negative da_status before any launch
+ *     and leave every output untouched.
+ *   - Problems that only the device can see (a block id outside
+ *     [0, num_blocks), a length beyond the table, ...) never fault: the
+ *     offending keys are treated as masked (a length is clamped) and the
+ *     matching DA_DEV_* bit is OR-ed into *dev_status when dev_status is
+ *     non-NULL.  The caller zeroes *dev_status before the call.
+ *   - Layouts (row-major, innermost last):
+ *       q            f32  [B, Hq, D]
+ *       k_pool/v_pool f16 [num_blocks, block_size, Hkv, D]
+ *       block_table  i32  [B, max_blocks_per_seq]; logical token t of
+ *                         sequence b lives in page block_table[b][t/bs] at
+ *                         row t % bs
+ *       seq_lens     i32  [B]
+ *       q_pos        i32  [B] absolute position of the query, or NULL
+ *                         (NULL: the last cached token, seq_len-1)
+ *       out          f32  [B, Hq, D]
+ *       lse          f32  [B, Hq] or NULL (not written)
+ *   - A sequence with no visible key (seq_len 0) gets out = 0, lse = -inf.
+ *   - Supported sizes: head_dim in {64, 128, 256}; num_q_heads a multiple of
+ *     num_kv_heads; block_size a power of two in [8, 256]; every pointer
+ *     16-byte aligned.  Other sizes return DA_ERR_UNSUPPORTED.
+ */
+#ifndef DECODE_ATTN_H
+#define DECODE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DA_OK = 0,
+  DA_ERR_INVALID = -1,     /* argument out of range, NULL or misaligned  */
+  DA_ERR_UNSUPPORTED = -2, /* valid request this build does not handle   */
+  DA_ERR_WORKSPACE = -3,   /* workspace too small for the requested path */
+  DA_ERR_CUDA = -4         /* a CUDA runtime or driver call failed       */
+} da_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+enum {
+  DA_DEV_BAD_BLOCK = 1,      /* block_table entry outside [0, num_blocks): its keys are masked */
+  DA_DEV_BAD_SEQ_LEN = 2,    /* length < 0 or beyond max_blocks_per_seq*block_size: clamped    */
+  DA_DEV_BAD_QPOS = 4,       /* q_pos[b] < 0: the row is written as empty (out 0, lse -inf)   */
+  DA_DEV_SPLIT_OVERFLOW = 8, /* split_partial: keys past max_splits*split_tokens were dropped  */
+  DA_DEV_BAD_TIER = 16,      /* tiered: hot_len > ring capacity or negative tier length        */
+  DA_DEV_TIMEOUT = 32        /* an internal pipeline wait gave up (never expected)             */
+};
+
+typedef struct {
+  int32_t batch;              /* B  >= 1                                                     */
+  int32_t num_q_heads;        /* Hq >= 1, multiple of num_kv_heads                           */
+  int32_t num_kv_heads;       /* Hkv >= 1                                                    */
+  int32_t head_dim;           /* D in {64, 128, 256}                                         */
+  int32_t block_size;         /* tokens per page, power of two in [8, 256]                   */
+  int32_t max_blocks_per_seq; /* columns of block_table                                      */
+  int32_t num_blocks;         /* pages in the pool (valid ids are [0, num_blocks))            */
+  int32_t max_seq_len;        /* host upper bound of the key lengths (sizes the launch);
+                                 0 = unknown.  Larger device lengths are still correct.       */
+  float scale;                /* score scale; 0 => 1/sqrt(D) rounded to f32; < 0 invalid      */
+  float softcap;              /* 0 => off; > 0 => s = cap*tanh(s/cap) after scaling; < 0 invalid */
+  int32_t sliding_window;     /* 0 => off; W > 0 => keys below qpos-W+1 are masked when qpos >= W */
+  int32_t causal;             /* 1 => keys after qpos are masked; 0 => not                    */
+} da_params;
+
+/*
+ * decode_attn_paged — f16 paged decode attention, f32 output and LSE.
+ * Operation: boostr "paged_attention.wgsl" paged_attention_fwd_f32 with a
+ * single query per (b, h), plus the causal / sliding-window / softcap rules
+ * of doppler "attention_f16kv.wgsl" is_masked and its softcap step.
+ *
+ * workspace: device scratch of at least decode_attn_workspace_size(p)
+ * bytes, zero-filled once before its first use (decode_attn_workspace_init
+ * or cudaMemsetAsync); every call leaves it zero-filled again.  With it
+ * the keys of long sequences are split across CTAs (flash-decoding) and the
+ * partial results are merged inside the same launch.  workspace = NULL and
+ * workspace_bytes = 0 selects the unsplit path (one CTA per (b, kv head)).
+ * Two calls that share a workspace must be ordered (same stream or
+ * synchronised); calls that overlap on the GPU race on it.
+ * Returns DA_OK or a negative da_status.
+ */
+int decode_attn_paged(const da_params* p, const float* q, const uint16_t* k_pool,
+                      const uint16_t* v_pool, const int32_t* block_table,
+                      const int32_t* seq_lens, const int32_t* q_pos, float* out,
+                      float* lse, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream);
+
+/*
+ * Tier geometry for decode_attn_tiered_int8.
+ * Cold keys have absolute positions 0 .. cold_len-1 and are paged through
+ * block_table (the f16 "coldPageTable" layout of doppler attention.js
+ * executeAttentionTiered, applied to the int8 tier).  Hot key j
+ * (0 <= j < hot_len) has absolute position hot_start + j and lives in ring
+ * slot (hot_start + j) % hot_window, or slot j when hot_window = 0
+ * (doppler "attention_decode_tiered_int8_f16kv.wgsl", get_hot_pos).
+ * The scalar lengths apply to every sequence unless the matching device
+ * array ([B] i32) is non-NULL.
+ */
+typedef struct {
+  int32_t hot_window;   /* ring size W >= 0                                             */
+  int32_t hot_capacity; /* rows per sequence in k_hot / v_hot; >= max(W, 1) and, when
+                           W = 0, >= every hot_len                                     */
+  int32_t cold_len;     /* used when cold_lens == NULL                                  */
+  int32_t hot_len;      /* used when hot_lens == NULL                                   */
+  int32_t hot_start;    /* used when hot_starts == NULL                                 */
+  const int32_t* cold_lens;  /* [B] device or NULL                                      */
+  const int32_t* hot_lens;   /* [B] device or NULL                                      */
+  const int32_t* hot_starts; /* [B] device or NULL                                      */
+} da_tier_params;
+
+/*
+ * decode_attn_tiered_int8 — decode attention over an int8 cold tier and an
+ * f16 hot ring.  Operation: doppler "attention_decode_tiered_int8_f16kv.wgsl"
+ * main (cold loop, hot loop, softmax, PV) batched over B and with the LSE of
+ * boostr paged_attention_fwd_f32.
+ *   k_hot, v_hot   f16 [B, hot_capacity, Hkv, D]
+ *   k_cold, v_cold u32 [num_blocks, block_size, Hkv, D/4]: value d of a row is
+ *                  the signed byte (d % 4) of word d / 4 (little endian)
+ *   k_scale, v_scale f16 [num_blocks, block_size, Hkv]: cold value =
+ *                  int8 * scale of its (token, kv head)
+ *   block_table    i32 [B, max_blocks_per_seq] (cold pages)
+ *   q_pos          i32 [B] or NULL (NULL: hot_start+hot_len-1 when hot_len > 0,
+ *                  else cold_len-1)
+ * p->head_dim must be 128 or 256 here.  p->max_seq_len bounds cold_len +
+ * hot_len.  Workspace rules as for decode_attn_paged.
+ */
+int decode_attn_tiered_int8(const da_params* p, const da_tier_params* t, const float* q,
+                            const uint16_t* k_hot, const uint16_t* v_hot,
+                            const uint32_t* k_cold, const uint32_t* v_cold,
+                            const uint16_t* k_scale, const uint16_t* v_scale,
+                            const int32_t* block_table, const int32_t* q_pos, float* out,
+                            float* lse, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, void* stream);
+
+/*
+ * decode_attn_split_partial — first half of flash-decoding: split s covers
+ * the visible keys of [s*split_tokens, (s+1)*split_tokens) and writes the
+ * normalised partial output and its LSE:
+ *   o_part   f32 [B, Hq, max_splits, D]
+ *   lse_part f32 [B, Hq, max_splits]
+ * A split with no visible key writes o = 0, lse = -inf.  Keys at or beyond
+ * max_splits*split_tokens are not read (DA_DEV_SPLIT_OVERFLOW).
+ * split_tokens must be a positive multiple of block_size.
+ */
+int decode_attn_split_partial(const da_params* p, int32_t split_tokens, int32_t max_splits,
+                              const float* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              const int32_t* q_pos, float* o_part, float* lse_part,
+                              int32_t* dev_status, void* stream);
+
+/*
+ * decode_attn_split_merge — second half: per (b, h), with M = max_s lse_s,
+ *   w_s = exp(lse_s - M),  out = sum_s w_s o_s / sum_s w_s,
+ *   lse = M + ln sum_s w_s;  all splits at -inf give out = 0, lse = -inf.
+ * This is the pairwise (m, d) merge of com.microsoft.SparseAttention
+ * combine_partials applied to max_splits states at once.
+ * lse may be NULL.
+ */
+int decode_attn_split_merge(int32_t batch, int32_t num_q_heads, int32_t head_dim,
+                            int32_t max_splits, const float* o_part, const float* lse_part,
+                            float* out, float* lse, void* stream);
+
+/* Bytes of workspace the split path of decode_attn_paged /
+ * decode_attn_tiered_int8 needs for these parameters on the current device;
+ * 0 when p is invalid. */
+size_t decode_attn_workspace_size(const da_params* p);
+
+/* Zero-fills a workspace (cudaMemsetAsync on stream). */
+int decode_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static text for a da_status value. */
+const char* decode_attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H */

@@ -1,0 +1,465 @@
+/*
+ * decode_attn_oracle.c — reference CPU implementation of paged / tiered
+ * decode attention in double precision.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  The product path
+ * (the CUDA library and its Python binding) never calls it, and this file
+ * shares no code, header or constant with the CUDA sources: every rule below
+ * is restated here from the defining pages.
+ *
+ * It is deliberately plain and slow: one (sequence, query head) row at a
+ * time, the keys visited in logical token order, two passes (the maximum,
+ * then the exponentials, the sum and the weighted V), every value widened to
+ * double before use.
+ *
+ * Pages followed
+ *   [B] boostr "paged_attention.wgsl", paged_attention_fwd_f32: paged
+ *       address ((block*block_size + offset)*Hkv + kv)*D + d, logical token t
+ *       in page block_table[b][t/block_size] row t%block_size, the two-pass
+ *       max / exp-sum structure and lse = ln(sum) + max.
+ *   [F] @simulatte/doppler 0.1.0 "attention_f16kv.wgsl": get_kv_head_idx
+ *       (kv = h / (Hq/Hkv)), is_masked (causal: key > query; window W: when
+ *       query >= W, key < query - W + 1), score = scale*dot then
+ *       cap*tanh(score/cap) when cap > 0, output zero when the sum is zero.
+ *   [T] @simulatte/doppler 0.1.0 "attention_decode_tiered_int8_f16kv.wgsl":
+ *       read_cold_k / read_cold_v (byte lane d%4 of word d/4, sign extended,
+ *       times the f16 scale of (token, kv head)), get_hot_pos (slot =
+ *       (hot_start + j) % hot_window, or j when hot_window = 0), absolute
+ *       position of hot key j = hot_start + j.
+ *   [S] com.microsoft.SparseAttention "sparse-attention.wgsl.jinja",
+ *       combine_partials: m = max(m1, m2), d = d1 e^(m1-m) + d2 e^(m2-m),
+ *       used here in its log-sum-exp form for the split merge.
+ *
+ * Readings where the pages are silent (each also listed in the design
+ * notes): the query position defaults to the last cached key; a row with no
+ * visible key gives out = 0 and lse = -inf; a block id outside
+ * [0, num_blocks) masks its keys and raises flag 1; a length beyond the
+ * block table is clamped (flag 2); q_pos < 0 empties the row (flag 4); keys
+ * past the last split are dropped (flag 8); a bad tier length is clamped
+ * (flag 16).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_FLAG_BAD_BLOCK 1
+#define ORACLE_FLAG_BAD_SEQ_LEN 2
+#define ORACLE_FLAG_BAD_QPOS 4
+#define ORACLE_FLAG_SPLIT_OVERFLOW 8
+#define ORACLE_FLAG_BAD_TIER 16
+
+/* ------------------------------------------------------------------ */
+/* IEEE binary16 -> double, written out from the format definition:   */
+/* 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.            */
+/* ------------------------------------------------------------------ */
+double oracle_half_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int expo = (h >> 10) & 0x1f;
+  int frac = h & 0x3ff;
+  double v;
+  if (expo == 0) {
+    v = ldexp((double)frac, -24); /* subnormal: frac * 2^-14 * 2^-10 */
+  } else if (expo == 31) {
+    v = frac ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(1024 + frac), expo - 25); /* (1 + frac/1024) * 2^(expo-15) */
+  }
+  return sign ? -v : v;
+}
+
+/* [T] read_cold_k: byte lane i of a little-endian u32, two's complement. */
+void oracle_unpack_int8_word(uint32_t word, int32_t out[4]) {
+  for (int lane = 0; lane < 4; ++lane) {
+    int32_t raw = (int32_t)((word >> (8 * lane)) & 0xffu);
+    out[lane] = raw >= 128 ? raw - 256 : raw;
+  }
+}
+
+/* Default score scale: 1/sqrt(D) rounded to f32, then widened. */
+static double effective_scale(double scale, int64_t head_dim) {
+  if (scale > 0.0) return scale;
+  float s = (float)(1.0 / sqrt((double)head_dim));
+  return (double)s;
+}
+
+/* [F] is_masked, with positions as signed 64-bit integers. */
+static int key_visible(int64_t key, int64_t qpos, int64_t causal, int64_t window) {
+  if (causal && key > qpos) return 0;
+  if (window > 0 && qpos >= window && key < qpos - window + 1) return 0;
+  return 1;
+}
+
+static double apply_softcap(double s, double cap) {
+  if (cap > 0.0) return cap * tanh(s / cap);
+  return s;
+}
+
+/*
+ * Two-pass softmax over n scores s[0..n) with value rows fetched through
+ * `vrow`; writes out[D] and *lse.  [B] first pass = max, second = exp, sum
+ * and weighted V; [F] zero output when nothing is visible.
+ */
+typedef void (*value_fetch_fn)(const void* ctx, int64_t key_index, double* v);
+
+static void softmax_two_pass(const double* s, int64_t n, int64_t D, value_fetch_fn vrow,
+                             const void* ctx, double* vbuf, double* out, double* lse) {
+  for (int64_t d = 0; d < D; ++d) out[d] = 0.0;
+  if (n == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double m = -INFINITY;
+  for (int64_t i = 0; i < n; ++i)
+    if (s[i] > m) m = s[i];
+  double l = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    double w = exp(s[i] - m);
+    l += w;
+    vrow(ctx, i, vbuf);
+    for (int64_t d = 0; d < D; ++d) out[d] += w * vbuf[d];
+  }
+  for (int64_t d = 0; d < D; ++d) out[d] /= l;
+  *lse = m + log(l);
+}
+
+/* ================================================================== */
+/* Paged f16 decode                                                   */
+/* ================================================================== */
+typedef struct {
+  int64_t B, Hq, Hkv, D, block_size, max_blocks, num_blocks;
+  double scale;   /* the f32 argument widened; 0 => 1/sqrt(D) */
+  double softcap; /* 0 => off */
+  int64_t window, causal;
+  const float* q;            /* [B, Hq, D] */
+  const uint16_t* k_pool;    /* [NB, bs, Hkv, D] f16 bits */
+  const uint16_t* v_pool;    /* [NB, bs, Hkv, D] f16 bits */
+  const int32_t* block_table;/* [B, max_blocks] */
+  const int32_t* seq_lens;   /* [B] */
+  const int32_t* q_pos;      /* [B] or NULL */
+} oracle_paged_args;
+
+typedef struct {
+  const oracle_paged_args* a;
+  const int64_t* rowaddr; /* element offset of each visible key's V row */
+} paged_vctx;
+
+static void paged_fetch_v(const void* ctx, int64_t i, double* v) {
+  const paged_vctx* c = (const paged_vctx*)ctx;
+  const uint16_t* row = c->a->v_pool + c->rowaddr[i];
+  for (int64_t d = 0; d < c->a->D; ++d) v[d] = oracle_half_to_double(row[d]);
+}
+
+/* Sequence length after the [B]-style bounds rule; sets flags. */
+static int64_t paged_len(const oracle_paged_args* a, int64_t b, int32_t* flags) {
+  int64_t L = a->seq_lens[b];
+  int64_t cap = a->max_blocks * a->block_size;
+  if (L < 0) {
+    *flags |= ORACLE_FLAG_BAD_SEQ_LEN;
+    L = 0;
+  }
+  if (L > cap) {
+    *flags |= ORACLE_FLAG_BAD_SEQ_LEN;
+    L = cap;
+  }
+  return L;
+}
+
+/*
+ * One row (b, h) restricted to keys in [t_begin, t_end) (the whole sequence
+ * for a plain call, one split's range for a split call).
+ */
+static void paged_row(const oracle_paged_args* a, int64_t b, int64_t h, int64_t t_begin,
+                      int64_t t_end, double* out, double* lse, int32_t* flags) {
+  const int64_t D = a->D;
+  const int64_t G = a->Hq / a->Hkv;
+  const int64_t kv = h / G;
+  const double scale = effective_scale(a->scale, D);
+  int64_t L = paged_len(a, b, flags);
+  int64_t qpos = L - 1;
+  if (a->q_pos) {
+    qpos = a->q_pos[b];
+    if (qpos < 0) {
+      *flags |= ORACLE_FLAG_BAD_QPOS;
+      L = 0;
+    }
+  }
+  if (t_end > L) t_end = L;
+  if (t_begin < 0) t_begin = 0;
+  int64_t n_max = t_end > t_begin ? t_end - t_begin : 0;
+  double* s = (double*)malloc(sizeof(double) * (size_t)(n_max + 1));
+  int64_t* rowaddr = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_max + 1));
+  double* vbuf = (double*)malloc(sizeof(double) * (size_t)D);
+  const float* qrow = a->q + (b * a->Hq + h) * D;
+  int64_t n = 0;
+  for (int64_t t = t_begin; t < t_end; ++t) {
+    if (!key_visible(t, qpos, a->causal, a->window)) continue;
+    int64_t blk = a->block_table[b * a->max_blocks + t / a->block_size];
+    if (blk < 0 || blk >= a->num_blocks) {
+      *flags |= ORACLE_FLAG_BAD_BLOCK;
+      continue;
+    }
+    int64_t addr = ((blk * a->block_size + t % a->block_size) * a->Hkv + kv) * D;
+    const uint16_t* krow = a->k_pool + addr;
+    double dot = 0.0;
+    for (int64_t d = 0; d < D; ++d) dot += (double)qrow[d] * oracle_half_to_double(krow[d]);
+    s[n] = apply_softcap(scale * dot, a->softcap);
+    rowaddr[n] = addr;
+    ++n;
+  }
+  paged_vctx ctx = {a, rowaddr};
+  softmax_two_pass(s, n, D, paged_fetch_v, &ctx, vbuf, out, lse);
+  free(s);
+  free(rowaddr);
+  free(vbuf);
+}
+
+/*
+ * rows: flat row ids r = b*Hq + h (NULL => all B*Hq rows in order).
+ * out: [nrows, D]; lse: [nrows].  Returns the OR of the flags.
+ */
+int32_t oracle_decode_paged(const oracle_paged_args* a, const int64_t* rows, int64_t nrows,
+                            double* out, double* lse) {
+  int32_t flags = 0;
+  if (!rows) nrows = a->B * a->Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : flags)
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t r = rows ? rows[i] : i;
+    int64_t b = r / a->Hq, h = r % a->Hq;
+    int32_t f = 0;
+    paged_row(a, b, h, 0, INT64_MAX, out + i * a->D, lse + i, &f);
+    flags |= f;
+  }
+  return flags;
+}
+
+/*
+ * Split partials: split s of row r covers keys [s*split_tokens,
+ * (s+1)*split_tokens).  o_part: [nrows, max_splits, D]; lse_part:
+ * [nrows, max_splits].  Visible keys at or past max_splits*split_tokens
+ * raise flag 8 and are left out.
+ */
+int32_t oracle_decode_paged_split(const oracle_paged_args* a, int64_t split_tokens,
+                                  int64_t max_splits, const int64_t* rows, int64_t nrows,
+                                  double* o_part, double* lse_part) {
+  int32_t flags = 0;
+  if (!rows) nrows = a->B * a->Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : flags)
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t r = rows ? rows[i] : i;
+    int64_t b = r / a->Hq, h = r % a->Hq;
+    int32_t f = 0;
+    for (int64_t sp = 0; sp < max_splits; ++sp) {
+      int64_t t0 = sp * split_tokens, t1 = t0 + split_tokens;
+      paged_row(a, b, h, t0, t1, o_part + (i * max_splits + sp) * a->D,
+                lse_part + i * max_splits + sp, &f);
+    }
+    /* keys beyond the last split: any visible one raises the flag */
+    double tail_lse;
+    double* tail = (double*)malloc(sizeof(double) * (size_t)a->D);
+    int32_t ftail = 0;
+    paged_row(a, b, h, max_splits * split_tokens, INT64_MAX, tail, &tail_lse, &ftail);
+    if (tail_lse > -INFINITY) f |= ORACLE_FLAG_SPLIT_OVERFLOW;
+    free(tail);
+    flags |= f;
+  }
+  return flags;
+}
+
+/*
+ * [S] merge of S partial states per row in log-sum-exp form:
+ * M = max lse_s, w_s = e^(lse_s - M), out = sum w_s o_s / sum w_s,
+ * lse = M + ln sum w_s; all -inf => out 0, lse -inf.
+ */
+void oracle_split_merge(int64_t nrows, int64_t max_splits, int64_t D, const double* o_part,
+                        const double* lse_part, double* out, double* lse) {
+  for (int64_t i = 0; i < nrows; ++i) {
+    double M = -INFINITY;
+    for (int64_t sp = 0; sp < max_splits; ++sp)
+      if (lse_part[i * max_splits + sp] > M) M = lse_part[i * max_splits + sp];
+    for (int64_t d = 0; d < D; ++d) out[i * D + d] = 0.0;
+    if (M == -INFINITY) {
+      lse[i] = -INFINITY;
+      continue;
+    }
+    double wsum = 0.0;
+    for (int64_t sp = 0; sp < max_splits; ++sp) {
+      double ls = lse_part[i * max_splits + sp];
+      if (ls == -INFINITY) continue;
+      double w = exp(ls - M);
+      wsum += w;
+      for (int64_t d = 0; d < D; ++d) out[i * D + d] += w * o_part[(i * max_splits + sp) * D + d];
+    }
+    for (int64_t d = 0; d < D; ++d) out[i * D + d] /= wsum;
+    lse[i] = M + log(wsum);
+  }
+}
+
+/* ================================================================== */
+/* Tiered decode: int8 cold pages + f16 hot ring                      */
+/* ================================================================== */
+typedef struct {
+  int64_t B, Hq, Hkv, D, block_size, max_blocks, num_blocks;
+  double scale, softcap;
+  int64_t window, causal;
+  int64_t hot_window, hot_capacity;
+  const float* q;             /* [B, Hq, D] */
+  const uint16_t* k_hot;      /* [B, cap, Hkv, D] f16 bits */
+  const uint16_t* v_hot;
+  const uint32_t* k_cold;     /* [NB, bs, Hkv, D/4] */
+  const uint32_t* v_cold;
+  const uint16_t* k_scale;    /* [NB, bs, Hkv] f16 bits */
+  const uint16_t* v_scale;
+  const int32_t* block_table; /* [B, max_blocks] (cold pages) */
+  const int32_t* cold_lens;   /* [B] */
+  const int32_t* hot_lens;    /* [B] */
+  const int32_t* hot_starts;  /* [B] */
+  const int32_t* q_pos;       /* [B] or NULL */
+} oracle_tiered_args;
+
+/* A visible key of the tiered cache: cold (page row) or hot (ring row). */
+typedef struct {
+  int is_hot;
+  int64_t row; /* cold: blk*bs + off; hot: b*cap + slot */
+} tiered_key;
+
+typedef struct {
+  const oracle_tiered_args* a;
+  const tiered_key* keys;
+  int64_t kv;
+} tiered_vctx;
+
+/* [T] read_cold_v / hot V read for key i, dequantised to double. */
+static void tiered_fetch_v(const void* ctx, int64_t i, double* v) {
+  const tiered_vctx* c = (const tiered_vctx*)ctx;
+  const oracle_tiered_args* a = c->a;
+  const int64_t D = a->D;
+  tiered_key k = c->keys[i];
+  if (k.is_hot) {
+    const uint16_t* row = a->v_hot + (k.row * a->Hkv + c->kv) * D;
+    for (int64_t d = 0; d < D; ++d) v[d] = oracle_half_to_double(row[d]);
+  } else {
+    const uint32_t* words = a->v_cold + (k.row * a->Hkv + c->kv) * (D / 4);
+    double sc = oracle_half_to_double(a->v_scale[k.row * a->Hkv + c->kv]);
+    for (int64_t w = 0; w < D / 4; ++w) {
+      int32_t vals[4];
+      oracle_unpack_int8_word(words[w], vals);
+      for (int lane = 0; lane < 4; ++lane) v[4 * w + lane] = (double)vals[lane] * sc;
+    }
+  }
+}
+
+static void tiered_row(const oracle_tiered_args* a, int64_t b, int64_t h, double* out,
+                       double* lse, int32_t* flags) {
+  const int64_t D = a->D;
+  const int64_t G = a->Hq / a->Hkv;
+  const int64_t kv = h / G;
+  const double scale = effective_scale(a->scale, D);
+  int64_t cold_len = a->cold_lens[b];
+  int64_t hot_len = a->hot_lens[b];
+  int64_t hot_start = a->hot_starts[b];
+  if (cold_len < 0) {
+    *flags |= ORACLE_FLAG_BAD_TIER;
+    cold_len = 0;
+  }
+  if (cold_len > a->max_blocks * a->block_size) {
+    *flags |= ORACLE_FLAG_BAD_SEQ_LEN;
+    cold_len = a->max_blocks * a->block_size;
+  }
+  int64_t hot_limit = a->hot_window > 0 ? a->hot_window : a->hot_capacity;
+  if (hot_len < 0) {
+    *flags |= ORACLE_FLAG_BAD_TIER;
+    hot_len = 0;
+  }
+  if (hot_len > hot_limit) {
+    *flags |= ORACLE_FLAG_BAD_TIER;
+    hot_len = hot_limit;
+  }
+  if (hot_start < 0) {
+    *flags |= ORACLE_FLAG_BAD_TIER;
+    hot_start = 0;
+  }
+  int64_t qpos = hot_len > 0 ? hot_start + hot_len - 1 : cold_len - 1;
+  int empty = 0;
+  if (a->q_pos) {
+    qpos = a->q_pos[b];
+    if (qpos < 0) {
+      *flags |= ORACLE_FLAG_BAD_QPOS;
+      empty = 1;
+    }
+  }
+  int64_t n_max = cold_len + hot_len;
+  double* s = (double*)malloc(sizeof(double) * (size_t)(n_max + 1));
+  tiered_key* keys = (tiered_key*)malloc(sizeof(tiered_key) * (size_t)(n_max + 1));
+  double* vbuf = (double*)malloc(sizeof(double) * (size_t)D);
+  const float* qrow = a->q + (b * a->Hq + h) * D;
+  int64_t n = 0;
+  /* cold keys, absolute position t */
+  for (int64_t t = 0; t < cold_len && !empty; ++t) {
+    if (!key_visible(t, qpos, a->causal, a->window)) continue;
+    int64_t blk = a->block_table[b * a->max_blocks + t / a->block_size];
+    if (blk < 0 || blk >= a->num_blocks) {
+      *flags |= ORACLE_FLAG_BAD_BLOCK;
+      continue;
+    }
+    int64_t row = blk * a->block_size + t % a->block_size;
+    const uint32_t* words = a->k_cold + (row * a->Hkv + kv) * (D / 4);
+    double sc = oracle_half_to_double(a->k_scale[row * a->Hkv + kv]);
+    double dot = 0.0;
+    for (int64_t w = 0; w < D / 4; ++w) {
+      int32_t vals[4];
+      oracle_unpack_int8_word(words[w], vals);
+      for (int lane = 0; lane < 4; ++lane)
+        dot += (double)qrow[4 * w + lane] * ((double)vals[lane] * sc);
+    }
+    s[n] = apply_softcap(scale * dot, a->softcap);
+    keys[n].is_hot = 0;
+    keys[n].row = row;
+    ++n;
+  }
+  /* hot keys, absolute position hot_start + j, ring slot per get_hot_pos */
+  for (int64_t j = 0; j < hot_len && !empty; ++j) {
+    int64_t pos = hot_start + j;
+    if (!key_visible(pos, qpos, a->causal, a->window)) continue;
+    int64_t slot = a->hot_window > 0 ? pos % a->hot_window : j;
+    int64_t row = b * a->hot_capacity + slot;
+    const uint16_t* krow = a->k_hot + (row * a->Hkv + kv) * D;
+    double dot = 0.0;
+    for (int64_t d = 0; d < D; ++d) dot += (double)qrow[d] * oracle_half_to_double(krow[d]);
+    s[n] = apply_softcap(scale * dot, a->softcap);
+    keys[n].is_hot = 1;
+    keys[n].row = row;
+    ++n;
+  }
+  tiered_vctx ctx = {a, keys, kv};
+  softmax_two_pass(s, n, D, tiered_fetch_v, &ctx, vbuf, out, lse);
+  free(s);
+  free(keys);
+  free(vbuf);
+}
+
+int32_t oracle_decode_tiered(const oracle_tiered_args* a, const int64_t* rows, int64_t nrows,
+                             double* out, double* lse) {
+  int32_t flags = 0;
+  if (!rows) nrows = a->B * a->Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : flags)
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t r = rows ? rows[i] : i;
+    int64_t b = r / a->Hq, h = r % a->Hq;
+    int32_t f = 0;
+    tiered_row(a, b, h, out + i * a->D, lse + i, &f);
+    flags |= f;
+  }
+  return flags;
+}
+
+/* Threads the OpenMP runtime will use (reported beside timings). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,56 @@
+"""Algorithmic byte counts of one decode step (the roofline numerator).
+
+Counts what the method must move: the visible K/V rows (int8 words plus
+their scales for the cold tier), the block-table entries of the pages those
+rows sit in, Q, out, lse and the length arrays.  Masked pages, unused pool
+pages and split-KV partials are not counted.
+"""
+from __future__ import annotations
+
+from .workloads import PagedCase, TieredCase
+
+
+def visible_range(L: int, qpos: int, causal: bool, window: int):
+    """[lo, hi) of absolute key positions a query at qpos sees among keys
+    0..L-1 (causal and sliding-window masks)."""
+    hi = min(L, qpos + 1) if causal else L
+    lo = qpos - window + 1 if (window > 0 and qpos >= window) else 0
+    return max(lo, 0), max(hi, 0)
+
+
+def algorithmic_bytes(case) -> dict:
+    """Bytes the decode step must read and write: visible K/V rows (int8 words
+    and their scales for the cold tier), the block-table entries of the
+    visible pages, Q, out, lse and the length arrays."""
+    if isinstance(case, PagedCase):
+        kv = 0
+        bt = 0
+        for b in range(case.B):
+            L = int(case.seq_lens[b])
+            qp = int(case.q_pos[b]) if case.q_pos is not None else L - 1
+            lo, hi = visible_range(L, qp, case.causal, case.sliding_window)
+            n = max(0, hi - lo)
+            kv += n * case.Hkv * case.D * 2 * 2
+            if n:
+                bs = case.block_size
+                bt += ((hi - 1) // bs - lo // bs + 1) * 4
+        io = case.B * case.Hq * case.D * 4 * 2 + case.B * case.Hq * 4 + case.B * 4
+        return dict(kv=kv, table=bt, io=io, total=kv + bt + io)
+    kv = 0
+    bt = 0
+    for b in range(case.B):
+        cl, hl, hs = int(case.cold_lens[b]), int(case.hot_lens[b]), int(case.hot_starts[b])
+        qp = int(case.q_pos[b]) if case.q_pos is not None else (hs + hl - 1 if hl > 0 else cl - 1)
+        lo, hi = visible_range(cl, qp, case.causal, case.sliding_window)
+        nc = max(0, hi - lo)
+        kv += nc * case.Hkv * (case.D * 2 + 2 * 2)
+        if nc:
+            bt += ((hi - 1) // case.block_size - lo // case.block_size + 1) * 4
+        for j in range(hl):
+            pos = hs + j
+            if (not case.causal or pos <= qp) and not (
+                    case.sliding_window > 0 and qp >= case.sliding_window
+                    and pos < qp - case.sliding_window + 1):
+                kv += case.Hkv * case.D * 2 * 2
+    io = case.B * case.Hq * case.D * 4 * 2 + case.B * case.Hq * 4 + case.B * 4 * 3
+    return dict(kv=kv, table=bt, io=io, total=kv + bt + io)

@@ -1,0 +1,503 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each test checks the oracle against something the pages or the mathematics
+fix independently of the oracle's code: hand-decoded formats, hand-worked
+tiny cases, library routines (numpy's binary16 decoder, torch's float64
+scaled_dot_product_attention, scipy's logsumexp), closed forms, and
+invariances of the definition.  Together they are meant to catch a dropped
+term, a wrong sign or index, or a transposed operand anywhere in the oracle.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# helpers: tiny caches laid out by hand (no attention arithmetic here)
+# ---------------------------------------------------------------------------
+
+def paged_from_dense(k, v, bs, rng=None, extra_pages=0):
+    """Place dense K/V [B, L, Hkv, D] into a pool [NB, bs, Hkv, D] through a
+    block table, optionally with shuffled page ids and unused pages."""
+    B, L, H, D = k.shape
+    npg = (L + bs - 1) // bs
+    NB = B * npg + extra_pages
+    ids = np.arange(NB) if rng is None else rng.permutation(NB)
+    table = ids[:B * npg].reshape(B, npg).astype(np.int32)
+    kp = np.zeros((NB, bs, H, D), np.float16)
+    vp = np.zeros((NB, bs, H, D), np.float16)
+    for b in range(B):
+        for t in range(L):
+            kp[table[b, t // bs], t % bs] = k[b, t]
+            vp[table[b, t // bs], t % bs] = v[b, t]
+    return kp, vp, table
+
+
+def rand_dense(rng, B, L, Hkv, D, scale=1.0):
+    k = (rng.standard_normal((B, L, Hkv, D)) * scale).astype(np.float16)
+    v = (rng.standard_normal((B, L, Hkv, D)) * scale).astype(np.float16)
+    return k, v
+
+
+# ---------------------------------------------------------------------------
+# formats
+# ---------------------------------------------------------------------------
+
+def test_half_decoder_matches_numpy_for_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # sign of zero
+    assert math.copysign(1.0, got[0x8000]) == -1.0
+
+
+def test_half_decoder_golden():
+    n = 0
+    with open(os.path.join(GOLDEN, "f16_bits.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            bits, val = line.split()
+            want = float(val)
+            got = oracle.half_to_double(int(bits, 16))
+            assert got == want, (bits, got, want)
+            if want == 0.0:
+                assert math.copysign(1.0, got) == math.copysign(1.0, want)
+            n += 1
+    assert n >= 16
+
+
+def test_int8_word_decode_golden():
+    n = 0
+    with open(os.path.join(GOLDEN, "int8_words.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            word, *vals = line.split()
+            assert oracle.unpack_int8_word(int(word, 16)) == [int(x) for x in vals], word
+            n += 1
+    assert n >= 10
+
+
+# ---------------------------------------------------------------------------
+# hand-worked cases
+# ---------------------------------------------------------------------------
+
+def _eval(expr):
+    ns = {"e": math.e, "exp": math.exp, "log": math.log, "tanh": math.tanh, "inf": math.inf}
+    return float(eval(expr, {"__builtins__": {}}, ns))
+
+
+def _hand_cases():
+    with open(os.path.join(GOLDEN, "hand_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _hand_cases(), ids=lambda c: c["name"])
+def test_hand_worked_cases(case):
+    D, bs = case["D"], case["block_size"]
+    k = np.array(case["k"], dtype=np.float16).reshape(1, -1, 1, D)
+    v = np.array(case["v"], dtype=np.float16).reshape(1, -1, 1, D)
+    kp, vp, table = paged_from_dense(k, v, bs)
+    q = np.array(case["q"], dtype=np.float32).reshape(1, 1, D)
+    q_pos = None if case["q_pos"] is None else np.array([case["q_pos"]], np.int32)
+    out, lse, flags = oracle.decode_paged(
+        q, kp, vp, table, np.array([case["seq_len"]], np.int32), q_pos,
+        scale=case["scale"], softcap=case["softcap"], sliding_window=case["window"],
+        causal=bool(case["causal"]))
+    assert flags == 0
+    want_out = np.array([_eval(x) for x in case["out"]])
+    want_lse = _eval(case["lse"])
+    np.testing.assert_allclose(out[0], want_out, rtol=1e-14, atol=1e-15)
+    if math.isinf(want_lse):
+        assert lse[0] == want_lse
+    else:
+        assert abs(lse[0] - want_lse) < 1e-14
+
+
+# ---------------------------------------------------------------------------
+# library routines: torch float64 SDPA and scipy logsumexp on the dense cache
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed,B,Hq,Hkv,D,bs,window,causal", [
+    (0, 2, 4, 2, 16, 4, 0, True),
+    (1, 3, 8, 2, 32, 8, 0, False),
+    (2, 2, 6, 3, 8, 2, 5, True),
+    (3, 1, 4, 4, 64, 16, 17, True),
+    (4, 2, 8, 1, 24, 8, 3, False),
+])
+def test_matches_torch_sdpa_float64(seed, B, Hq, Hkv, D, bs, window, causal):
+    torch = pytest.importorskip("torch")
+    from scipy.special import logsumexp
+
+    rng = np.random.default_rng(seed)
+    Lmax = 37
+    lens = rng.integers(1, Lmax + 1, size=B).astype(np.int32)
+    k, v = rand_dense(rng, B, Lmax, Hkv, D)
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng, extra_pages=3)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    qpos = np.array([rng.integers(0, L) if causal else rng.integers(0, Lmax) for L in lens],
+                    dtype=np.int32)
+    scale = np.float32(1.0 / math.sqrt(D))
+    out, lse, flags = oracle.decode_paged(q, kp, vp, table, lens, qpos, scale=float(scale),
+                                          sliding_window=window, causal=causal)
+    assert flags == 0
+    G = Hq // Hkv
+    for b in range(B):
+        L = int(lens[b])
+        p = int(qpos[b])
+        t = np.arange(L)
+        vis = np.ones(L, bool)
+        if causal:
+            vis &= t <= p
+        if window > 0 and p >= window:
+            vis &= t >= p - window + 1
+        Kd = torch.from_numpy(k[b, :L].astype(np.float64)).permute(1, 0, 2)  # [Hkv, L, D]
+        Vd = torch.from_numpy(v[b, :L].astype(np.float64)).permute(1, 0, 2)
+        Kd = Kd.repeat_interleave(G, dim=0)
+        Vd = Vd.repeat_interleave(G, dim=0)
+        Qd = torch.from_numpy(q[b].astype(np.float64)).unsqueeze(1)  # [Hq, 1, D]
+        mask = torch.from_numpy(vis).view(1, 1, L).expand(Hq, 1, L)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            Qd, Kd, Vd, attn_mask=mask, scale=float(scale))[:, 0, :].numpy()
+        scores = (Qd @ Kd.transpose(1, 2))[:, 0, :].numpy() * float(scale)
+        ref_lse = logsumexp(np.where(vis[None, :], scores, -np.inf), axis=1)
+        np.testing.assert_allclose(out[b * Hq:(b + 1) * Hq], ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[b * Hq:(b + 1) * Hq], ref_lse, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+# ---------------------------------------------------------------------------
+
+def test_single_visible_key_returns_its_value_row():
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, D, bs, L = 2, 4, 2, 16, 4, 11
+    k, v = rand_dense(rng, B, L, Hkv, D)
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    out, lse, _ = oracle.decode_paged(q, kp, vp, table, np.full(B, L, np.int32),
+                                      scale=0.25, sliding_window=1)
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // (Hq // Hkv)
+            assert np.array_equal(out[b * Hq + h], v[b, L - 1, kv].astype(np.float64))
+            s = 0.25 * float(np.dot(q[b, h].astype(np.float64), k[b, L - 1, kv].astype(np.float64)))
+            assert abs(lse[b * Hq + h] - s) < 1e-12
+
+
+def test_constant_value_rows_return_the_constant():
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, D, bs, L = 1, 4, 1, 8, 4, 29
+    k, _ = rand_dense(rng, B, L, Hkv, D)
+    v = np.broadcast_to(np.arange(D, dtype=np.float16) - 3, (B, L, Hkv, D)).copy()
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32) * 3
+    out, _, _ = oracle.decode_paged(q, kp, vp, table, np.array([L], np.int32))
+    np.testing.assert_allclose(out, np.broadcast_to(np.arange(D) - 3.0, out.shape), atol=1e-13)
+
+
+def test_zero_keys_give_log_count_and_mean_value():
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, D, bs = 3, 2, 1, 8, 4
+    lens = np.array([1, 7, 23], np.int32)
+    k = np.zeros((B, 23, Hkv, D), np.float16)
+    _, v = rand_dense(rng, B, 23, Hkv, D)
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    out, lse, _ = oracle.decode_paged(q, kp, vp, table, lens, sliding_window=5)
+    for b in range(B):
+        n = min(int(lens[b]), 5)
+        for h in range(Hq):
+            assert abs(lse[b * Hq + h] - math.log(n)) < 1e-14
+            want = v[b, lens[b] - n:lens[b], 0].astype(np.float64).mean(axis=0)
+            np.testing.assert_allclose(out[b * Hq + h], want, atol=1e-14)
+
+
+def test_softcap_saturation_closed_form():
+    # cap = 1 and |q.k| huge: every score becomes +-1 (tanh saturates).
+    D, bs = 4, 2
+    k = np.array([[100, 0, 0, 0], [-100, 0, 0, 0], [100, 0, 0, 0]], np.float16).reshape(1, 3, 1, D)
+    v = np.array([[1, 0, 0, 0], [0, 1, 0, 0], [0, 0, 1, 0]], np.float16).reshape(1, 3, 1, D)
+    kp, vp, table = paged_from_dense(k, v, bs)
+    q = np.array([[[100, 0, 0, 0]]], np.float32)
+    out, lse, _ = oracle.decode_paged(q, kp, vp, table, np.array([3], np.int32), scale=1.0,
+                                      softcap=1.0)
+    Z = 2 * math.e + math.exp(-1)
+    np.testing.assert_allclose(out[0], [math.e / Z, math.exp(-1) / Z, math.e / Z, 0], atol=1e-15)
+    assert abs(lse[0] - math.log(Z)) < 1e-14
+
+
+# ---------------------------------------------------------------------------
+# invariances of the definition
+# ---------------------------------------------------------------------------
+
+def test_block_permutation_invariance_is_bitwise():
+    rng = np.random.default_rng(8)
+    B, Hq, Hkv, D, bs, L = 2, 4, 2, 16, 4, 30
+    k, v = rand_dense(rng, B, L, Hkv, D)
+    kp, vp, table = paged_from_dense(k, v, bs, extra_pages=4)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    lens = np.array([30, 13], np.int32)
+    a = oracle.decode_paged(q, kp, vp, table, lens, softcap=7.0)
+    perm = rng.permutation(kp.shape[0])          # new id of old page i is perm[i]
+    kp2 = np.empty_like(kp)
+    vp2 = np.empty_like(vp)
+    kp2[perm] = kp
+    vp2[perm] = vp
+    table2 = perm[table].astype(np.int32)
+    b_ = oracle.decode_paged(q, kp2, vp2, table2, lens, softcap=7.0)
+    assert np.array_equal(a[0], b_[0]) and np.array_equal(a[1], b_[1])
+
+
+def test_sliding_window_equals_truncated_dense_cache():
+    rng = np.random.default_rng(9)
+    B, Hq, Hkv, D, bs, L, W = 2, 4, 2, 16, 4, 41, 9
+    k, v = rand_dense(rng, B, L, Hkv, D)
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    a_out, a_lse, _ = oracle.decode_paged(q, kp, vp, table, np.full(B, L, np.int32),
+                                          sliding_window=W)
+    kt, vt = k[:, L - W:], v[:, L - W:]
+    kp2, vp2, table2 = paged_from_dense(kt, vt, bs)
+    b_out, b_lse, _ = oracle.decode_paged(q, kp2, vp2, table2, np.full(B, W, np.int32))
+    assert np.array_equal(a_out, b_out) and np.array_equal(a_lse, b_lse)
+
+
+def test_huge_softcap_equals_no_softcap():
+    rng = np.random.default_rng(10)
+    B, Hq, Hkv, D, bs, L = 2, 4, 2, 32, 8, 50
+    k, v = rand_dense(rng, B, L, Hkv, D)
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    a = oracle.decode_paged(q, kp, vp, table, np.full(B, L, np.int32))
+    b_ = oracle.decode_paged(q, kp, vp, table, np.full(B, L, np.int32), softcap=1e12)
+    np.testing.assert_allclose(a[0], b_[0], atol=1e-12)
+    np.testing.assert_allclose(a[1], b_[1], atol=1e-12)
+    c = oracle.decode_paged(q, kp, vp, table, np.full(B, L, np.int32), softcap=0.5)
+    assert np.abs(c[1] - a[1]).max() > 1e-3   # a small cap does change the result
+
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, D, bs, L = 2, 8, 2, 16, 4, 21
+    G = Hq // Hkv
+    k, v = rand_dense(rng, B, L, Hkv, D)
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    a = oracle.decode_paged(q, kp, vp, table, np.full(B, L, np.int32), softcap=3.0)
+    k2 = np.repeat(k, G, axis=2)
+    v2 = np.repeat(v, G, axis=2)
+    kp2, vp2, table2 = paged_from_dense(k2, v2, bs, rng=rng)
+    b_ = oracle.decode_paged(q, kp2, vp2, table2, np.full(B, L, np.int32), softcap=3.0)
+    assert np.array_equal(a[0], b_[0]) and np.array_equal(a[1], b_[1])
+
+
+@pytest.mark.parametrize("split_tokens", [4, 8, 16, 64])
+def test_split_merge_equals_unsplit(split_tokens):
+    rng = np.random.default_rng(12)
+    B, Hq, Hkv, D, bs = 3, 4, 2, 16, 4
+    lens = np.array([0, 19, 57], np.int32)
+    k, v = rand_dense(rng, B, 57, Hkv, D, scale=2.0)
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    S = (57 + split_tokens - 1) // split_tokens
+    out, lse, _ = oracle.decode_paged(q, kp, vp, table, lens, sliding_window=40)
+    op, lp, flags = oracle.decode_paged_split(q, kp, vp, table, lens, split_tokens=split_tokens,
+                                              max_splits=S, sliding_window=40)
+    assert flags == 0
+    mo, ml = oracle.split_merge(op, lp)
+    np.testing.assert_allclose(mo, out, atol=1e-12)
+    np.testing.assert_allclose(ml, lse, atol=1e-12)
+
+
+def test_split_overflow_flag():
+    rng = np.random.default_rng(13)
+    k, v = rand_dense(rng, 1, 40, 1, 8)
+    kp, vp, table = paged_from_dense(k, v, 4)
+    q = rng.standard_normal((1, 1, 8)).astype(np.float32)
+    _, _, flags = oracle.decode_paged_split(q, kp, vp, table, np.array([40], np.int32),
+                                            split_tokens=8, max_splits=4)
+    assert flags & oracle.FLAG_SPLIT_OVERFLOW
+
+
+# ---------------------------------------------------------------------------
+# tiered cache
+# ---------------------------------------------------------------------------
+
+def _tiered_from_dense(kc_int, vc_int, ks, vs, kh, vh, bs, hot_window, hot_start, rng=None):
+    """Cold int8 values [B, C, H, D] with f16 scales [B, C, H] into pages; hot
+    rows [B, Hl, H, D] into the ring at slot (hot_start + j) % W."""
+    B, C, H, D = kc_int.shape
+    npg = max(1, (C + bs - 1) // bs)
+    NB = B * npg
+    ids = np.arange(NB) if rng is None else rng.permutation(NB)
+    table = ids.reshape(B, npg).astype(np.int32)
+    words_k = np.zeros((NB, bs, H, D // 4), np.uint32)
+    words_v = np.zeros_like(words_k)
+    sk = np.zeros((NB, bs, H), np.float16)
+    sv = np.zeros_like(sk)
+    def pack(x):
+        u = x.astype(np.int8).view(np.uint8).astype(np.uint32).reshape(-1, 4)
+        return u[:, 0] | (u[:, 1] << 8) | (u[:, 2] << 16) | (u[:, 3] << 24)
+    for b in range(B):
+        for t in range(C):
+            for h in range(H):
+                words_k[table[b, t // bs], t % bs, h] = pack(kc_int[b, t, h])
+                words_v[table[b, t // bs], t % bs, h] = pack(vc_int[b, t, h])
+                sk[table[b, t // bs], t % bs, h] = ks[b, t, h]
+                sv[table[b, t // bs], t % bs, h] = vs[b, t, h]
+    Hl = kh.shape[1]
+    cap = max(hot_window, Hl, 1)
+    hk = np.zeros((B, cap, H, D), np.float16)
+    hv = np.zeros_like(hk)
+    for j in range(Hl):
+        slot = (hot_start + j) % hot_window if hot_window > 0 else j
+        hk[:, slot] = kh[:, j]
+        hv[:, slot] = vh[:, j]
+    return hk, hv, words_k, words_v, sk, sv, table
+
+
+def test_int8_tier_with_unit_scales_equals_f16_paged_bitwise():
+    rng = np.random.default_rng(14)
+    B, Hq, H, D, bs, C = 2, 4, 2, 16, 4, 22
+    kc = rng.integers(-127, 128, size=(B, C, H, D))
+    vc = rng.integers(-127, 128, size=(B, C, H, D))
+    ones = np.ones((B, C, H), np.float16)
+    empty = np.zeros((B, 0, H, D), np.float16)
+    hk, hv, wk, wv, sk, sv, table = _tiered_from_dense(kc, vc, ones, ones, empty, empty, bs,
+                                                       hot_window=0, hot_start=C, rng=rng)
+    q = (rng.standard_normal((B, Hq, D)) * 0.05).astype(np.float32)
+    a = oracle.decode_tiered(q, hk, hv, wk, wv, sk, sv, table, C, 0, C, hot_window=0,
+                             softcap=30.0)
+    kp, vp, table2 = paged_from_dense(kc.astype(np.float16), vc.astype(np.float16), bs, rng=rng)
+    b_ = oracle.decode_paged(q, kp, vp, table2, np.full(B, C, np.int32), softcap=30.0)
+    assert a[2] == 0 and b_[2] == 0
+    assert np.array_equal(a[0], b_[0]) and np.array_equal(a[1], b_[1])
+
+
+def test_int8_scales_multiply_each_value():
+    # one cold key: out must be int8 * v_scale; lse = scale * sum q_d int8_d * k_scale
+    D = 8
+    kc = np.array([[[[1, -2, 3, -4, 127, -128, 0, 5]]]])
+    vc = np.array([[[[-1, 2, -3, 4, -127, 127, 9, 0]]]])
+    ks = np.array([[[0.5]]], np.float16)
+    vs = np.array([[[0.25]]], np.float16)
+    empty = np.zeros((1, 0, 1, D), np.float16)
+    hk, hv, wk, wv, sk, sv, table = _tiered_from_dense(kc, vc, ks, vs, empty, empty, 16, 0, 1)
+    q = np.arange(D, dtype=np.float32).reshape(1, 1, D)
+    out, lse, _ = oracle.decode_tiered(q, hk, hv, wk, wv, sk, sv, table, 1, 0, 1, hot_window=0,
+                                       scale=1.0)
+    np.testing.assert_array_equal(out[0], vc[0, 0, 0] * 0.25)
+    assert lse[0] == float(np.dot(np.arange(D), kc[0, 0, 0]) * 0.5)
+
+
+def test_tiered_equals_dense_attention_over_logical_order():
+    """Cold + hot keys against a dense f16 cache holding the dequantised cold
+    rows followed by the hot rows (positions contiguous)."""
+    rng = np.random.default_rng(15)
+    B, Hq, H, D, bs, C, Hl, W = 2, 4, 2, 16, 4, 13, 6, 8
+    kc = rng.integers(-127, 128, size=(B, C, H, D))
+    vc = rng.integers(-127, 128, size=(B, C, H, D))
+    ks = (rng.random((B, C, H)) * 0.05 + 0.001).astype(np.float16)
+    vs = (rng.random((B, C, H)) * 0.05 + 0.001).astype(np.float16)
+    kh, vh = rand_dense(rng, B, Hl, H, D)
+    hk, hv, wk, wv, sk, sv, table = _tiered_from_dense(kc, vc, ks, vs, kh, vh, bs, W, C, rng=rng)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    a_out, a_lse, flags = oracle.decode_tiered(q, hk, hv, wk, wv, sk, sv, table, C, Hl, C,
+                                               hot_window=W, softcap=20.0, sliding_window=15)
+    assert flags == 0
+    # dense reference in float64 through scipy
+    from scipy.special import logsumexp
+    G = Hq // H
+    kd = np.concatenate([kc * ks[..., None].astype(np.float64), kh.astype(np.float64)], axis=1)
+    vd = np.concatenate([vc * vs[..., None].astype(np.float64), vh.astype(np.float64)], axis=1)
+    L = C + Hl
+    vis = np.arange(L) >= L - 15
+    scale = float(np.float32(1 / math.sqrt(D)))
+    for b in range(B):
+        for h in range(Hq):
+            s = kd[b, :, h // G] @ q[b, h].astype(np.float64) * scale
+            s = 20.0 * np.tanh(s / 20.0)
+            s = np.where(vis, s, -np.inf)
+            lse = logsumexp(s)
+            w = np.exp(s - lse)
+            np.testing.assert_allclose(a_out[b * Hq + h], w @ vd[b, :, h // G], atol=1e-12)
+            assert abs(a_lse[b * Hq + h] - lse) < 1e-12
+
+
+def test_hot_ring_rotation_invariance():
+    """The same hot keys stored at a different ring phase (hot_start not a
+    multiple of the window) give bit-identical results."""
+    rng = np.random.default_rng(16)
+    B, Hq, H, D, bs, Hl, W = 1, 2, 1, 8, 4, 7, 10
+    kh, vh = rand_dense(rng, B, Hl, H, D)
+    zero_c = np.zeros((B, 0, H, D), np.int64)
+    zs = np.zeros((B, 0, H), np.float16)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    res = []
+    for hot_start in (0, 3, 13, 27):
+        hk, hv, wk, wv, sk, sv, table = _tiered_from_dense(zero_c, zero_c, zs, zs, kh, vh, bs, W,
+                                                           hot_start)
+        res.append(oracle.decode_tiered(q, hk, hv, wk, wv, sk, sv, table, 0, Hl, hot_start,
+                                        hot_window=W))
+    for r in res[1:]:
+        assert np.array_equal(r[0], res[0][0]) and np.array_equal(r[1], res[0][1])
+    # a wrong phase (reading slot j instead of (start+j)%W) would differ
+    hk, hv, wk, wv, sk, sv, table = _tiered_from_dense(zero_c, zero_c, zs, zs, kh, vh, bs, W, 3)
+    wrong = oracle.decode_tiered(q, hk, hv, wk, wv, sk, sv, table, 0, Hl, 0, hot_window=W)
+    assert not np.array_equal(wrong[0], res[0][0])
+
+
+# ---------------------------------------------------------------------------
+# device-visible error conventions (restated in the oracle)
+# ---------------------------------------------------------------------------
+
+def test_bad_block_id_masks_its_keys_and_flags():
+    rng = np.random.default_rng(17)
+    k, v = rand_dense(rng, 1, 12, 1, 8)
+    kp, vp, table = paged_from_dense(k, v, 4)
+    q = rng.standard_normal((1, 2, 8)).astype(np.float32)
+    bad = table.copy()
+    bad[0, 1] = 999
+    out, lse, flags = oracle.decode_paged(q, kp, vp, bad, np.array([12], np.int32))
+    assert flags & oracle.FLAG_BAD_BLOCK
+    # equals attention over keys 0-3 and 8-11 only
+    keep = np.r_[0:4, 8:12]
+    kp2, vp2, t2 = paged_from_dense(k[:, keep], v[:, keep], 4)
+    ref = oracle.decode_paged(q, kp2, vp2, t2, np.array([8], np.int32), causal=False)
+    np.testing.assert_array_equal(out, ref[0])
+
+
+def test_length_beyond_table_is_clamped_and_flagged():
+    rng = np.random.default_rng(18)
+    k, v = rand_dense(rng, 1, 8, 1, 8)
+    kp, vp, table = paged_from_dense(k, v, 4)
+    q = rng.standard_normal((1, 1, 8)).astype(np.float32)
+    a = oracle.decode_paged(q, kp, vp, table, np.array([100], np.int32), causal=False)
+    b_ = oracle.decode_paged(q, kp, vp, table, np.array([8], np.int32), causal=False)
+    assert a[2] & oracle.FLAG_BAD_SEQ_LEN and b_[2] == 0
+    np.testing.assert_array_equal(a[0], b_[0])
+
+
+def test_negative_qpos_gives_empty_row():
+    rng = np.random.default_rng(19)
+    k, v = rand_dense(rng, 1, 8, 1, 8)
+    kp, vp, table = paged_from_dense(k, v, 4)
+    q = rng.standard_normal((1, 1, 8)).astype(np.float32)
+    out, lse, flags = oracle.decode_paged(q, kp, vp, table, np.array([8], np.int32),
+                                          np.array([-3], np.int32))
+    assert flags & oracle.FLAG_BAD_QPOS
+    assert not out.any() and lse[0] == -np.inf
