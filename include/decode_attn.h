@@ -54,8 +54,9 @@
  *       lse          f32  [B, Hq] or NULL (not written)
  *   - A sequence with no visible key (seq_len 0) gets out = 0, lse = -inf.
  *   - Supported sizes: head_dim in {64, 128, 256}; num_q_heads a multiple of
- *     num_kv_heads; block_size a power of two in [8, 256]; every pointer
- *     16-byte aligned.  Other sizes return DA_ERR_UNSUPPORTED.
+ *     num_kv_heads with G = Hq/Hkv <= 8 or a multiple of 8; block_size a
+ *     power of two in [8, 256]; tensor pointers 16-byte aligned (index
+ *     arrays 4-byte aligned).  Other sizes return DA_ERR_UNSUPPORTED.
  */
 #ifndef DECODE_ATTN_H
 #define DECODE_ATTN_H

@@ -1,0 +1,460 @@
+// api.cu — the C ABI of libdecode_attn.so (declared in include/decode_attn.h):
+// argument validation, TMA tensor-map encoding, schedule and stage sizing,
+// batch chunking, and the kernel launches.  Host code only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/decode_attn.h"
+#include "kernel_params.h"
+#include "launch.h"
+
+namespace {
+
+using da::KParams;
+using da::SmemLayout;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 128;
+
+int device_sms(int* sms_out) {
+  static int sms[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DA_ERR_CUDA;
+  if (sms[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return DA_ERR_CUDA;
+    sms[dev] = v;
+  }
+  *sms_out = sms[dev];
+  return DA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int ilog2(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+// Validation shared by every entry point that takes da_params.
+int check_params(const da_params* p, bool tiered) {
+  if (!p) return DA_ERR_INVALID;
+  if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0) return DA_ERR_INVALID;
+  if (p->num_q_heads % p->num_kv_heads != 0) return DA_ERR_INVALID;
+  {
+    // head groups of 8: a group size above 8 must split into whole groups
+    const int G = p->num_q_heads / p->num_kv_heads;
+    if (G > da::kHeadTile && G % da::kHeadTile != 0) return DA_ERR_UNSUPPORTED;
+  }
+  if (p->head_dim <= 0) return DA_ERR_INVALID;
+  if (tiered) {
+    if (p->head_dim != 128 && p->head_dim != 256) return DA_ERR_UNSUPPORTED;
+  } else {
+    if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return DA_ERR_UNSUPPORTED;
+  }
+  if (p->block_size <= 0 || p->max_blocks_per_seq <= 0 || p->num_blocks <= 0)
+    return DA_ERR_INVALID;
+  if (!pow2(p->block_size) || p->block_size < 8 || p->block_size > 256) return DA_ERR_UNSUPPORTED;
+  if ((long long)p->num_blocks * p->block_size > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
+  if ((long long)p->max_blocks_per_seq * p->block_size > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
+  if (!(p->scale >= 0.f) || isinf(p->scale)) return DA_ERR_INVALID;
+  if (!(p->softcap >= 0.f) || isinf(p->softcap)) return DA_ERR_INVALID;
+  if (p->sliding_window < 0) return DA_ERR_INVALID;
+  if (p->causal != 0 && p->causal != 1) return DA_ERR_INVALID;
+  if (p->max_seq_len < 0) return DA_ERR_INVALID;
+  return DA_OK;
+}
+
+// 1/sqrt(D) rounded to f32 when scale is 0, then times log2(e) (the kernels
+// keep scores in base-2 units).
+float effective_qscale(const da_params* p) {
+  const double s = p->scale > 0.f ? (double)p->scale : (double)(float)(1.0 / sqrt((double)p->head_dim));
+  return (float)s * 1.4426950408889634f;
+}
+
+void fill_common(KParams& k, const da_params* p) {
+  k.B = p->batch;
+  k.Hq = p->num_q_heads;
+  k.Hkv = p->num_kv_heads;
+  k.D = p->head_dim;
+  k.G = p->num_q_heads / p->num_kv_heads;
+  k.NH = k.G < da::kHeadTile ? k.G : da::kHeadTile;
+  k.HG = (k.G + da::kHeadTile - 1) / da::kHeadTile;
+  k.bs = p->block_size;
+  k.log2_bs = ilog2(p->block_size);
+  k.max_blocks = p->max_blocks_per_seq;
+  k.num_blocks = p->num_blocks;
+  k.qscale = effective_qscale(p);
+  k.softcap2 = p->softcap > 0.f ? p->softcap * 1.4426950408889634f : 0.f;
+  k.window = p->sliding_window;
+  k.causal = p->causal;
+}
+
+// 3-D map over a [rows, Hkv, inner] array (inner contiguous): box
+// {box_inner, 1, box_rows}, 128-byte swizzle.
+int encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
+                    long long inner, long long heads, long long rows, int box_inner,
+                    int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)(inner * elem_bytes), (cuuint64_t)(inner * heads * elem_bytes)};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, 1u, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
+// 4-D map over the hot ring [B, cap, Hkv, D] f16: box {64, 1, 64, 1}.
+int encode_ring_map(CUtensorMap* m, const void* base, long long D, long long heads, long long cap,
+                    long long B) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)cap, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)(D * 2), (cuuint64_t)(D * heads * 2),
+                           (cuuint64_t)(D * heads * cap * 2)};
+  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)da::kTile, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
+// Largest stage count that fits in shared memory (at least 2), or 0.
+int pick_stages(int kind, int D, int NH, int Hkv, int nplan, int* smem_out) {
+  for (int s = da::kMaxStages; s >= 2; --s) {
+    SmemLayout L = da::make_layout(kind, D, NH, Hkv, s, nplan);
+    if (L.total <= da::kSmemLimit) {
+      *smem_out = L.total;
+      return s;
+    }
+  }
+  return 0;
+}
+
+struct WsLayout {
+  size_t o_off, lse_off, cnt_off, total;
+};
+
+WsLayout ws_layout(int grid, int units, int D) {
+  WsLayout w;
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  w.o_off = 0;
+  w.lse_off = al((size_t)grid * 2 * da::kHeadTile * D * 4);
+  w.cnt_off = w.lse_off + al((size_t)grid * 2 * da::kHeadTile * 4);
+  w.total = w.cnt_off + al((size_t)units * 4);
+  return w;
+}
+
+int units_per_launch(const da_params* p) {
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const int HG = (G + da::kHeadTile - 1) / da::kHeadTile;
+  const int nb = p->batch < da::kMaxBatchPerLaunch ? p->batch : da::kMaxBatchPerLaunch;
+  return nb * p->num_kv_heads * HG;
+}
+
+struct Launch {
+  int kind;
+  const da_params* p;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+// Runs the decode kernel over the batch in chunks of kMaxBatchPerLaunch.
+// `base` holds every field except the per-chunk pointers, which
+// `offset_chunk` shifts.
+template <typename OffsetFn>
+int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStream_t stream) {
+  const da_params* p = lc.p;
+  int sms = 0;
+  int st = device_sms(&sms);
+  if (st != DA_OK) return st;
+  const bool use_ws = lc.workspace != nullptr;
+  if (use_ws) {
+    const size_t need = decode_attn_workspace_size(p);
+    if (lc.workspace_bytes < need) return DA_ERR_WORKSPACE;
+    if (!aligned(lc.workspace, 256)) return DA_ERR_INVALID;
+  } else if (lc.workspace_bytes != 0) {
+    return DA_ERR_INVALID;
+  }
+  const int grid_max = sms;
+  const WsLayout w = ws_layout(grid_max, units_per_launch(p), p->head_dim);
+  for (int b0 = 0; b0 < p->batch; b0 += da::kMaxBatchPerLaunch) {
+    const int nb = (p->batch - b0) < da::kMaxBatchPerLaunch ? (p->batch - b0)
+                                                             : da::kMaxBatchPerLaunch;
+    KParams k = base;
+    k.B = nb;
+    offset_chunk(k, b0);
+    const int units = nb * k.Hkv * k.HG;
+    int smem = 0;
+    k.stages = pick_stages(lc.kind, k.D, k.NH, k.Hkv, nb, &smem);
+    if (k.stages == 0) return DA_ERR_UNSUPPORTED;
+    int grid;
+    if (use_ws) {
+      k.sched = da::SCHED_STREAM;
+      grid = grid_max;
+      if (p->max_seq_len > 0) {
+        // never more CTAs than key tiles
+        const long long tiles = (long long)units * ((p->max_seq_len + da::kTile - 1) / da::kTile + 1);
+        if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
+      }
+      k.ws_o = reinterpret_cast<float*>(static_cast<char*>(lc.workspace) + w.o_off);
+      k.ws_lse = reinterpret_cast<float*>(static_cast<char*>(lc.workspace) + w.lse_off);
+      k.ws_cnt = reinterpret_cast<int*>(static_cast<char*>(lc.workspace) + w.cnt_off);
+    } else {
+      k.sched = da::SCHED_UNITS;
+      grid = units < 8 * sms ? units : 8 * sms;
+      if (grid < 1) grid = 1;
+    }
+    k.grid = grid;
+    cudaError_t e = da::launch_decode(lc.kind, k.D, k, dim3(grid), smem, stream);
+    if (e != cudaSuccess) return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* decode_attn_status_string(int status) {
+  switch (status) {
+    case DA_OK: return "ok";
+    case DA_ERR_INVALID: return "invalid argument";
+    case DA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DA_ERR_WORKSPACE: return "workspace too small";
+    case DA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+size_t decode_attn_workspace_size(const da_params* p) {
+  if (check_params(p, false) != DA_OK && check_params(p, true) != DA_OK) return 0;
+  int sms = 0;
+  if (device_sms(&sms) != DA_OK) return 0;
+  return ws_layout(sms, units_per_launch(p), p->head_dim).total;
+}
+
+int decode_attn_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (!workspace && bytes) return DA_ERR_INVALID;
+  if (!bytes) return DA_OK;
+  return cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DA_OK
+             : DA_ERR_CUDA;
+}
+
+int decode_attn_paged(const da_params* p, const float* q, const uint16_t* k_pool,
+                      const uint16_t* v_pool, const int32_t* block_table,
+                      const int32_t* seq_lens, const int32_t* q_pos, float* out, float* lse,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                      void* stream) {
+  int st = check_params(p, false);
+  if (st != DA_OK) return st;
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out) return DA_ERR_INVALID;
+  if (!workspace && workspace_bytes) return DA_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || (q_pos && !aligned(q_pos, 4)) ||
+      (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
+    return DA_ERR_INVALID;
+  if (p->batch == 0) return DA_OK;
+  KParams k;
+  memset(&k, 0, sizeof(k));
+  fill_common(k, p);
+  const int rows_box = p->block_size < da::kTile ? p->block_size : da::kTile;
+  const long long rows = (long long)p->num_blocks * p->block_size;
+  st = encode_rows_map(&k.tm_k, k_pool, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p->head_dim,
+                       p->num_kv_heads, rows, 64, rows_box);
+  if (st != DA_OK) return st;
+  st = encode_rows_map(&k.tm_v, v_pool, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p->head_dim,
+                       p->num_kv_heads, rows, 64, rows_box);
+  if (st != DA_OK) return st;
+  k.dev_status = dev_status;
+  Launch lc{da::KIND_PAGED, p, workspace, workspace_bytes};
+  const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
+  auto off = [&](KParams& kk, int b0) {
+    kk.q = q + (long long)b0 * Hq * D;
+    kk.block_table = block_table + (long long)b0 * mb;
+    kk.seq_lens = seq_lens + b0;
+    kk.q_pos = q_pos ? q_pos + b0 : nullptr;
+    kk.out = out + (long long)b0 * Hq * D;
+    kk.lse = lse ? lse + (long long)b0 * Hq : nullptr;
+  };
+  return run_batched(k, lc, off, static_cast<cudaStream_t>(stream));
+}
+
+int decode_attn_split_partial(const da_params* p, int32_t split_tokens, int32_t max_splits,
+                              const float* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              const int32_t* q_pos, float* o_part, float* lse_part,
+                              int32_t* dev_status, void* stream) {
+  int st = check_params(p, false);
+  if (st != DA_OK) return st;
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !o_part || !lse_part)
+    return DA_ERR_INVALID;
+  if (split_tokens <= 0 || max_splits <= 0 || split_tokens % p->block_size != 0)
+    return DA_ERR_INVALID;
+  if ((long long)split_tokens * max_splits > 0x7fffffffLL) return DA_ERR_INVALID;
+  if (max_splits > 65535) return DA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o_part, 4) ||
+      !aligned(lse_part, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      (q_pos && !aligned(q_pos, 4)) || (dev_status && !aligned(dev_status, 4)))
+    return DA_ERR_INVALID;
+  if (p->batch == 0) return DA_OK;
+  KParams k;
+  memset(&k, 0, sizeof(k));
+  fill_common(k, p);
+  const int rows_box = p->block_size < da::kTile ? p->block_size : da::kTile;
+  const long long rows = (long long)p->num_blocks * p->block_size;
+  st = encode_rows_map(&k.tm_k, k_pool, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p->head_dim,
+                       p->num_kv_heads, rows, 64, rows_box);
+  if (st != DA_OK) return st;
+  st = encode_rows_map(&k.tm_v, v_pool, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p->head_dim,
+                       p->num_kv_heads, rows, 64, rows_box);
+  if (st != DA_OK) return st;
+  k.dev_status = dev_status;
+  k.sched = da::SCHED_SPLIT;
+  k.split_tokens = split_tokens;
+  k.max_splits = max_splits;
+  int smem = 0;
+  k.stages = pick_stages(da::KIND_PAGED, k.D, k.NH, k.Hkv, 1, &smem);
+  if (k.stages == 0) return DA_ERR_UNSUPPORTED;
+  const long long units_total = (long long)p->batch * k.Hkv * k.HG;
+  const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
+  // grid.y is limited to 65535 units per launch: chunk whole sequences
+  const int upb = k.Hkv * k.HG;
+  const int seqs_per_launch = 65535 / upb > 0 ? 65535 / upb : 1;
+  if (upb > 65535) return DA_ERR_UNSUPPORTED;
+  (void)units_total;
+  for (int b0 = 0; b0 < p->batch; b0 += seqs_per_launch) {
+    const int nb = (p->batch - b0) < seqs_per_launch ? (p->batch - b0) : seqs_per_launch;
+    KParams kk = k;
+    kk.B = nb;
+    kk.q = q + (long long)b0 * Hq * D;
+    kk.block_table = block_table + (long long)b0 * mb;
+    kk.seq_lens = seq_lens + b0;
+    kk.q_pos = q_pos ? q_pos + b0 : nullptr;
+    kk.o_part = o_part + (long long)b0 * Hq * max_splits * D;
+    kk.lse_part = lse_part + (long long)b0 * Hq * max_splits;
+    kk.grid = max_splits;
+    cudaError_t e = da::launch_decode(da::KIND_PAGED, kk.D, kk, dim3(max_splits, nb * upb), smem,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+int decode_attn_split_merge(int32_t batch, int32_t num_q_heads, int32_t head_dim,
+                            int32_t max_splits, const float* o_part, const float* lse_part,
+                            float* out, float* lse, void* stream) {
+  if (batch < 0 || num_q_heads <= 0 || head_dim <= 0 || max_splits <= 0) return DA_ERR_INVALID;
+  if (!o_part || !lse_part || !out) return DA_ERR_INVALID;
+  if ((long long)batch * num_q_heads > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
+  if (batch == 0) return DA_OK;
+  cudaError_t e = da::launch_split_merge(batch * num_q_heads, max_splits, head_dim, o_part,
+                                         lse_part, out, lse, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+int decode_attn_tiered_int8(const da_params* p, const da_tier_params* t, const float* q,
+                            const uint16_t* k_hot, const uint16_t* v_hot,
+                            const uint32_t* k_cold, const uint32_t* v_cold,
+                            const uint16_t* k_scale, const uint16_t* v_scale,
+                            const int32_t* block_table, const int32_t* q_pos, float* out,
+                            float* lse, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, void* stream) {
+  int st = check_params(p, true);
+  if (st != DA_OK) return st;
+  if (!t || !q || !k_hot || !v_hot || !k_cold || !v_cold || !k_scale || !v_scale ||
+      !block_table || !out)
+    return DA_ERR_INVALID;
+  if (!workspace && workspace_bytes) return DA_ERR_INVALID;
+  if (t->hot_window < 0 || t->hot_capacity < 1 || t->hot_capacity < t->hot_window)
+    return DA_ERR_INVALID;
+  if (!t->cold_lens && t->cold_len < 0) return DA_ERR_INVALID;
+  if (!t->hot_starts && t->hot_start < 0) return DA_ERR_INVALID;
+  if (!t->hot_lens) {
+    const int limit = t->hot_window > 0 ? t->hot_window : t->hot_capacity;
+    if (t->hot_len < 0 || t->hot_len > limit) return DA_ERR_INVALID;
+  }
+  if (!t->cold_lens && (long long)t->cold_len > (long long)p->max_blocks_per_seq * p->block_size)
+    return DA_ERR_INVALID;
+  if (((long long)p->block_size * p->num_kv_heads * 2) % 16 != 0) return DA_ERR_UNSUPPORTED;
+  if ((long long)t->hot_capacity * p->batch > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_hot, 16) || !aligned(v_hot, 16) || !aligned(k_cold, 16) ||
+      !aligned(v_cold, 16) || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
+      !aligned(out, 16) || !aligned(block_table, 4) || (q_pos && !aligned(q_pos, 4)) ||
+      (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
+    return DA_ERR_INVALID;
+  if (p->batch == 0) return DA_OK;
+  KParams k;
+  memset(&k, 0, sizeof(k));
+  fill_common(k, p);
+  const int rows_box = p->block_size < da::kTile ? p->block_size : da::kTile;
+  const long long rows = (long long)p->num_blocks * p->block_size;
+  st = encode_rows_map(&k.tm_k, k_cold, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->head_dim,
+                       p->num_kv_heads, rows, 128, rows_box);
+  if (st != DA_OK) return st;
+  st = encode_rows_map(&k.tm_v, v_cold, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->head_dim,
+                       p->num_kv_heads, rows, 128, rows_box);
+  if (st != DA_OK) return st;
+  st = encode_ring_map(&k.tm_kh, k_hot, p->head_dim, p->num_kv_heads, t->hot_capacity, p->batch);
+  if (st != DA_OK) return st;
+  st = encode_ring_map(&k.tm_vh, v_hot, p->head_dim, p->num_kv_heads, t->hot_capacity, p->batch);
+  if (st != DA_OK) return st;
+  k.dev_status = dev_status;
+  k.k_scale = k_scale;
+  k.v_scale = v_scale;
+  k.hot_window = t->hot_window;
+  k.hot_cap = t->hot_capacity;
+  k.cold_len = t->cold_len;
+  k.hot_len = t->hot_len;
+  k.hot_start = t->hot_start;
+  Launch lc{da::KIND_TIERED, p, workspace, workspace_bytes};
+  const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
+  // The hot-ring tensor map spans the whole batch; a chunk keeps the global
+  // sequence index through `hot_b0`, so the ring map is not re-encoded.
+  auto off = [&](KParams& kk, int b0) {
+    kk.q = q + (long long)b0 * Hq * D;
+    kk.block_table = block_table + (long long)b0 * mb;
+    kk.q_pos = q_pos ? q_pos + b0 : nullptr;
+    kk.out = out + (long long)b0 * Hq * D;
+    kk.lse = lse ? lse + (long long)b0 * Hq : nullptr;
+    kk.cold_lens = t->cold_lens ? t->cold_lens + b0 : nullptr;
+    kk.hot_lens = t->hot_lens ? t->hot_lens + b0 : nullptr;
+    kk.hot_starts = t->hot_starts ? t->hot_starts + b0 : nullptr;
+    kk.hot_b0 = b0;
+  };
+  return run_batched(k, lc, off, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,37 @@
+// decode_paged.cu — instantiations of the decode kernel for the f16 paged
+// cache, plus the launch switch shared with the tiered unit.
+#include "decode_kernel.cuh"
+#include "launch.h"
+
+namespace da {
+
+template <int KIND, int D>
+cudaError_t launch_decode_impl(const KParams& p, dim3 grid, int smem, cudaStream_t stream) {
+  static int configured[128] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 0 && dev < 128 && !configured[dev]) {
+    err = cudaFuncSetAttribute(decode_attn_kernel<KIND, D>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (err != cudaSuccess) return err;
+    configured[dev] = 1;
+  }
+  decode_attn_kernel<KIND, D><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tiered(int D, const KParams& p, dim3 grid, int smem, cudaStream_t stream);
+
+cudaError_t launch_decode(int kind, int D, const KParams& p, dim3 grid, int smem,
+                          cudaStream_t stream) {
+  if (kind == KIND_TIERED) return launch_tiered(D, p, grid, smem, stream);
+  switch (D) {
+    case 64: return launch_decode_impl<KIND_PAGED, 64>(p, grid, smem, stream);
+    case 128: return launch_decode_impl<KIND_PAGED, 128>(p, grid, smem, stream);
+    case 256: return launch_decode_impl<KIND_PAGED, 256>(p, grid, smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace da

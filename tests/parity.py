@@ -1,0 +1,58 @@
+"""Shared helpers for the GPU-vs-oracle parity tests (not collected)."""
+import numpy as np
+
+import oracle
+import quantized_kv_decode_paged_gb300 as qk
+
+# Tolerances from the benchmark spec of this path: per element
+# |gpu - oracle| <= 1e-3 + 1e-3*|oracle| on the f32 outputs, |dLSE| <= 1e-4.
+OUT_ATOL = 1e-3
+OUT_RTOL = 1e-3
+LSE_ATOL = 1e-4
+
+
+def assert_parity(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
+    out_gpu = np.asarray(out_gpu, dtype=np.float64).reshape(out_ref.shape)
+    lse_gpu = np.asarray(lse_gpu, dtype=np.float64).reshape(lse_ref.shape)
+    assert np.isfinite(out_gpu).all(), f"{what}: non-finite output"
+    err = np.abs(out_gpu - out_ref)
+    bound = OUT_ATOL + OUT_RTOL * np.abs(out_ref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} outputs off, max abs err {err.max():.3e}, "
+                           f"worst at {np.unravel_index(np.argmax(err - bound), err.shape)}")
+    ninf = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse_gpu), ninf), f"{what}: -inf LSE pattern differs"
+    if (~ninf).any():
+        lerr = np.abs(lse_gpu[~ninf] - lse_ref[~ninf])
+        assert lerr.max() <= LSE_ATOL, f"{what}: max LSE err {lerr.max():.3e}"
+    return float(err.max()) if err.size else 0.0
+
+
+def oracle_paged(case, rows=None):
+    seqs = None if rows is None else sorted({int(r) // case.Hq for r in rows})
+    kp, vp = case.host_pools(seqs)
+    return oracle.decode_paged(case.q, kp, vp, case.block_table, case.seq_lens, case.q_pos,
+                               scale=case.scale, softcap=case.softcap,
+                               sliding_window=case.sliding_window, causal=case.causal, rows=rows)
+
+
+def run_paged(case, t, mode, split_tokens=256, dev_status=None):
+    """Runs the CUDA path on device tensors ``t`` in one of the schedules:
+    'stream' (auto workspace), 'units' (no workspace) or 'split'
+    (split_partial + split_merge).  Returns (out, lse) as numpy."""
+    import torch
+    kw = dict(scale=case.scale, softcap=case.softcap, sliding_window=case.sliding_window,
+              causal=case.causal)
+    if mode in ("stream", "units"):
+        out, lse = qk.decode_attn_paged(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                        t["seq_lens"], t["q_pos"], max_seq_len=case.max_seq_len,
+                                        workspace="auto" if mode == "stream" else None,
+                                        dev_status=dev_status, **kw)
+    else:
+        S = max(1, -(-max(case.max_seq_len, 1) // split_tokens))
+        op, lp = qk.decode_attn_split_partial(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                              t["seq_lens"], t["q_pos"], split_tokens=split_tokens,
+                                              max_splits=S, dev_status=dev_status, **kw)
+        out, lse = qk.decode_attn_split_merge(op, lp)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), lse.cpu().numpy()

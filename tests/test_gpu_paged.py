@@ -1,0 +1,185 @@
+"""GPU parity of the f16 paged decode path against the double-precision
+oracle, through the C ABI (via the ctypes binding)."""
+import numpy as np
+import pytest
+
+import oracle
+import quantized_kv_decode_paged_gb300 as qk
+from quantized_kv_decode_paged_gb300 import workloads as wl
+from parity import assert_parity, oracle_paged, run_paged
+
+pytestmark = pytest.mark.gpu
+
+MODES = ("stream", "units", "split")
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    yield
+    import torch
+    torch.cuda.empty_cache()
+
+
+def _case(seed, D, Hq, Hkv, bs, lens, **kw):
+    B = len(lens)
+    pages = sum((max(L, 0) + bs - 1) // bs for L in lens)
+    return wl.make_paged(f"edge{seed}", seed, B=B, Hq=Hq, Hkv=Hkv, D=D, block_size=bs,
+                         seq_lens=lens, num_blocks=pages + 3, **kw)
+
+
+def _check_all_rows(case, mode, **run_kw):
+    t = case.device_tensors("cuda")
+    out, lse = run_paged(case, t, mode, **run_kw)
+    ref_out, ref_lse, _ = oracle_paged(case)
+    assert_parity(out.reshape(-1, case.D), lse.reshape(-1), ref_out, ref_lse,
+                  f"{case.name}/{mode}")
+
+
+def test_tiny_workload_all_modes():
+    case = wl.workload("tiny")
+    t = case.device_tensors("cuda")
+    ref_out, ref_lse, flags = oracle_paged(case)
+    assert flags == 0
+    for mode in MODES:
+        out, lse = run_paged(case, t, mode, split_tokens=64)
+        assert_parity(out.reshape(-1, case.D), lse.reshape(-1), ref_out, ref_lse, f"tiny/{mode}")
+
+
+EDGE_LENS = [1, 7, 8, 9, 15, 16, 17, 63, 64, 65, 127, 128, 129, 200, 511, 777]
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_head_dims_and_group_sizes(D, G):
+    Hkv = 2
+    case = _case(100 + D + G, D, G * Hkv, Hkv, 16, EDGE_LENS[:: 2 if D == 256 else 1])
+    for mode in MODES:
+        _check_all_rows(case, mode)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 256])
+def test_block_sizes(bs):
+    case = _case(200 + bs, 128, 8, 2, bs, [1, bs - 1, bs, bs + 1, 3 * bs + 5, 700])
+    for mode in MODES:
+        _check_all_rows(case, mode, split_tokens=max(bs, 128))
+
+
+@pytest.mark.parametrize("window,softcap", [(1, 0.0), (7, 0.0), (100, 5.0), (300, 50.0),
+                                            (0, 2.0)])
+def test_window_and_softcap(window, softcap):
+    case = _case(300 + window, 128, 8, 2, 16, [1, 5, 64, 99, 150, 400, 1000],
+                 sliding_window=window, softcap=softcap)
+    for mode in MODES:
+        _check_all_rows(case, mode)
+
+
+def test_non_causal_and_explicit_query_positions():
+    lens = [10, 100, 300, 64, 1]
+    q_pos = [3, 99, 500, 0, 0]
+    for causal in (True, False):
+        case = _case(400 + causal, 128, 8, 2, 16, lens, q_pos=q_pos, causal=causal,
+                     sliding_window=37)
+        for mode in MODES:
+            _check_all_rows(case, mode)
+
+
+def test_empty_sequences():
+    case = _case(500, 128, 8, 2, 16, [0, 5, 0, 300, 0])
+    for mode in MODES:
+        _check_all_rows(case, mode)
+    out, lse = run_paged(case, case.device_tensors("cuda"), "stream")
+    assert not out[0].any() and np.isneginf(lse[0]).all()
+
+
+def test_non_finite_rows_past_the_end_do_not_leak():
+    case = _case(600, 128, 8, 2, 16, [3, 17, 50, 129], nonfinite_tail=True)
+    for mode in MODES:
+        _check_all_rows(case, mode)
+
+
+def test_bad_block_ids_are_masked_and_flagged():
+    import torch
+    case = _case(700, 128, 8, 2, 16, [100, 300, 64])
+    bt = case.block_table.copy()
+    bt[0, 2] = case.num_blocks + 5
+    bt[1, 7] = -9
+    case.block_table = bt
+    ref_out, ref_lse, flags = oracle_paged(case)
+    assert flags & oracle.FLAG_BAD_BLOCK
+    t = case.device_tensors("cuda")
+    for mode in MODES:
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out, lse = run_paged(case, t, mode, dev_status=st)
+        assert int(st.item()) & qk.DEV_BAD_BLOCK, mode
+        assert_parity(out.reshape(-1, case.D), lse.reshape(-1), ref_out, ref_lse, f"badblock/{mode}")
+
+
+def test_length_beyond_table_is_clamped_and_flagged():
+    import torch
+    case = _case(800, 128, 8, 2, 16, [64, 100])
+    case.seq_lens = np.array([64, 100 + 10_000], np.int32)  # table holds 7 pages
+    ref_out, ref_lse, flags = oracle_paged(case)
+    assert flags & oracle.FLAG_BAD_SEQ_LEN
+    t = case.device_tensors("cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_paged(case, t, "stream", dev_status=st)
+    assert int(st.item()) & qk.DEV_BAD_SEQ_LEN
+    assert_parity(out.reshape(-1, case.D), lse.reshape(-1), ref_out, ref_lse, "clamp")
+
+
+def test_negative_query_position_flags_and_empties():
+    import torch
+    case = _case(900, 128, 8, 2, 16, [64, 100], q_pos=[-1, 50])
+    ref_out, ref_lse, _ = oracle_paged(case)
+    t = case.device_tensors("cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_paged(case, t, "stream", dev_status=st)
+    assert int(st.item()) & qk.DEV_BAD_QPOS
+    assert_parity(out.reshape(-1, case.D), lse.reshape(-1), ref_out, ref_lse, "qpos")
+
+
+def test_large_batch_is_chunked():
+    rng = np.random.default_rng(5)
+    lens = rng.integers(0, 300, size=300).tolist()
+    case = _case(1000, 64, 4, 2, 16, lens)
+    for mode in MODES:
+        _check_all_rows(case, mode)
+
+
+def test_repeated_calls_are_stable():
+    """The stream schedule leaves its ticket counters at zero: calling again
+    (same workspace) must give the same bits."""
+    case = _case(1100, 128, 32, 8, 16, [4096, 3000, 17, 2500])
+    t = case.device_tensors("cuda")
+    a = run_paged(case, t, "stream")
+    for _ in range(3):
+        b = run_paged(case, t, "stream")
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# --------------------------------------------------------------- full size
+def _sampled_rows(case, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(case.B * case.Hq, size=min(n, case.B * case.Hq), replace=False)
+    # always include the longest and the shortest sequence
+    for b in (int(np.argmax(case.seq_lens)), int(np.argmin(case.seq_lens))):
+        rows = np.concatenate([rows, [b * case.Hq, b * case.Hq + case.Hq - 1]])
+    return np.unique(rows)
+
+
+@pytest.mark.parametrize("name", ["paged", "window", "longctx"])
+def test_full_size_workloads_sampled_rows(name):
+    import torch
+    case = wl.workload(name)
+    t = case.device_tensors("cuda")
+    rows = _sampled_rows(case, 40, 7)
+    ref_out, ref_lse, flags = oracle_paged(case, rows)
+    assert flags == 0
+    modes = ("stream", "units") if name != "paged" else MODES
+    for mode in modes:
+        out, lse = run_paged(case, t, mode, split_tokens=1024)
+        out = out.reshape(-1, case.D)[rows]
+        lse = lse.reshape(-1)[rows]
+        assert_parity(out, lse, ref_out, ref_lse, f"{name}/{mode}")
+    del t
+    torch.cuda.empty_cache()
