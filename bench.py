@@ -1,0 +1,493 @@
+#!/usr/bin/env python3
+"""Benchmark: decode-attention KV-cache bandwidth and time per decode step.
+
+One step = one decode step of the whole batch: a single call of the paged
+(or tiered) decode attention through the library's public API, i.e. one
+launch of the decode kernel (stream-K split-KV with the in-kernel merge).
+Inputs are resident in HBM; the L2 is flushed (a write of 2x its size)
+before every timed step, outside the step's CUDA-event interval.
+
+value = algorithmic bytes per step (visible K/V rows, the block-table
+entries of their pages, Q, out, lse, lengths) / device time per step.
+
+Prints ONE JSON line on rank 0.  `--impl reference` times the CPU oracle on
+a bounded sample of the same workload instead (the reference arm).
+Under torchrun (N > 1) every rank runs an independent replica (the path
+does not shard across GPUs) and rank 0 reports the sum of bytes over the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV-cache HBM GB/s (% of GB300 peak); µs per decode step"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "paged"
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    pat = os.path.join(ROOT, "quantized_kv_decode_paged_gb300", "csrc", "*")
+    for f in sorted(glob.glob(pat)):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken from the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_attn_kernel_{workload}.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = max(smax, float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workloads
+def load_case(name):
+    from quantized_kv_decode_paged_gb300 import workloads as wl
+    return wl.workload(name)
+
+
+def describe(case):
+    from quantized_kv_decode_paged_gb300.workloads import PagedCase
+    if isinstance(case, PagedCase):
+        lens = case.seq_lens
+        return {"workload": case.name, "kind": "paged f16", "B": case.B, "Hq": case.Hq,
+                "Hkv": case.Hkv, "D": case.D, "block_size": case.block_size,
+                "num_blocks": case.num_blocks, "seq_len_min": int(lens.min()),
+                "seq_len_max": int(lens.max()), "seq_len_mean": float(lens.mean()),
+                "sliding_window": case.sliding_window, "softcap": case.softcap}
+    return {"workload": case.name, "kind": "tiered int8 cold + f16 hot ring", "B": case.B,
+            "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D, "block_size": case.block_size,
+            "cold_len": int(case.cold_lens[0]), "hot_len": int(case.hot_lens[0]),
+            "hot_window": case.hot_window, "hot_start": int(case.hot_starts[0])}
+
+
+def make_step(case, t):
+    """Returns step() running one decode step on the current stream."""
+    import quantized_kv_decode_paged_gb300 as qk
+    from quantized_kv_decode_paged_gb300.workloads import PagedCase
+    import torch
+    out = torch.empty((case.B, case.Hq, case.D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
+    if isinstance(case, PagedCase):
+        params = qk.make_params(t["q"], case.block_size, case.Hkv, case.max_blocks,
+                                case.num_blocks, scale=case.scale, softcap=case.softcap,
+                                sliding_window=case.sliding_window, causal=case.causal,
+                                max_seq_len=case.max_seq_len)
+        nbytes = qk.decode_attn_workspace_size(params)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+
+        def step(q=None, block_table=None, seq_lens=None):
+            return qk.decode_attn_paged(
+                t["q"] if q is None else q, t["k_pool"], t["v_pool"],
+                t["block_table"] if block_table is None else block_table,
+                t["seq_lens"] if seq_lens is None else seq_lens, t["q_pos"],
+                scale=case.scale, softcap=case.softcap, sliding_window=case.sliding_window,
+                causal=case.causal, max_seq_len=case.max_seq_len, out=out, lse=lse,
+                workspace=ws)
+    else:
+        params = qk.make_params(t["q"], case.block_size, case.Hkv, case.max_blocks,
+                                case.num_blocks, scale=case.scale, softcap=case.softcap,
+                                sliding_window=case.sliding_window, causal=case.causal,
+                                max_seq_len=case.max_seq_len)
+        nbytes = qk.decode_attn_workspace_size(params)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+
+        def step(q=None, block_table=None, seq_lens=None):
+            return qk.decode_attn_tiered_int8(
+                t["q"] if q is None else q, t["k_hot"], t["v_hot"], t["k_cold"], t["v_cold"],
+                t["k_scale"], t["v_scale"],
+                t["block_table"] if block_table is None else block_table,
+                hot_window=case.hot_window, cold_len=int(case.cold_lens[0]),
+                hot_len=int(case.hot_lens[0]), hot_start=int(case.hot_starts[0]),
+                q_pos=t["q_pos"], scale=case.scale, softcap=case.softcap,
+                sliding_window=case.sliding_window, causal=case.causal,
+                max_seq_len=case.max_seq_len, out=out, lse=lse, workspace=ws)
+    return step, out, lse
+
+
+# ------------------------------------------------------------ CPU / oracle arm
+def oracle_sample(case, target_s, max_units=None):
+    """Times the oracle on whole (sequence, kv head) units of the workload,
+    adding units until about target_s seconds of CPU work.  Returns
+    (GB/s of algorithmic bytes, seconds, description, threads)."""
+    import numpy as np
+    import oracle
+    from quantized_kv_decode_paged_gb300.accounting import visible_range
+    from quantized_kv_decode_paged_gb300.workloads import PagedCase
+    G = case.Hq // case.Hkv
+    units = [(b, kv) for b in range(case.B) for kv in range(case.Hkv)]
+    rng = np.random.default_rng(0)
+    order = rng.permutation(len(units))
+    if max_units is not None:
+        order = order[:max_units]
+    is_paged = isinstance(case, PagedCase)
+
+    def unit_bytes(b):
+        if is_paged:
+            L = int(case.seq_lens[b])
+            lo, hi = visible_range(L, L - 1, case.causal, case.sliding_window)
+            return max(0, hi - lo) * case.D * 2 * 2 + G * case.D * 8
+        cl, hl = int(case.cold_lens[b]), int(case.hot_lens[b])
+        return cl * (case.D * 2 + 4) + hl * case.D * 4 + G * case.D * 8
+
+    def run(sel):
+        rows = np.array([b * case.Hq + kv * G + g for (b, kv) in sel for g in range(G)])
+        seqs = sorted({b for b, _ in sel})
+        if is_paged:
+            kp, vp = case.host_pools(seqs)
+            t0 = time.perf_counter()
+            oracle.decode_paged(case.q, kp, vp, case.block_table, case.seq_lens, case.q_pos,
+                                scale=case.scale, softcap=case.softcap,
+                                sliding_window=case.sliding_window, causal=case.causal, rows=rows)
+        else:
+            h = case.host_arrays(seqs)
+            t0 = time.perf_counter()
+            oracle.decode_tiered(case.q, h["k_hot"], h["v_hot"], h["k_cold"], h["v_cold"],
+                                 h["k_scale"], h["v_scale"], case.block_table, case.cold_lens,
+                                 case.hot_lens, case.hot_starts, hot_window=case.hot_window,
+                                 q_pos=case.q_pos, scale=case.scale, softcap=case.softcap,
+                                 sliding_window=case.sliding_window, causal=case.causal,
+                                 rows=rows)
+        return time.perf_counter() - t0
+
+    # calibrate on a few units, then size the sample; when the whole step is
+    # quicker than the target, repeat it
+    n = min(len(order), 4)
+    sel = [units[i] for i in order[:n]]
+    dt = run(sel)
+    reps = 1
+    if dt < target_s and n < len(order):
+        per_unit = max(dt / n, 1e-6)
+        n = int(min(len(order), max(n, target_s / per_unit)))
+        sel = [units[i] for i in order[:n]]
+        dt = run(sel)
+    if dt < target_s and n == len(order):
+        reps = max(1, int(target_s / max(dt, 1e-6)))
+        dt = sum(run(sel) for _ in range(reps))
+    nbytes = sum(unit_bytes(b) for b, _ in sel) * reps
+    desc = (f"{n} of {len(units)} (sequence, kv head) units of workload '{case.name}' "
+            f"({n * G} query-head rows) x {reps} repetition(s), keys in logical order, "
+            f"double precision")
+    return nbytes / dt / 1e9, dt, desc, oracle.num_threads()
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    case = load_case(args.workload)
+    target = args.ref_step_seconds
+    vals = []
+    desc, threads = "", 1
+    for i in range(args.warmup + args.steps):
+        gbs, dt, desc, threads = oracle_sample(case, target)
+        if i >= args.warmup:
+            vals.append((gbs, dt))
+    gbs = sum(v for v, _ in vals) / len(vals)
+    ms = sum(d for _, d in vals) / len(vals) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {**describe(case), "sample": "bounded oracle sample per step"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+def gpu_arm(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    import quantized_kv_decode_paged_gb300 as qk
+    from quantized_kv_decode_paged_gb300.accounting import algorithmic_bytes
+
+    local = _env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    qk.build()
+    qk.load_library()
+    case = load_case(args.workload)
+    t = case.device_tensors("cuda")
+    step, out, lse = make_step(case, t)
+    acc = algorithmic_bytes(case)
+    bytes_per_step = acc["total"]
+    launches_per_step = -(-case.B // 256)
+
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        w0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        barrier()
+        wall = time.perf_counter() - w0
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dev_ms = sum(times_ms)
+    clocks = clk.summary()
+
+    # e2e: host buffers in, host result out, every step
+    q_h = torch.from_numpy(case.q).pin_memory()
+    bt_h = torch.from_numpy(case.block_table).pin_memory()
+    lens_np = case.seq_lens if hasattr(case, "seq_lens") else case.cold_lens + case.hot_lens
+    sl_h = torch.from_numpy(lens_np.astype("int32")).pin_memory()
+    q_d = torch.empty_like(t["q"])
+    bt_d = torch.empty_like(t["block_table"])
+    sl_d = torch.empty(sl_h.shape, dtype=torch.int32, device="cuda")
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    from quantized_kv_decode_paged_gb300.workloads import PagedCase
+    paged = isinstance(case, PagedCase)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        if paged:
+            sl_d.copy_(sl_h, non_blocking=True)
+            step(q=q_d, block_table=bt_d, seq_lens=sl_d)
+        else:
+            step(q=q_d, block_table=bt_d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    h2d = q_h.numel() * 4 + bt_h.numel() * 4 + (sl_h.numel() * 4 if paged else 0)
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    e2e_steps = max(10, min(args.steps, 500))
+    for _ in range(3):
+        flush.zero_()
+        e2e_step()
+    barrier()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.zero_()
+        e_s[i].record(stream)
+        e2e_step()
+        e_e[i].record(stream)
+    barrier()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps
+
+    # max over ranks
+    stats = torch.tensor([dev_ms, e2e_ms, float(bytes_per_step)], dtype=torch.float64,
+                         device="cuda")
+    if world > 1:
+        mx = stats.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        tot = stats.clone()
+        dist.all_reduce(tot, op=dist.ReduceOp.SUM)
+        dev_ms_max, e2e_ms_max = float(mx[0]), float(mx[1])
+        total_bytes = float(tot[2])
+    else:
+        dev_ms_max, e2e_ms_max, total_bytes = dev_ms, e2e_ms, float(bytes_per_step)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            import oracle
+            oracle.build()
+            gbs, dt, desc, threads = oracle_sample(case, args.cpu_seconds)
+            cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                   "sample": desc, "seconds": round(dt, 2)}
+        except Exception as exc:  # the baseline never blocks the GPU line
+            cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle",
+                   "sample": f"failed: {exc}"}
+
+    if rank == 0:
+        ms_per_step = dev_ms_max / args.steps
+        value = total_bytes * args.steps / (dev_ms_max * 1e-3) / 1e9
+        per_launch_s = dev_ms / args.steps / launches_per_step * 1e-3
+        achieved = bytes_per_step / launches_per_step / per_launch_s / 1e9
+        peak, peak_src = measured_hbm_peak()
+        traffic = profiled_traffic(case.name)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "us_per_step": round(ms_per_step * 1e3, 2),
+            "frac_of_spec_8000": round(value / world / SPEC_HBM_GBS, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 K/V, f32 softmax and accumulate", "data": "synthetic",
+            "config": {**describe(case),
+                       "l2": "flushed before every timed step (write of 2x L2), outside the "
+                             "step's events",
+                       "bytes_per_step": bytes_per_step, "kv_bytes_per_step": acc["kv"],
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "launches_per_step": launches_per_step},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
+                         "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_src == "measured" else "fallback",
+                         "traffic": traffic},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(total_bytes / (e2e_ms_max * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "us_per_step": round(e2e_ms_max * 1e3, 2),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_region": round(wall, 3),
+            "step_us_min": round(min(times_ms) * 1e3, 2),
+            "step_us_median": round(sorted(times_ms)[len(times_ms) // 2] * 1e3, 2),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=["tiny", "paged", "tiered", "window", "longctx", "paged_compact"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work of the oracle baseline sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=4.0,
+                    help="CPU work per step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    if world != args.gpus:
+        world = max(world, 1)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        if args.impl == "reference":
+            return reference_arm(args, rank, world)
+        return gpu_arm(args, rank, world)
+    finally:
+        if world > 1 and args.impl == "ours":
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -110,12 +110,14 @@ typedef struct {
  *
  * workspace: device scratch of at least decode_attn_workspace_size(p)
  * bytes, zero-filled once before its first use (decode_attn_workspace_init
- * or cudaMemsetAsync); every call leaves it zero-filled again.  With it
- * the keys of long sequences are split across CTAs (flash-decoding) and the
- * partial results are merged inside the same launch.  workspace = NULL and
- * workspace_bytes = 0 selects the unsplit path (one CTA per (b, kv head)).
- * Two calls that share a workspace must be ordered (same stream or
- * synchronised); calls that overlap on the GPU race on it.
+ * or cudaMemsetAsync).  Its leading ticket counters are left at zero by
+ * every call, so one buffer serves later calls of any shape that fit in it.
+ * With it the keys of long sequences are split across CTAs (flash-decoding)
+ * and the partial results are merged inside the same launch.
+ * workspace = NULL and workspace_bytes = 0 selects the unsplit path (whole
+ * (b, kv head) units per CTA).  Two calls that share a workspace must be
+ * ordered (same stream or synchronised); calls that overlap on the GPU race
+ * on it.
  * Returns DA_OK or a negative da_status.
  */
 int decode_attn_paged(const da_params* p, const float* q, const uint16_t* k_pool,

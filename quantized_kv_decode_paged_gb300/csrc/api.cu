@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -150,10 +151,23 @@ int encode_ring_map(CUtensorMap* m, const void* base, long long D, long long hea
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
-// Largest stage count that fits in shared memory (at least 2), or 0.
+// Upper bound on pipeline stages: kMaxStages, or DA_MAX_STAGES from the
+// environment when set (a tuning knob; values below 2 are ignored).
+int max_stages() {
+  const char* e = getenv("DA_MAX_STAGES");
+  if (e) {
+    const int v = atoi(e);
+    if (v >= 2 && v <= da::kMaxStages) return v;
+  }
+  return da::kMaxStages;
+}
+
+// Largest stage count that fits in shared memory, a multiple of the
+// consumer groups (each group owns every groups-th stage), or 0.
 int pick_stages(int kind, int D, int NH, int Hkv, int nplan, int* smem_out) {
-  for (int s = da::kMaxStages; s >= 2; --s) {
-    SmemLayout L = da::make_layout(kind, D, NH, Hkv, s, nplan);
+  const int groups = da::decode_groups(D);
+  for (int s = max_stages() / groups * groups; s >= 2; s -= groups) {
+    SmemLayout L = da::make_layout(kind, D, NH, Hkv, s, nplan, groups);
     if (L.total <= da::kSmemLimit) {
       *smem_out = L.total;
       return s;
@@ -162,25 +176,22 @@ int pick_stages(int kind, int D, int NH, int Hkv, int nplan, int* smem_out) {
   return 0;
 }
 
+// Workspace: [tickets: one int per CTA][partial lse][partial o].  The ticket
+// region comes first and its size depends only on the device, so a
+// workspace can serve calls of any shape: only the tickets must be zero
+// between calls, and every call leaves them zero.
 struct WsLayout {
-  size_t o_off, lse_off, cnt_off, total;
+  size_t cnt_off, lse_off, o_off, total;
 };
 
-WsLayout ws_layout(int grid, int units, int D) {
+WsLayout ws_layout(int grid, int D) {
   WsLayout w;
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
-  w.o_off = 0;
-  w.lse_off = al((size_t)grid * 2 * da::kHeadTile * D * 4);
-  w.cnt_off = w.lse_off + al((size_t)grid * 2 * da::kHeadTile * 4);
-  w.total = w.cnt_off + al((size_t)units * 4);
+  w.cnt_off = 0;
+  w.lse_off = al((size_t)grid * 4);
+  w.o_off = w.lse_off + al((size_t)grid * 2 * da::kHeadTile * 4);
+  w.total = w.o_off + al((size_t)grid * 2 * da::kHeadTile * D * 4);
   return w;
-}
-
-int units_per_launch(const da_params* p) {
-  const int G = p->num_q_heads / p->num_kv_heads;
-  const int HG = (G + da::kHeadTile - 1) / da::kHeadTile;
-  const int nb = p->batch < da::kMaxBatchPerLaunch ? p->batch : da::kMaxBatchPerLaunch;
-  return nb * p->num_kv_heads * HG;
 }
 
 struct Launch {
@@ -208,7 +219,7 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
     return DA_ERR_INVALID;
   }
   const int grid_max = sms;
-  const WsLayout w = ws_layout(grid_max, units_per_launch(p), p->head_dim);
+  const WsLayout w = ws_layout(grid_max, p->head_dim);
   for (int b0 = 0; b0 < p->batch; b0 += da::kMaxBatchPerLaunch) {
     const int nb = (p->batch - b0) < da::kMaxBatchPerLaunch ? (p->batch - b0)
                                                              : da::kMaxBatchPerLaunch;
@@ -262,7 +273,7 @@ size_t decode_attn_workspace_size(const da_params* p) {
   if (check_params(p, false) != DA_OK && check_params(p, true) != DA_OK) return 0;
   int sms = 0;
   if (device_sms(&sms) != DA_OK) return 0;
-  return ws_layout(sms, units_per_launch(p), p->head_dim).total;
+  return ws_layout(sms, p->head_dim).total;
 }
 
 int decode_attn_workspace_init(void* workspace, size_t bytes, void* stream) {

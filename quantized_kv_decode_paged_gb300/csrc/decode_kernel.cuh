@@ -7,6 +7,10 @@
 //   keys masked by the causal / sliding-window rule of is_masked there,
 //   out = softmax(s) V and lse = max + ln(sum)
 //   (boostr "paged_attention.wgsl", paged_attention_fwd_f32).
+//   The int8 cold tier decodes byte d%4 of word d/4 as a signed value times
+//   the f16 scale of its (token, kv head), and hot key j sits in ring slot
+//   (hot_start + j) % W (doppler "attention_decode_tiered_int8_f16kv.wgsl",
+//   read_cold_k / get_hot_pos).
 //
 // How (GB300 design, not the pages' WGSL):
 //   * A work unit is (sequence, kv head, group of <= 8 query heads).  All
@@ -14,16 +18,20 @@
 //     n = 8 dimension of mma.m16n8k16, so QK^T is S^T[16 keys x 8 heads] =
 //     K[16 x D] * Q^T and PV is O^T[D x 8] += V^T[D x 16] * P^T[16 x 8].
 //   * f32 Q and P enter the f16 tensor cores as hi + lo f16 pairs, so the
-//     products keep ~22 bits; accumulation is f32.
+//     products keep ~22 bits; accumulation is f32.  int8 values become exact
+//     f16 integers (byte bias + magic-number subtraction); the per-key
+//     scales multiply the score (K) and fold into the weight (V).
 //   * One producer warp streams 64-key stages through TMA (3-D tensor maps
-//     over the pool, one box per page and 64-wide slice of D, 128-byte
-//     swizzle) into a ring of shared-memory stages guarded by mbarriers; four
-//     consumer warps take 16 keys each and keep their own online-softmax
-//     state, merged through shared memory at the end of a unit.
+//     over the pool, one box per page and 128-byte slice of a row, 128-byte
+//     swizzle) into a ring of shared-memory stages guarded by mbarriers.
+//     GROUPS groups of four consumer warps alternate stages (group g owns
+//     the stages s with s % GROUPS == g); in a stage each warp takes 16 keys
+//     and keeps its own online-softmax state, merged through shared memory
+//     at the end of a unit.  Q arrives through its own two-slot ring.
 //   * Stream-K split-KV: the key tiles of all units are concatenated and cut
 //     into one equal share per CTA.  A unit cut between CTAs leaves partial
 //     (o, lse) states in the workspace; the last CTA to finish the unit
-//     (atomic ticket, no waiting) merges them with the log-sum-exp rule of
+//     (atomic ticket, no waiting) merges them with the log-sum-exp form of
 //     com.microsoft.SparseAttention combine_partials.
 #pragma once
 
@@ -36,6 +44,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_inff();
 
 enum { DEST_OUT = 0, DEST_PARTIAL = 1, DEST_SPLIT = 2 };
+enum { TK_PAGED = 0, TK_COLD = 1, TK_HOT = 2 };
 
 struct Seg {
   int b, kv, hg, unit;
@@ -56,13 +65,33 @@ struct Misc {
   int abort;
 };
 
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) { return __uint_as_float(lds32(addr)); }
+
+__device__ __forceinline__ uint16_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
 // ------------------------------------------------------------------ plan
 __device__ __forceinline__ int ceil_div_i(long long a, int b) { return (int)((a + b - 1) / b); }
 
 // Fills plan entry `e` for sequence b (lengths validated, visible range,
 // tile counts); returns device-status bits.
 template <int KIND>
-__device__ int plan_sequence(const KParams& p, int b, SeqPlan& e) {
+__device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e) {
   int flags = 0;
   const long long cap = (long long)p.max_blocks * p.bs;
   e.ntiles = 0;
@@ -126,6 +155,7 @@ __device__ int plan_sequence(const KParams& p, int b, SeqPlan& e) {
     int nhot = 0;
     if (j1 > j0) {
       if (p.hot_window > 0) {
+        // visible ring slots: [s0, s0 + n) modulo W, as one or two tile runs
         const int W = p.hot_window;
         const int nT = ceil_div_i(W, kTile);
         long long s0 = (hs + j0) % W;
@@ -158,7 +188,8 @@ __device__ int plan_sequence(const KParams& p, int b, SeqPlan& e) {
 }
 
 // Exclusive prefix of ntiles * units_per_seq over the batch (one warp).
-__device__ __forceinline__ void plan_prefix(const SeqPlan* plan, int* pre, int B, int upb, int lane) {
+__device__ __forceinline__ void plan_prefix(const SeqPlan* plan, int* pre, int B, int upb,
+                                            int lane) {
   const int per = (B + 31) / 32;
   const int b0 = lane * per;
   long long sum = 0;
@@ -186,13 +217,23 @@ __device__ __forceinline__ int stream_cta_of(long long g, long long T, int grid)
 __device__ __forceinline__ long long stream_start(int c, long long T, int grid) {
   return (long long)c * T / grid;
 }
+// CTAs that share the key tiles in the STREAM schedule: never more than the
+// tiles, so every participating CTA owns at least one tile.
+__device__ __forceinline__ int stream_grid(const KParams& p, long long T) {
+  return (int)(T < p.grid ? T : p.grid);
+}
 
 __device__ __forceinline__ void seg_init(const KParams& p, const int* pre, SegIter& it) {
   it.n = 0;
   if (p.sched == SCHED_STREAM) {
     const long long T = pre[p.B];
-    it.g = stream_start(blockIdx.x, T, p.grid);
-    it.g_end = stream_start(blockIdx.x + 1, T, p.grid);
+    const int sg = stream_grid(p, T);
+    if ((int)blockIdx.x >= sg) {
+      it.g = it.g_end = 0;
+      return;
+    }
+    it.g = stream_start(blockIdx.x, T, sg);
+    it.g_end = stream_start(blockIdx.x + 1, T, sg);
   } else if (p.sched == SCHED_UNITS) {
     const long long U = (long long)p.B * p.Hkv * p.HG;
     it.g = (long long)blockIdx.x * U / p.grid;
@@ -282,8 +323,8 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const SeqPlan* plan, 
   return true;
 }
 
-// Flat index of the last CTA's partial slot for participant c of a unit
-// whose first tile is g0 (STREAM).
+// Flat index of the partial slot of participant c of a unit whose first
+// tile is g0 (STREAM): slot 1 when the unit is not c's first segment.
 __device__ __forceinline__ int stream_slot(int c, int c0, long long g0, long long T, int grid) {
   const int j = (c == c0 && stream_start(c, T, grid) < g0) ? 1 : 0;
   return c * 2 + j;
@@ -298,65 +339,86 @@ struct PageSpan {
   int row_off;  // row offset inside the page (bs > 64)
 };
 
-__device__ __forceinline__ PageSpan page_span(const KParams& p, int at) {
+__device__ __forceinline__ PageSpan page_span(int bs, int log2_bs, int at) {
   PageSpan ps;
   const int tok0 = at * kTile;
-  ps.p_first = tok0 >> p.log2_bs;
-  if (p.bs <= kTile) {
-    ps.npg = kTile >> p.log2_bs;
-    ps.rows = p.bs;
+  ps.p_first = tok0 >> log2_bs;
+  if (bs <= kTile) {
+    ps.npg = kTile >> log2_bs;
+    ps.rows = bs;
     ps.row_off = 0;
   } else {
     ps.npg = 1;
     ps.rows = kTile;
-    ps.row_off = tok0 & (p.bs - 1);
+    ps.row_off = tok0 & (bs - 1);
   }
   return ps;
 }
 
+// Absolute tile of unit-local tile i (tiered: hot tiles follow cold ones).
+template <int KIND>
+__device__ __forceinline__ int tile_of(const SeqPlan& e, int i, bool& is_hot) {
+  if (KIND == KIND_TIERED && i >= e.ncold) {
+    is_hot = true;
+    const int hi_ = i - e.ncold;
+    const int na = e.ha1 - e.ha0;
+    return hi_ < na ? e.ha0 + hi_ : e.hb0 + (hi_ - na);
+  }
+  is_hot = false;
+  return e.t0 + i;
+}
+
 // ============================================================== producer
 template <int KIND, int D>
-__device__ void producer_loop(const KParams& p, const SeqPlan* plan, const int* pre,
-                              uint8_t* stages, const SmemLayout& L, uint64_t* full,
-                              uint64_t* empty, Misc* misc) {
+__device__ __forceinline__ void producer_loop(const KParams& p, const SeqPlan* plan,
+                                              const int* pre, uint8_t* stages, uint8_t* qring,
+                                              const SmemLayout& L, uint64_t* full,
+                                              uint64_t* empty, uint64_t* qfull, uint64_t* qempty,
+                                              Misc* misc) {
   const int lane = threadIdx.x & 31;
-  constexpr int CH = D / 64;  // 64-element slices of D (f16 boxes)
+  constexpr int CH = D / 64;  // 128-byte slices of an f16 row
+  constexpr int CC = D / 128;  // 128-byte slices of an int8 row
+  constexpr int OPS = (KIND == KIND_PAGED) ? 2 * CH : 2 * CC + 2;  // copies per page
+  const int nstages = p.stages;
+  const int bs = p.bs, log2_bs = p.log2_bs, max_blocks = p.max_blocks, nblocks = p.num_blocks;
+  const uint32_t q_bytes = (uint32_t)(p.NH * D * 4);
   SegIter it;
   seg_init(p, pre, it);
   Seg s;
   int stage = 0;
   uint32_t round = 0;
+  int qn = 0;  // non-empty segments so far (Q ring position)
   int bt_b = -1, bt_base = 0, bt_cur = -1, bt_nxt = -1;
   int flags = 0;
-  const int* bt_all = p.block_table;
   while (seg_next(p, plan, pre, it, s)) {
     if (s.i0 >= s.i1) continue;
-    const SeqPlan& e = plan[s.pidx];
-    const int* bt_row = bt_all + (long long)s.b * p.max_blocks;
+    const SeqPlan e = plan[s.pidx];
+    const int* bt_row = p.block_table + (long long)s.b * max_blocks;
+    // ---- Q rows of the head group into the Q ring
+    {
+      const int slot = qn & 1;
+      if (!mbar_wait(&qempty[slot], ((qn >> 1) & 1) ^ 1)) {
+        if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
+        return;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&qfull[slot], q_bytes);
+        const float* src = p.q + ((long long)s.b * p.Hq + s.kv * p.G + s.hg * kHeadTile) * D;
+        bulk_load(qring + slot * L.q_slot_bytes, src, q_bytes, &qfull[slot]);
+      }
+      ++qn;
+    }
     for (int i = s.i0; i < s.i1; ++i) {
       if (!mbar_wait(&empty[stage], (round & 1) ^ 1)) {
         if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
-        misc->abort = 1;
         return;
       }
       uint8_t* st = stages + (size_t)stage * L.stage_bytes;
-      uint32_t bytes = 0;
-      uint32_t bad_mask = 0;
-      const bool q_load = (i == s.i0);
-      if (q_load) bytes += (uint32_t)p.NH * D * 4;
-      bool is_hot = false;
-      int at = 0;
-      if (KIND == KIND_TIERED && i >= e.ncold) {
-        is_hot = true;
-        const int hi_ = i - e.ncold;
-        const int na = e.ha1 - e.ha0;
-        at = hi_ < na ? e.ha0 + hi_ : e.hb0 + (hi_ - na);
-      } else {
-        at = e.t0 + i;
-      }
+      bool is_hot;
+      const int at = tile_of<KIND>(e, i, is_hot);
       if (!is_hot) {
         // ----- pages through the block table
-        const PageSpan ps = page_span(p, at);
+        const PageSpan ps = page_span(bs, log2_bs, at);
         // keep a 64-entry window of block-table entries in two registers
         if (s.b != bt_b || ps.p_first < bt_base || ps.p_first + ps.npg > bt_base + 64) {
           if (s.b == bt_b && ps.p_first >= bt_base + 32 && ps.p_first + ps.npg <= bt_base + 96) {
@@ -365,27 +427,25 @@ __device__ void producer_loop(const KParams& p, const SeqPlan* plan, const int* 
           } else {
             bt_base = ps.p_first;
             const int pc = bt_base + lane;
-            bt_cur = pc < p.max_blocks ? __ldg(bt_row + pc) : -1;
+            bt_cur = pc < max_blocks ? __ldg(bt_row + pc) : -1;
           }
           const int pn = bt_base + 32 + lane;
-          bt_nxt = pn < p.max_blocks ? __ldg(bt_row + pn) : -1;
+          bt_nxt = pn < max_blocks ? __ldg(bt_row + pn) : -1;
           bt_b = s.b;
         }
         const int vhi_keys = (KIND == KIND_TIERED) ? min(s.vhi, e.cold_len) : s.vhi;
-        // page ids of this lane's copies (lane -> page lane / (2*CH'))
-        constexpr int OPS = (KIND == KIND_PAGED) ? 2 * CH : 2 * (D / 128) + 2;
         int my_blk0 = -1, my_blk1 = -1;
-        uint32_t need_mask = 0;
+        uint32_t need_mask = 0, bad_mask = 0, bytes = 0;
         for (int j = 0; j < ps.npg; ++j) {
           const int pg = ps.p_first + j;
           const int idx = pg - bt_base;
           const int vc = __shfl_sync(0xffffffffu, bt_cur, idx & 31);
           const int vn = __shfl_sync(0xffffffffu, bt_nxt, idx & 31);
-          const int blk = pg < p.max_blocks ? (idx < 32 ? vc : vn) : -1;
+          const int blk = pg < max_blocks ? (idx < 32 ? vc : vn) : -1;
           const int r0 = at * kTile + j * ps.rows;
           const bool needed = (r0 < vhi_keys) && (r0 + ps.rows > s.vlo);
           if (!needed) continue;
-          if (blk < 0 || blk >= p.num_blocks) {
+          if (blk < 0 || blk >= nblocks) {
             bad_mask |= 1u << j;
             continue;
           }
@@ -393,18 +453,17 @@ __device__ void producer_loop(const KParams& p, const SeqPlan* plan, const int* 
           if constexpr (KIND == KIND_PAGED) {
             bytes += (uint32_t)(2 * CH * ps.rows * 128);
           } else {
-            bytes += (uint32_t)(2 * (D / 128) * ps.rows * 128 + 2 * p.bs * p.Hkv * 2);
+            bytes += (uint32_t)(2 * CC * ps.rows * 128 + 2 * ps.rows * p.Hkv * 2);
           }
           if (lane / OPS == j) my_blk0 = blk;
           if ((lane + 32) / OPS == j) my_blk1 = blk;
         }
         if (bad_mask) flags |= DEV_BAD_BLOCK;
         if (lane == 0) {
-          *reinterpret_cast<uint32_t*>(st + L.off_hdr) = bad_mask;
+          *reinterpret_cast<volatile uint32_t*>(st + L.off_hdr) = bad_mask;
           mbar_arrive_expect_tx(&full[stage], bytes);
         }
         __syncwarp();
-        // issue the copies: op = lane (and lane + 32)
 #pragma unroll
         for (int rep = 0; rep < 2; ++rep) {
           const int op = lane + rep * 32;
@@ -412,24 +471,24 @@ __device__ void producer_loop(const KParams& p, const SeqPlan* plan, const int* 
           const int blk = rep ? my_blk1 : my_blk0;
           if (j < ps.npg && ((need_mask >> j) & 1u)) {
             const int r = op % OPS;
-            const int row = blk * p.bs + ps.row_off;
+            const int row = blk * bs + ps.row_off;
             if constexpr (KIND == KIND_PAGED) {
               const int isv = r / CH;
               const int ch = r % CH;
               uint8_t* dst = st + (isv ? L.off_v : L.off_k) + ch * (kTile * 128) + j * ps.rows * 128;
               tma_load_3d(dst, isv ? &p.tm_v : &p.tm_k, &full[stage], ch * 64, s.kv, row);
             } else {
-              constexpr int CC = D / 128;  // 128-byte slices of an int8 row
               if (r < 2 * CC) {
                 const int isv = r / CC;
                 const int ch = r % CC;
                 uint8_t* dst = st + (isv ? L.off_v : L.off_k) + ch * (kTile * 128) + j * ps.rows * 128;
                 tma_load_3d(dst, isv ? &p.tm_v : &p.tm_k, &full[stage], ch * 128, s.kv, row);
               } else {
+                // the tile's rows of the page's [rows, Hkv] f16 scale slab
                 const int isv = r - 2 * CC;
-                const uint16_t* src = (isv ? p.v_scale : p.k_scale) + (long long)blk * p.bs * p.Hkv;
-                uint8_t* dst = st + L.off_sc + isv * (kTile * p.Hkv * 2) + j * p.bs * p.Hkv * 2;
-                bulk_load(dst, src, (uint32_t)(p.bs * p.Hkv * 2), &full[stage]);
+                const uint16_t* src = (isv ? p.v_scale : p.k_scale) + (long long)row * p.Hkv;
+                uint8_t* dst = st + L.off_sc + isv * (kTile * p.Hkv * 2) + j * ps.rows * p.Hkv * 2;
+                bulk_load(dst, src, (uint32_t)(ps.rows * p.Hkv * 2), &full[stage]);
               }
             }
           }
@@ -437,9 +496,8 @@ __device__ void producer_loop(const KParams& p, const SeqPlan* plan, const int* 
       } else {
         // ----- hot ring tile: slots [at*64, at*64+64) of sequence b
         if (lane == 0) {
-          bytes += (uint32_t)(2 * CH * kTile * 128);
-          *reinterpret_cast<uint32_t*>(st + L.off_hdr) = 0u;
-          mbar_arrive_expect_tx(&full[stage], bytes);
+          *reinterpret_cast<volatile uint32_t*>(st + L.off_hdr) = 0u;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * CH * kTile * 128));
         }
         __syncwarp();
         if (lane < 2 * CH) {
@@ -450,11 +508,7 @@ __device__ void producer_loop(const KParams& p, const SeqPlan* plan, const int* 
                       s.b + p.hot_b0);
         }
       }
-      if (q_load && lane == 0) {
-        const float* src = p.q + ((long long)s.b * p.Hq + s.kv * p.G + s.hg * kHeadTile) * D;
-        bulk_load(st + L.off_q, src, (uint32_t)(p.NH * D * 4), &full[stage]);
-      }
-      if (++stage == p.stages) {
+      if (++stage == nstages) {
         stage = 0;
         ++round;
       }
@@ -466,15 +520,307 @@ __device__ void producer_loop(const KParams& p, const SeqPlan* plan, const int* 
 // ============================================================== consumer
 template <int D>
 struct Acc {
-  float o[D / 16][4];  // O^T fragments: (d = 16mt + r (+8), head 2c (+1))
+  float o[D / 16][4];  // O^T fragments: (d row r (+8) of m-tile mt, head 2c (+1))
   float m[2], l[2];    // heads 2c, 2c+1 (base-2 units)
 };
 
-// Writes the merged result of the four consumer warps for segment s.
+template <int D>
+struct QFrag {
+  uint32_t hi[D / 16][2], lo[D / 16][2];
+};
+
+// Head-dimension index held by accumulator row r (+8 when hi8) of m-tile mt.
+// Paged f16 keys use the natural order (ldmatrix.trans fragments); the
+// tiered kernel loads V rows four values at a time, so m-tile pair
+// (2p, 2p+1) covers d = 4*(8p + r) + {0, 1, 2, 3}.
+template <int KIND>
+__device__ __forceinline__ int o_row_d(int mt, int r, int hi8) {
+  if constexpr (KIND == KIND_PAGED) {
+    return 16 * mt + r + 8 * hi8;
+  } else {
+    return 4 * (8 * (mt >> 1) + r) + 2 * (mt & 1) + hi8;
+  }
+}
+
+// Q rows of the head group, prescaled (scale*log2 e), as hi/lo f16 B
+// fragments.  Natural order: k-step ks covers d = 16ks + {2c, 2c+1} and
+// {2c+8, 2c+9}; permuted order (tiered): d = 16ks + 4c + {0, 1} and {2, 3}.
 template <int KIND, int D>
-__device__ void finish_segment(const KParams& p, const Seg& s, Acc<D>& a, float* red_o,
-                               float* red_ml, Misc* misc, const int* pre, const SeqPlan* plan) {
-  const int tid = threadIdx.x;  // 0..127
+__device__ __forceinline__ void load_q(uint32_t qs, int NH, float qscale, int r, int c,
+                                       QFrag<D>& q) {
+  const bool hv = r < NH;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    int d0, d2;
+    if constexpr (KIND == KIND_PAGED) {
+      d0 = 16 * ks + 2 * c;
+      d2 = d0 + 8;
+    } else {
+      d0 = 16 * ks + 4 * c;
+      d2 = d0 + 2;
+    }
+    float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+    if (hv) {
+      const uint32_t row = qs + (uint32_t)(r * D) * 4u;
+      const uint2 a = lds64(row + d0 * 4);
+      const uint2 b = lds64(row + d2 * 4);
+      x0 = __uint_as_float(a.x) * qscale;
+      x1 = __uint_as_float(a.y) * qscale;
+      x2 = __uint_as_float(b.x) * qscale;
+      x3 = __uint_as_float(b.y) * qscale;
+    }
+    split_half2(x0, x1, q.hi[ks][0], q.lo[ks][0]);
+    split_half2(x2, x3, q.hi[ks][1], q.lo[ks][1]);
+  }
+}
+
+// Two signed bytes of a word already biased by 0x80 (so byte = x + 128) to
+// an exact f16x2 pair: 0x64XX is 1024 + XX as f16, minus 1152 gives x.
+// `sel` picks the bytes (0x4140: bytes 0,1; 0x4342: bytes 2,3).
+__device__ __forceinline__ uint32_t biased_i8x2_to_h2(uint32_t wb, uint32_t sel) {
+  uint32_t t = __byte_perm(wb, 0x64646464u, sel);
+  __half2 h = *reinterpret_cast<__half2*>(&t);
+  h = __hsub2(h, __half2half2(__ushort_as_half((unsigned short)0x6480u)));  // 1152
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// S^T[16 keys x 8 heads] of keys k0..k0+15.  Four accumulators (hi/lo Q
+// parts x even/odd k-steps) keep the dependency chains short.
+template <int TK, int D>
+__device__ __forceinline__ void tile_qk(uint32_t kbase, int k0, int lane, const QFrag<D>& q,
+                                        float (&s4)[4][4]) {
+  const int r = lane >> 2, c = lane & 3;
+  if constexpr (TK == TK_PAGED) {
+    const int mat = lane >> 3;
+    const int key = k0 + (lane & 7) + ((mat & 1) << 3);
+    const uint32_t rowaddr = kbase + key * 128;
+    const int x = lane & 7;
+    const int dh = mat >> 1;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int ug = 2 * ks + dh;
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(rowaddr + (ug >> 3) * (kTile * 128) + (((ug & 7) ^ x) << 4), a0, a1, a2, a3);
+      mma_f16_16816(s4[(ks & 1)], a0, a1, a2, a3, q.hi[ks][0], q.hi[ks][1]);
+      mma_f16_16816(s4[2 + (ks & 1)], a0, a1, a2, a3, q.lo[ks][0], q.lo[ks][1]);
+    }
+  } else if constexpr (TK == TK_COLD) {
+    // int8 rows of D bytes: word c of 16-byte unit ks holds d = 16ks + 4c .. +3
+    const uint32_t rb0 = kbase + (k0 + r) * 128 + 4 * c;
+    const uint32_t rb1 = rb0 + 8 * 128;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint32_t off = (ks >> 3) * (kTile * 128) + (((ks & 7) ^ r) << 4);
+      const uint32_t w0 = lds32(rb0 + off) ^ 0x80808080u;
+      const uint32_t w1 = lds32(rb1 + off) ^ 0x80808080u;
+      const uint32_t a0 = biased_i8x2_to_h2(w0, 0x4140u), a2 = biased_i8x2_to_h2(w0, 0x4342u);
+      const uint32_t a1 = biased_i8x2_to_h2(w1, 0x4140u), a3 = biased_i8x2_to_h2(w1, 0x4342u);
+      mma_f16_16816(s4[(ks & 1)], a0, a1, a2, a3, q.hi[ks][0], q.hi[ks][1]);
+      mma_f16_16816(s4[2 + (ks & 1)], a0, a1, a2, a3, q.lo[ks][0], q.lo[ks][1]);
+    }
+  } else {
+    // f16 rows: 8 bytes at d = 16ks + 4c
+    const uint32_t rb0 = kbase + (k0 + r) * 128 + (c & 1) * 8;
+    const uint32_t rb1 = rb0 + 8 * 128;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int u = 2 * (ks & 3) + (c >> 1);
+      const uint32_t off = (ks >> 2) * (kTile * 128) + ((u ^ r) << 4);
+      const uint2 v0 = lds64(rb0 + off);
+      const uint2 v1 = lds64(rb1 + off);
+      mma_f16_16816(s4[(ks & 1)], v0.x, v1.x, v0.y, v1.y, q.hi[ks][0], q.hi[ks][1]);
+      mma_f16_16816(s4[2 + (ks & 1)], v0.x, v1.x, v0.y, v1.y, q.lo[ks][0], q.lo[ks][1]);
+    }
+  }
+}
+
+// O^T += V^T P^T for keys k0..k0+15; b* are the P^T fragments.
+template <int TK, int D>
+__device__ __forceinline__ void tile_pv(uint32_t vbase, int k0, int lane, float (&o)[D / 16][4],
+                                        uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
+  const int r = lane >> 2, c = lane & 3;
+  if constexpr (TK == TK_PAGED) {
+    const int mat = lane >> 3;
+    const int key = k0 + (lane & 7) + ((mat >> 1) << 3);
+    const uint32_t rowaddr = vbase + key * 128;
+    const int x = lane & 7;
+    const int dh = mat & 1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      const int ug = 2 * mt + dh;
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_trans(rowaddr + (ug >> 3) * (kTile * 128) + (((ug & 7) ^ x) << 4), a0, a1, a2, a3);
+      mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
+      mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+    }
+  } else if constexpr (TK == TK_COLD) {
+    // word q = 8pp + r (d = 4q .. 4q+3) of keys 2c, 2c+1, 2c+8, 2c+9
+    const int tA = k0 + 2 * c;
+#pragma unroll
+    for (int pp = 0; pp < D / 32; ++pp) {
+      const int u = 2 * (pp & 3) + (r >> 2);
+      const uint32_t base = vbase + (pp >> 2) * (kTile * 128) + (r & 3) * 4;
+      const uint32_t WA = lds32(base + tA * 128 + ((u ^ (2 * c)) << 4)) ^ 0x80808080u;
+      const uint32_t WB = lds32(base + (tA + 1) * 128 + ((u ^ (2 * c + 1)) << 4)) ^ 0x80808080u;
+      const uint32_t WC = lds32(base + (tA + 8) * 128 + ((u ^ (2 * c)) << 4)) ^ 0x80808080u;
+      const uint32_t WD = lds32(base + (tA + 9) * 128 + ((u ^ (2 * c + 1)) << 4)) ^ 0x80808080u;
+      const uint32_t E = __byte_perm(WA, WB, 0x5140u), F = __byte_perm(WA, WB, 0x7362u);
+      const uint32_t E2 = __byte_perm(WC, WD, 0x5140u), F2 = __byte_perm(WC, WD, 0x7362u);
+      {
+        const uint32_t a0 = biased_i8x2_to_h2(E, 0x4140u), a1 = biased_i8x2_to_h2(E, 0x4342u);
+        const uint32_t a2 = biased_i8x2_to_h2(E2, 0x4140u), a3 = biased_i8x2_to_h2(E2, 0x4342u);
+        mma_f16_16816(o[2 * pp], a0, a1, a2, a3, bh0, bh1);
+        mma_f16_16816(o[2 * pp], a0, a1, a2, a3, bl0, bl1);
+      }
+      {
+        const uint32_t a0 = biased_i8x2_to_h2(F, 0x4140u), a1 = biased_i8x2_to_h2(F, 0x4342u);
+        const uint32_t a2 = biased_i8x2_to_h2(F2, 0x4140u), a3 = biased_i8x2_to_h2(F2, 0x4342u);
+        mma_f16_16816(o[2 * pp + 1], a0, a1, a2, a3, bh0, bh1);
+        mma_f16_16816(o[2 * pp + 1], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+  } else {
+    // f16 rows, 8 bytes (d = 4q .. 4q+3, q = 8pp + r) of keys 2c, 2c+1, 2c+8, 2c+9
+    const int tA = k0 + 2 * c;
+#pragma unroll
+    for (int pp = 0; pp < D / 32; ++pp) {
+      const int u = 4 * (pp & 1) + (r >> 1);
+      const uint32_t base = vbase + (pp >> 1) * (kTile * 128) + (r & 1) * 8;
+      const uint2 A = lds64(base + tA * 128 + ((u ^ (2 * c)) << 4));
+      const uint2 B = lds64(base + (tA + 1) * 128 + ((u ^ (2 * c + 1)) << 4));
+      const uint2 C = lds64(base + (tA + 8) * 128 + ((u ^ (2 * c)) << 4));
+      const uint2 E = lds64(base + (tA + 9) * 128 + ((u ^ (2 * c + 1)) << 4));
+      {
+        const uint32_t a0 = __byte_perm(A.x, B.x, 0x5410u), a1 = __byte_perm(A.x, B.x, 0x7632u);
+        const uint32_t a2 = __byte_perm(C.x, E.x, 0x5410u), a3 = __byte_perm(C.x, E.x, 0x7632u);
+        mma_f16_16816(o[2 * pp], a0, a1, a2, a3, bh0, bh1);
+        mma_f16_16816(o[2 * pp], a0, a1, a2, a3, bl0, bl1);
+      }
+      {
+        const uint32_t a0 = __byte_perm(A.y, B.y, 0x5410u), a1 = __byte_perm(A.y, B.y, 0x7632u);
+        const uint32_t a2 = __byte_perm(C.y, E.y, 0x5410u), a3 = __byte_perm(C.y, E.y, 0x7632u);
+        mma_f16_16816(o[2 * pp + 1], a0, a1, a2, a3, bh0, bh1);
+        mma_f16_16816(o[2 * pp + 1], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+  }
+}
+
+// One stage for this warp's 16 keys: QK, mask, online softmax, PV.
+// vA / vB: validity of keys k0+r and k0+r+8.  ksA.. / vsA..: per-key K and
+// V scales of the int8 tier (rows r and r+8), 1 otherwise.
+template <int TK, int D>
+__device__ __forceinline__ void tile_compute(uint8_t* st, const SmemLayout& L, float softcap2,
+                                             int k0, int lane, const QFrag<D>& q, Acc<D>& a,
+                                             bool vA, bool vB, float ksA, float ksB, float vsA,
+                                             float vsB) {
+  const uint32_t kbase = smem_u32(st + L.off_k);
+  const uint32_t vbase = smem_u32(st + L.off_v);
+  float s4[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s4[i][0] = s4[i][1] = s4[i][2] = s4[i][3] = 0.f;
+  tile_qk<TK, D>(kbase, k0, lane, q, s4);
+  float sc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float v = (s4[0][j] + s4[1][j]) + (s4[2][j] + s4[3][j]);
+    if constexpr (TK == TK_COLD) v *= (j < 2 ? ksA : ksB);
+    if (softcap2 > 0.f) v = softcap2 * tanhf(v / softcap2);
+    sc[j] = v;
+  }
+  if (!vA) sc[0] = sc[1] = kNegInf;
+  if (!vB) sc[2] = sc[3] = kNegInf;
+  // ---- online softmax (base 2)
+  float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const float mn0 = fmaxf(a.m[0], mx0), mn1 = fmaxf(a.m[1], mx1);
+  const float al0 = (mn0 == kNegInf) ? 1.f : exp2f(a.m[0] - mn0);
+  const float al1 = (mn1 == kNegInf) ? 1.f : exp2f(a.m[1] - mn1);
+  const float mu0 = (mn0 == kNegInf) ? 0.f : mn0;
+  const float mu1 = (mn1 == kNegInf) ? 0.f : mn1;
+  float p0 = exp2f(sc[0] - mu0), p1 = exp2f(sc[1] - mu1);
+  float p2 = exp2f(sc[2] - mu0), p3 = exp2f(sc[3] - mu1);
+  a.l[0] = a.l[0] * al0 + (p0 + p2);
+  a.l[1] = a.l[1] * al1 + (p1 + p3);
+  a.m[0] = mn0;
+  a.m[1] = mn1;
+  if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      a.o[mt][0] *= al0;
+      a.o[mt][1] *= al1;
+      a.o[mt][2] *= al0;
+      a.o[mt][3] *= al1;
+    }
+  }
+  if constexpr (TK == TK_COLD) {
+    // the V scale of each key folds into its weight (masked keys: exactly 0)
+    p0 = vA ? p0 * vsA : 0.f;
+    p1 = vA ? p1 * vsA : 0.f;
+    p2 = vB ? p2 * vsB : 0.f;
+    p3 = vB ? p3 * vsB : 0.f;
+  }
+  // ---- P^T as the B operand (hi + lo), via an 8x8 transpose
+  uint32_t h01, l01, h23, l23;
+  split_half2(p0, p1, h01, l01);
+  split_half2(p2, p3, h23, l23);
+  const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+  const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+  tile_pv<TK, D>(vbase, k0, lane, a.o, bh0, bh1, bl0, bl1);
+}
+
+// Zeroes the V rows of masked keys among k0..k0+15 (f16 tiles), so that a
+// zero weight never meets a stale or non-finite value.
+template <int D, typename OkFn>
+__device__ __forceinline__ void zero_masked_v_rows(uint8_t* vst, int k0, int lane, OkFn ok) {
+  constexpr int UPR = D / 8;  // 16-byte units per f16 row
+  for (int u = lane; u < 16 * UPR; u += 32) {
+    const int row = u / UPR, ug = u % UPR;
+    const int k = k0 + row;
+    if (!ok(k)) {
+      uint8_t* dst = vst + (ug >> 3) * (kTile * 128) + k * 128 + (((ug & 7) ^ (k & 7)) << 4);
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
+// Key validity of row k (0..63) of a paged / cold tile.
+__device__ __forceinline__ bool key_ok_paged(int bs, int log2_bs, int at, int k, int vlo, int vhi,
+                                             uint32_t bad_mask) {
+  const int t = at * kTile + k;
+  if (t < vlo || t >= vhi) return false;
+  const int j = bs <= kTile ? (k >> log2_bs) : 0;
+  return ((bad_mask >> j) & 1u) == 0;
+}
+
+// What a hot-ring tile can see: ring slot s holds hot key
+// j = (s - hot_start) mod W (or j = s without a ring), visible when
+// j0 <= j < j1.
+struct HotView {
+  int W, cap_eff, hs_mod;
+  long long j0, j1;
+};
+
+__device__ __forceinline__ bool key_ok_hot(const HotView& hv, int at, int k) {
+  const int sl = at * kTile + k;
+  if (sl >= hv.cap_eff) return false;
+  const int j = hv.W > 0 ? (sl - hv.hs_mod + hv.W) % hv.W : sl;
+  return j >= hv.j0 && j < hv.j1;
+}
+
+// Merges the consumer warps' states for segment s and writes the result.
+template <int KIND, int D, int GROUPS>
+__device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, Acc<D>& a,
+                                               float* red_o, float* red_ml, Misc* misc,
+                                               const int* pre, const SeqPlan* plan) {
+  constexpr int NCW = consumer_warps(GROUPS);
+  const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
   const int NH = p.NH;
@@ -493,8 +839,8 @@ __device__ void finish_segment(const KParams& p, const Seg& s, Acc<D>& a, float*
       float* ro = red_o + (warp * NH + h) * D;
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
-        ro[16 * mt + r] = a.o[mt][j];
-        ro[16 * mt + r + 8] = a.o[mt][2 + j];
+        ro[o_row_d<KIND>(mt, r, 0)] = a.o[mt][j];
+        ro[o_row_d<KIND>(mt, r, 1)] = a.o[mt][2 + j];
       }
       if (r == 0) {
         red_ml[(warp * NH + h) * 2 + 0] = a.m[j];
@@ -502,19 +848,19 @@ __device__ void finish_segment(const KParams& p, const Seg& s, Acc<D>& a, float*
       }
     }
   }
-  named_bar_sync(kRedBarrier, kConsumerWarps * 32);
+  named_bar_sync(kRedBarrier, NCW * 32);
   const int h0 = s.kv * p.G + s.hg * kHeadTile;
   const long long row0 = (long long)s.b * p.Hq + h0;
-  for (int idx = tid; idx < NH * D; idx += kConsumerWarps * 32) {
+  for (int idx = tid; idx < NH * D; idx += NCW * 32) {
     const int h = idx / D, d = idx % D;
     float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_ml[(w * NH + h) * 2]);
+    for (int w = 0; w < NCW; ++w) M = fmaxf(M, red_ml[(w * NH + h) * 2]);
     float o = 0.f, lse = kNegInf;
     if (M != kNegInf) {
       float Ls = 0.f, Os = 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
+      for (int w = 0; w < NCW; ++w) {
         const float f = exp2f(red_ml[(w * NH + h) * 2] - M);
         Ls += f * red_ml[(w * NH + h) * 2 + 1];
         Os += f * red_o[(w * NH + h) * D + d];
@@ -536,33 +882,36 @@ __device__ void finish_segment(const KParams& p, const Seg& s, Acc<D>& a, float*
     }
   }
   if (s.dest == DEST_PARTIAL) __threadfence();
-  named_bar_sync(kRedBarrier, kConsumerWarps * 32);
+  named_bar_sync(kRedBarrier, NCW * 32);
   if (s.dest != DEST_PARTIAL) return;
   // ---- last-arriver merge of the unit's partial states
   const long long T = pre[p.B];
+  const int sg = stream_grid(p, T);
   const int nt = plan[s.pidx].ntiles;
   const int uib = s.unit - s.b * p.Hkv * p.HG;
   const long long g0 = pre[s.b] + (long long)uib * nt;
   const long long g1 = g0 + nt - 1;
-  const int c0 = stream_cta_of(g0, T, p.grid);
-  const int c1 = stream_cta_of(g1, T, p.grid);
-  if (tid == 0) misc->ticket = atomicAdd(&p.ws_cnt[s.unit], 1);
-  named_bar_sync(kRedBarrier, kConsumerWarps * 32);
+  const int c0 = stream_cta_of(g0, T, sg);
+  const int c1 = stream_cta_of(g1, T, sg);
+  // A unit cut between CTAs is the last segment of its first CTA c0, so c0
+  // names the unit's ticket counter.
+  if (tid == 0) misc->ticket = atomicAdd(&p.ws_cnt[c0], 1);
+  named_bar_sync(kRedBarrier, NCW * 32);
   const int ticket = misc->ticket;
   if (ticket == c1 - c0) {
     __threadfence();
-    for (int idx = tid; idx < NH * D; idx += kConsumerWarps * 32) {
+    for (int idx = tid; idx < NH * D; idx += NCW * 32) {
       const int h = idx / D, d = idx % D;
       float M = kNegInf;
       for (int cc = c0; cc <= c1; ++cc) {
-        const long long sl = (long long)stream_slot(cc, c0, g0, T, p.grid) * kHeadTile + h;
+        const long long sl = (long long)stream_slot(cc, c0, g0, T, sg) * kHeadTile + h;
         M = fmaxf(M, __ldcg(p.ws_lse + sl));
       }
       float o = 0.f, lse = kNegInf;
       if (M != kNegInf) {
         float Ws = 0.f, Os = 0.f;
         for (int cc = c0; cc <= c1; ++cc) {
-          const long long sl = (long long)stream_slot(cc, c0, g0, T, p.grid) * kHeadTile + h;
+          const long long sl = (long long)stream_slot(cc, c0, g0, T, sg) * kHeadTile + h;
           const float ls = __ldcg(p.ws_lse + sl);
           const float w = (ls == kNegInf) ? 0.f : expf(ls - M);
           Ws += w;
@@ -574,38 +923,36 @@ __device__ void finish_segment(const KParams& p, const Seg& s, Acc<D>& a, float*
       p.out[(row0 + h) * D + d] = o;
       if (d == 0 && p.lse) p.lse[row0 + h] = lse;
     }
-    if (tid == 0) p.ws_cnt[s.unit] = 0;
+    if (tid == 0) p.ws_cnt[c0] = 0;
   }
-  named_bar_sync(kRedBarrier, kConsumerWarps * 32);
+  named_bar_sync(kRedBarrier, NCW * 32);
 }
 
-// Key validity of row k (0..63) of a paged / cold tile.
-__device__ __forceinline__ bool key_ok_paged(const KParams& p, int at, int k, int vlo, int vhi,
-                                             uint32_t bad_mask) {
-  const int t = at * kTile + k;
-  if (t < vlo || t >= vhi) return false;
-  const int j = p.bs <= kTile ? (k >> p.log2_bs) : 0;
-  return ((bad_mask >> j) & 1u) == 0;
-}
-
-template <int KIND, int D>
-__device__ void consumer_loop(const KParams& p, const SeqPlan* plan, const int* pre,
-                              uint8_t* stages, const SmemLayout& L, uint64_t* full,
-                              uint64_t* empty, float* red_o, float* red_ml, Misc* misc) {
-  constexpr int KS = D / 16;  // k-steps of QK, m-tiles of PV
+template <int KIND, int D, int GROUPS>
+__device__ __forceinline__ void consumer_loop(const KParams& p, const SeqPlan* plan,
+                                              const int* pre, uint8_t* stages, uint8_t* qring,
+                                              const SmemLayout& L, uint64_t* full,
+                                              uint64_t* empty, uint64_t* qfull, uint64_t* qempty,
+                                              float* red_o, float* red_ml, Misc* misc) {
+  constexpr int NCW = consumer_warps(GROUPS);
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
-  const int k0 = warp * 16;
+  const int group = warp / kGroupWarps;
+  const int k0 = (warp % kGroupWarps) * 16;
+  const int nstages = p.stages;
+  const int bs = p.bs, log2_bs = p.log2_bs;
+  const float softcap2 = p.softcap2, qscale = p.qscale;
+  const int NH = p.NH;
 
   // Sequences with no visible key: out = 0, lse = -inf.
   if (p.sched != SCHED_SPLIT) {
     for (int b = blockIdx.x; b < p.B; b += p.grid) {
       if (plan[b].ntiles != 0) continue;
-      for (int idx = tid; idx < p.Hq * D; idx += kConsumerWarps * 32)
+      for (int idx = tid; idx < p.Hq * D; idx += NCW * 32)
         p.out[(long long)b * p.Hq * D + idx] = 0.f;
       if (p.lse)
-        for (int h = tid; h < p.Hq; h += kConsumerWarps * 32) p.lse[(long long)b * p.Hq + h] = kNegInf;
+        for (int h = tid; h < p.Hq; h += NCW * 32) p.lse[(long long)b * p.Hq + h] = kNegInf;
     }
   }
 
@@ -614,14 +961,15 @@ __device__ void consumer_loop(const KParams& p, const SeqPlan* plan, const int* 
   Seg s;
   int stage = 0;
   uint32_t round = 0;
+  int qn = 0;
   Acc<D> a;
-  uint32_t qhi[KS][2], qlo[KS][2];
+  QFrag<D> q;
 
   while (seg_next(p, plan, pre, it, s)) {
     if (s.i0 >= s.i1) {
       // SPLIT with no visible key: o = 0, lse = -inf
       const int h0 = s.kv * p.G + s.hg * kHeadTile;
-      for (int idx = tid; idx < p.NH * D; idx += kConsumerWarps * 32) {
+      for (int idx = tid; idx < NH * D; idx += NCW * 32) {
         const int h = idx / D, d = idx % D;
         const long long pr = ((long long)s.b * p.Hq + h0 + h) * p.max_splits + s.slot;
         p.o_part[pr * D + d] = 0.f;
@@ -629,178 +977,125 @@ __device__ void consumer_loop(const KParams& p, const SeqPlan* plan, const int* 
       }
       continue;
     }
-    const SeqPlan& e = plan[s.pidx];
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) a.o[mt][0] = a.o[mt][1] = a.o[mt][2] = a.o[mt][3] = 0.f;
-    a.m[0] = a.m[1] = kNegInf;
-    a.l[0] = a.l[1] = 0.f;
-
-    for (int i = s.i0; i < s.i1; ++i) {
-      if (!mbar_wait(&full[stage], round & 1)) {
+    const SeqPlan e = plan[s.pidx];
+    {
+      const int slot = qn & 1;
+      if (!mbar_wait(&qfull[slot], (qn >> 1) & 1)) {
         if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
-        misc->abort = 1;
         return;
       }
-      uint8_t* st = stages + (size_t)stage * L.stage_bytes;
-      if (i == s.i0) {
-        // Q rows of the head group, prescaled by scale*log2(e), as hi/lo f16
-        const float* qs = reinterpret_cast<const float*>(st + L.off_q);
-        const bool hv = r < p.NH;
+      load_q<KIND, D>(smem_u32(qring + slot * L.q_slot_bytes), NH, qscale, r, c, q);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qempty[slot]);
+      ++qn;
+    }
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const int d0 = 16 * ks + 2 * c;
-          float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-          if (hv) {
-            x0 = qs[r * D + d0] * p.qscale;
-            x1 = qs[r * D + d0 + 1] * p.qscale;
-            x2 = qs[r * D + d0 + 8] * p.qscale;
-            x3 = qs[r * D + d0 + 9] * p.qscale;
-          }
-          split_half2(x0, x1, qhi[ks][0], qlo[ks][0]);
-          split_half2(x2, x3, qhi[ks][1], qlo[ks][1]);
+    for (int mt = 0; mt < D / 16; ++mt) a.o[mt][0] = a.o[mt][1] = a.o[mt][2] = a.o[mt][3] = 0.f;
+    a.m[0] = a.m[1] = kNegInf;
+    a.l[0] = a.l[1] = 0.f;
+    HotView hv;
+    if constexpr (KIND == KIND_TIERED) {
+      hv.W = p.hot_window;
+      hv.cap_eff = p.hot_window > 0 ? p.hot_window : p.hot_cap;
+      hv.hs_mod = p.hot_window > 0 ? e.hot_start % p.hot_window : 0;
+      const long long j0 = (long long)s.vlo - e.hot_start;
+      const long long j1 = (long long)s.vhi - e.hot_start;
+      hv.j0 = j0 > 0 ? j0 : 0;
+      hv.j1 = j1 < e.hot_len ? j1 : e.hot_len;
+    }
+
+    for (int i = s.i0; i < s.i1; ++i) {
+      if (stage % GROUPS == group) {
+        if (!mbar_wait(&full[stage], round & 1)) {
+          if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
+          return;
         }
-      }
-      const uint32_t bad_mask = *reinterpret_cast<const uint32_t*>(st + L.off_hdr);
-      const int at = e.t0 + i;
-      const bool vA = key_ok_paged(p, at, k0 + r, s.vlo, s.vhi, bad_mask);
-      const bool vB = key_ok_paged(p, at, k0 + r + 8, s.vlo, s.vhi, bad_mask);
-      const bool any = __any_sync(0xffffffffu, vA || vB);
-      if (any) {
-        const uint8_t* kst = st + L.off_k;
-        uint8_t* vst = st + L.off_v;
-        if (!__all_sync(0xffffffffu, vA && vB)) {
-          // zero the V rows of masked keys so 0 * (stale or non-finite) cannot leak
-          constexpr int UPR = D / 8;  // 16-byte units per row
-          for (int u = lane; u < 16 * UPR; u += 32) {
-            const int row = u / UPR, ug = u % UPR;
-            const int k = k0 + row;
-            if (!key_ok_paged(p, at, k, s.vlo, s.vhi, bad_mask)) {
-              uint8_t* dst = vst + (ug >> 3) * (kTile * 128) + k * 128 + (((ug & 7) ^ (k & 7)) << 4);
-              *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        uint8_t* st = stages + (size_t)stage * L.stage_bytes;
+        const uint32_t bad_mask = lds32(smem_u32(st + L.off_hdr));
+        bool is_hot;
+        const int at = tile_of<KIND>(e, i, is_hot);
+        if (!is_hot) {
+          const int vhc = (KIND == KIND_TIERED) ? min(s.vhi, e.cold_len) : s.vhi;
+          auto ok = [&](int k) { return key_ok_paged(bs, log2_bs, at, k, s.vlo, vhc, bad_mask); };
+          const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
+          if (__any_sync(0xffffffffu, vA || vB)) {
+            if constexpr (KIND == KIND_PAGED) {
+              if (!__all_sync(0xffffffffu, vA && vB))
+                zero_masked_v_rows<D>(st + L.off_v, k0, lane, ok);
+              tile_compute<TK_PAGED, D>(st, L, softcap2, k0, lane, q, a, vA, vB, 1.f, 1.f, 1.f,
+                                        1.f);
+            } else {
+              const uint32_t sck = smem_u32(st + L.off_sc);
+              const uint32_t scv = sck + kTile * p.Hkv * 2;
+              const uint32_t iA = ((k0 + r) * p.Hkv + s.kv) * 2, iB = iA + 8 * p.Hkv * 2;
+              tile_compute<TK_COLD, D>(
+                  st, L, softcap2, k0, lane, q, a, vA, vB,
+                  __half2float(__ushort_as_half(lds16(sck + iA))),
+                  __half2float(__ushort_as_half(lds16(sck + iB))),
+                  __half2float(__ushort_as_half(lds16(scv + iA))),
+                  __half2float(__ushort_as_half(lds16(scv + iB))));
             }
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        // ---- S^T = K Q^T (16 keys x 8 heads)
-        float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          const int mat = lane >> 3;
-          const int key = k0 + (lane & 7) + ((mat & 1) << 3);
-          const uint32_t rowaddr = smem_u32(kst) + key * 128;
-          const int x = lane & 7;
-          const int dh = mat >> 1;
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            const int ug = 2 * ks + dh;
-            const uint32_t addr = rowaddr + (ug >> 3) * (kTile * 128) + (((ug & 7) ^ x) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(addr, a0, a1, a2, a3);
-            mma_f16_16816(sh, a0, a1, a2, a3, qhi[ks][0], qhi[ks][1]);
-            mma_f16_16816(sl, a0, a1, a2, a3, qlo[ks][0], qlo[ks][1]);
+        } else if constexpr (KIND == KIND_TIERED) {
+          auto ok = [&](int k) { return key_ok_hot(hv, at, k); };
+          const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
+          if (__any_sync(0xffffffffu, vA || vB)) {
+            if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(st + L.off_v, k0, lane, ok);
+            tile_compute<TK_HOT, D>(st, L, softcap2, k0, lane, q, a, vA, vB, 1.f, 1.f, 1.f, 1.f);
           }
         }
-        float sc[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float v = sh[j] + sl[j];
-          if (p.softcap2 > 0.f) v = p.softcap2 * tanhf(v / p.softcap2);
-          sc[j] = v;
-        }
-        if (!vA) sc[0] = sc[1] = kNegInf;
-        if (!vB) sc[2] = sc[3] = kNegInf;
-        // ---- online softmax (base 2)
-        float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(a.m[0], mx0), mn1 = fmaxf(a.m[1], mx1);
-        const float al0 = (mn0 == kNegInf) ? 1.f : exp2f(a.m[0] - mn0);
-        const float al1 = (mn1 == kNegInf) ? 1.f : exp2f(a.m[1] - mn1);
-        const float mu0 = (mn0 == kNegInf) ? 0.f : mn0;
-        const float mu1 = (mn1 == kNegInf) ? 0.f : mn1;
-        const float p0 = exp2f(sc[0] - mu0), p1 = exp2f(sc[1] - mu1);
-        const float p2 = exp2f(sc[2] - mu0), p3 = exp2f(sc[3] - mu1);
-        a.l[0] = a.l[0] * al0 + (p0 + p2);
-        a.l[1] = a.l[1] * al1 + (p1 + p3);
-        a.m[0] = mn0;
-        a.m[1] = mn1;
-        if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {
-#pragma unroll
-          for (int mt = 0; mt < KS; ++mt) {
-            a.o[mt][0] *= al0;
-            a.o[mt][1] *= al1;
-            a.o[mt][2] *= al0;
-            a.o[mt][3] *= al1;
-          }
-        }
-        // ---- P^T as the B operand (hi + lo), via an 8x8 transpose
-        uint32_t h01, l01, h23, l23;
-        split_half2(p0, p1, h01, l01);
-        split_half2(p2, p3, h23, l23);
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-        // ---- O^T += V^T P^T
-        {
-          const int mat = lane >> 3;
-          const int key = k0 + (lane & 7) + ((mat >> 1) << 3);
-          const uint32_t rowaddr = smem_u32(vst) + key * 128;
-          const int x = lane & 7;
-          const int dh = mat & 1;
-#pragma unroll
-          for (int mt = 0; mt < KS; ++mt) {
-            const int ug = 2 * mt + dh;
-            const uint32_t addr = rowaddr + (ug >> 3) * (kTile * 128) + (((ug & 7) ^ x) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(addr, a0, a1, a2, a3);
-            mma_f16_16816(a.o[mt], a0, a1, a2, a3, bh0, bh1);
-            mma_f16_16816(a.o[mt], a0, a1, a2, a3, bl0, bl1);
-          }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == p.stages) {
+      if (++stage == nstages) {
         stage = 0;
         ++round;
       }
     }
-    finish_segment<KIND, D>(p, s, a, red_o, red_ml, misc, pre, plan);
+    finish_segment<KIND, D, GROUPS>(p, s, a, red_o, red_ml, misc, pre, plan);
   }
 }
 
 // ================================================================ kernel
-template <int KIND, int D>
-__global__ void __launch_bounds__(kThreads, 1) decode_attn_kernel(const __grid_constant__ KParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+template <int KIND, int D, int GROUPS>
+__global__ void __launch_bounds__(cta_threads(GROUPS), 1)
+    decode_attn_kernel(const __grid_constant__ KParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  // 1024-aligned base (128-byte TMA swizzle atoms), by pointer arithmetic so
+  // the compiler keeps the shared address space.
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int nplan = (p.sched == SCHED_SPLIT) ? 1 : p.B;
-  const SmemLayout L = make_layout(KIND, D, p.NH, p.Hkv, p.stages, nplan);
+  const SmemLayout L = make_layout(KIND, D, p.NH, p.Hkv, p.stages, nplan, GROUPS);
   uint8_t* stages = base + L.off_stages;
+  uint8_t* qring = base + L.off_q;
   float* red_o = reinterpret_cast<float*>(base + L.off_red_o);
   float* red_ml = reinterpret_cast<float*>(base + L.off_red_ml);
   SeqPlan* plan = reinterpret_cast<SeqPlan*>(base + L.off_plan);
   int* pre = reinterpret_cast<int*>(base + L.off_pre);
   uint64_t* full = reinterpret_cast<uint64_t*>(base + L.off_bar);
   uint64_t* empty = full + p.stages;
+  uint64_t* qfull = empty + p.stages;
+  uint64_t* qempty = qfull + 2;
   Misc* misc = reinterpret_cast<Misc*>(base + L.off_misc);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  constexpr int NCW = consumer_warps(GROUPS);
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], kGroupWarps);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&qfull[s], 1);
+      mbar_init(&qempty[s], NCW);
     }
     fence_mbarrier_init();
     misc->flags = 0;
     misc->ticket = 0;
     misc->abort = 0;
   }
-  if (warp == kConsumerWarps && (tid & 31) == 0) {
+  if (warp == NCW && (tid & 31) == 0) {
     prefetch_tensormap(&p.tm_k);
     prefetch_tensormap(&p.tm_v);
     if (KIND == KIND_TIERED) {
@@ -819,7 +1114,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_attn_kernel(const __grid_c
         fl |= DEV_SPLIT_OVERFLOW;
     }
   } else {
-    for (int b = tid; b < p.B; b += kThreads) {
+    for (int b = tid; b < p.B; b += cta_threads(GROUPS)) {
       int f = plan_sequence<KIND>(p, b, plan[b]);
       if (b % p.grid == (int)blockIdx.x) fl |= f;  // report once per sequence
     }
@@ -829,10 +1124,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_attn_kernel(const __grid_c
   if (p.sched != SCHED_SPLIT && warp == 0) plan_prefix(plan, pre, p.B, p.Hkv * p.HG, tid & 31);
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
-    producer_loop<KIND, D>(p, plan, pre, stages, L, full, empty, misc);
+  if (warp == NCW) {
+    producer_loop<KIND, D>(p, plan, pre, stages, qring, L, full, empty, qfull, qempty, misc);
   } else {
-    consumer_loop<KIND, D>(p, plan, pre, stages, L, full, empty, red_o, red_ml, misc);
+    consumer_loop<KIND, D, GROUPS>(p, plan, pre, stages, qring, L, full, empty, qfull, qempty,
+                                   red_o, red_ml, misc);
   }
   __syncthreads();
   if (tid == 0 && misc->flags && p.dev_status) atomicOr(p.dev_status, misc->flags);

@@ -5,19 +5,19 @@
 
 namespace da {
 
-template <int KIND, int D>
+template <int KIND, int D, int GROUPS>
 cudaError_t launch_decode_impl(const KParams& p, dim3 grid, int smem, cudaStream_t stream) {
   static int configured[128] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 0 && dev < 128 && !configured[dev]) {
-    err = cudaFuncSetAttribute(decode_attn_kernel<KIND, D>,
+    err = cudaFuncSetAttribute(decode_attn_kernel<KIND, D, GROUPS>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (err != cudaSuccess) return err;
     configured[dev] = 1;
   }
-  decode_attn_kernel<KIND, D><<<grid, kThreads, smem, stream>>>(p);
+  decode_attn_kernel<KIND, D, GROUPS><<<grid, cta_threads(GROUPS), smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -27,9 +27,9 @@ cudaError_t launch_decode(int kind, int D, const KParams& p, dim3 grid, int smem
                           cudaStream_t stream) {
   if (kind == KIND_TIERED) return launch_tiered(D, p, grid, smem, stream);
   switch (D) {
-    case 64: return launch_decode_impl<KIND_PAGED, 64>(p, grid, smem, stream);
-    case 128: return launch_decode_impl<KIND_PAGED, 128>(p, grid, smem, stream);
-    case 256: return launch_decode_impl<KIND_PAGED, 256>(p, grid, smem, stream);
+    case 64: return launch_decode_impl<KIND_PAGED, 64, 2>(p, grid, smem, stream);
+    case 128: return launch_decode_impl<KIND_PAGED, 128, 2>(p, grid, smem, stream);
+    case 256: return launch_decode_impl<KIND_PAGED, 256, 1>(p, grid, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -8,13 +8,19 @@
 namespace da {
 
 constexpr int kTile = 64;          // keys per pipeline stage
-constexpr int kConsumerWarps = 4;  // each takes 16 keys of a stage
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kGroupWarps = 4;     // consumer warps of a group; each takes 16 keys of a stage
 constexpr int kHeadTile = 8;       // query heads per work unit (the MMA n dimension)
 constexpr int kMaxStages = 8;
 constexpr int kMaxBatchPerLaunch = 256;  // per-sequence plan lives in shared memory
 constexpr int kSmemLimit = 232448;       // 227 KB opt-in per block on sm_100-class parts
 constexpr uint32_t kRedBarrier = 1;      // named barrier id for the consumer warps
+
+// Consumer warps and threads of a CTA with `groups` consumer groups (group g
+// takes the stages s with s % groups == g) plus one producer warp.
+__host__ __device__ constexpr int consumer_warps(int groups) { return kGroupWarps * groups; }
+__host__ __device__ constexpr int cta_threads(int groups) {
+  return (consumer_warps(groups) + 1) * 32;
+}
 
 enum Kind : int { KIND_PAGED = 0, KIND_TIERED = 1 };
 // STREAM: every CTA takes an equal share of the concatenated key tiles of all
@@ -63,7 +69,7 @@ struct alignas(128) KParams {
   // STREAM workspace
   float* ws_o;      // [grid][2][kHeadTile][D]
   float* ws_lse;    // [grid][2][kHeadTile]
-  int* ws_cnt;      // [B * Hkv * HG] tickets, zero between calls
+  int* ws_cnt;      // [grid] tickets (one per CTA that starts a cut unit), zero between calls
 
   // SPLIT outputs
   int split_tokens, max_splits;
@@ -95,8 +101,9 @@ struct SeqPlan {
 
 struct SmemLayout {
   int stage_bytes;
-  int off_k, off_v, off_q, off_sc, off_hdr;  // inside a stage
-  int off_stages;  // from the 1024-aligned base
+  int off_k, off_v, off_sc, off_hdr;  // inside a stage
+  int off_stages;                     // from the 1024-aligned base
+  int q_slot_bytes, off_q;            // two-slot Q ring
   int off_red_o, off_red_ml;
   int off_plan, off_pre;
   int off_bar, off_misc;
@@ -106,22 +113,24 @@ struct SmemLayout {
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline SmemLayout make_layout(int kind, int D, int NH, int Hkv, int stages,
-                                                  int B) {
+                                                  int B, int groups) {
   SmemLayout L;
   const int kv_region = kTile * D * 2;  // f16 rows (int8 cold rows use the first half)
   L.off_k = 0;
   L.off_v = kv_region;
-  L.off_q = 2 * kv_region;
-  L.off_sc = L.off_q + align_up(NH * D * 4, 128);
+  L.off_sc = 2 * kv_region;
   const int sc_bytes = (kind == KIND_TIERED) ? align_up(2 * kTile * Hkv * 2, 128) : 0;
   L.off_hdr = L.off_sc + sc_bytes;
   L.stage_bytes = align_up(L.off_hdr + 16, 1024);
   L.off_stages = 0;
   int off = stages * L.stage_bytes;
+  L.q_slot_bytes = align_up(NH * D * 4, 128);
+  L.off_q = off;
+  off += 2 * L.q_slot_bytes;
   L.off_red_o = off;
-  off += kConsumerWarps * NH * D * 4;
+  off += consumer_warps(groups) * NH * D * 4;
   L.off_red_ml = off;
-  off += kConsumerWarps * NH * 2 * 4;
+  off += consumer_warps(groups) * NH * 2 * 4;
   off = align_up(off, 16);
   L.off_plan = off;
   off += B * (int)sizeof(SeqPlan);
@@ -129,7 +138,7 @@ __host__ __device__ inline SmemLayout make_layout(int kind, int D, int NH, int H
   off += (B + 1) * 4;
   off = align_up(off, 8);
   L.off_bar = off;
-  off += 2 * stages * 8;
+  off += (2 * stages + 4) * 8;  // full[stages], empty[stages], qfull[2], qempty[2]
   L.off_misc = off;
   off += 64;
   L.total = off + 1024;

@@ -7,9 +7,13 @@
 
 namespace da {
 
+// Consumer groups of the decode kernel for head dimension D (two groups
+// need about 180 registers per thread; D = 256 keeps one).
+inline int decode_groups(int D) { return D <= 128 ? 2 : 1; }
+
 // Launches the decode kernel of `kind` for head dimension D (64/128/256 for
-// paged, 128/256 for tiered).  Returns cudaErrorInvalidValue for a D that has
-// no instantiation.
+// paged, 128/256 for tiered) with decode_groups(D) consumer groups.  Returns
+// cudaErrorInvalidValue for a D that has no instantiation.
 cudaError_t launch_decode(int kind, int D, const KParams& p, dim3 grid, int smem_bytes,
                           cudaStream_t stream);
 

@@ -35,6 +35,9 @@ _S_K, _S_V, _S_OUTLIER, _S_Q, _S_META = 0, 1, 2, 3, 4
 _GLOBAL = 1 << 30  # "sequence" index used for batch-wide draws
 
 WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx")
+# Same keys and values as "paged", in a pool holding exactly the used pages
+# (about 310 MB instead of 4 GiB of device memory): for profiler captures.
+VARIANTS = ("paged_compact",)
 
 
 def _rng(seed: int, seq: int, stream: int) -> np.random.Generator:
@@ -202,6 +205,11 @@ def workload(name: str):
         lens = meta.integers(512, 4096, size=32, endpoint=True)
         return make_paged("paged", 1, B=32, Hq=32, Hkv=8, D=128, block_size=16, seq_lens=lens,
                           num_blocks=65536, max_blocks=256)
+    if name == "paged_compact":
+        meta = _rng(1, _GLOBAL, _S_META + 1)
+        lens = meta.integers(512, 4096, size=32, endpoint=True)
+        return make_paged("paged_compact", 1, B=32, Hq=32, Hkv=8, D=128, block_size=16,
+                          seq_lens=lens, max_blocks=256)
     if name == "tiered":
         return make_tiered("tiered", 2, B=16, Hq=32, Hkv=8, D=128, block_size=16,
                            cold_len=7168, hot_len=1024, hot_window=1024, hot_start=7168)
@@ -320,8 +328,9 @@ class TieredCase:
             for b, enc in zip(todo, ex.map(self.seq_encoded, todo)):
                 kw, vw, ks, vs, kh, vh = enc
                 pages = self.block_table[b, :int(self.pages_per_seq[b])].astype(np.int64)
-                k_cold[pages], v_cold[pages] = kw, vw
-                k_scale[pages], v_scale[pages] = ks, vs
+                ok = (pages >= 0) & (pages < self.num_blocks)  # a corrupted entry holds no data
+                k_cold[pages[ok]], v_cold[pages[ok]] = kw[ok], vw[ok]
+                k_scale[pages[ok]], v_scale[pages[ok]] = ks[ok], vs[ok]
                 slots = self._hot_slots(b)
                 k_hot[b, slots] = kh
                 v_hot[b, slots] = vh
@@ -332,6 +341,8 @@ class TieredCase:
         import torch
 
         h = self.host_arrays()
+        for k in ("k_cold", "v_cold"):
+            h[k] = h[k].view(np.int32)  # the same 32-bit words, as a torch-friendly dtype
         t = {k: torch.from_numpy(v).to(device) for k, v in h.items()}
         t["q"] = torch.from_numpy(self.q).to(device)
         t["block_table"] = torch.from_numpy(self.block_table).to(device)

@@ -56,3 +56,34 @@ def run_paged(case, t, mode, split_tokens=256, dev_status=None):
         out, lse = qk.decode_attn_split_merge(op, lp)
     torch.cuda.synchronize()
     return out.cpu().numpy(), lse.cpu().numpy()
+
+
+def oracle_tiered(case, rows=None):
+    seqs = None if rows is None else sorted({int(r) // case.Hq for r in rows})
+    h = case.host_arrays(seqs)
+    return oracle.decode_tiered(case.q, h["k_hot"], h["v_hot"], h["k_cold"], h["v_cold"],
+                                h["k_scale"], h["v_scale"], case.block_table, case.cold_lens,
+                                case.hot_lens, case.hot_starts, hot_window=case.hot_window,
+                                q_pos=case.q_pos, scale=case.scale, softcap=case.softcap,
+                                sliding_window=case.sliding_window, causal=case.causal, rows=rows)
+
+
+def run_tiered(case, t, mode, per_seq=None, dev_status=None):
+    """CUDA tiered path; ``per_seq`` passes the tier lengths as device arrays
+    (default: arrays unless every sequence has the same lengths)."""
+    import torch
+    if per_seq is None:
+        per_seq = not case.uniform
+    kw = dict(scale=case.scale, softcap=case.softcap, sliding_window=case.sliding_window,
+              causal=case.causal, hot_window=case.hot_window, max_seq_len=case.max_seq_len)
+    if per_seq:
+        kw.update(cold_lens=t["cold_lens"], hot_lens=t["hot_lens"], hot_starts=t["hot_starts"])
+    else:
+        kw.update(cold_len=int(case.cold_lens[0]), hot_len=int(case.hot_lens[0]),
+                  hot_start=int(case.hot_starts[0]))
+    out, lse = qk.decode_attn_tiered_int8(
+        t["q"], t["k_hot"], t["v_hot"], t["k_cold"], t["v_cold"], t["k_scale"], t["v_scale"],
+        t["block_table"], q_pos=t["q_pos"], workspace="auto" if mode == "stream" else None,
+        dev_status=dev_status, **kw)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), lse.cpu().numpy()

@@ -183,3 +183,22 @@ def test_full_size_workloads_sampled_rows(name):
         assert_parity(out, lse, ref_out, ref_lse, f"{name}/{mode}")
     del t
     torch.cuda.empty_cache()
+
+
+def test_workspace_reuse_across_shapes():
+    """One zero-filled workspace serves calls of different head dims and
+    batch shapes: only its leading ticket counters must stay zero."""
+    import torch
+    big = _case(1200, 256, 8, 2, 16, [777, 511, 129, 64, 3])
+    params = qk.make_params(torch.empty(big.B, big.Hq, big.D), big.block_size, big.Hkv,
+                            big.max_blocks, big.num_blocks, max_seq_len=big.max_seq_len)
+    ws = torch.zeros(qk.decode_attn_workspace_size(params), dtype=torch.uint8, device="cuda")
+    cases = [big, _case(1201, 64, 8, 2, 16, EDGE_LENS), _case(1202, 128, 8, 4, 32, [900, 5, 300]),
+             big]
+    for case in cases:
+        t = case.device_tensors("cuda")
+        out, lse = qk.decode_attn_paged(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                        t["seq_lens"], max_seq_len=case.max_seq_len, workspace=ws)
+        ref_out, ref_lse, _ = oracle_paged(case)
+        assert_parity(out.cpu().numpy().reshape(-1, case.D), lse.cpu().numpy().reshape(-1),
+                      ref_out, ref_lse, f"reuse/{case.name}")
