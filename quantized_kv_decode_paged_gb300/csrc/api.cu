@@ -116,37 +116,65 @@ void fill_common(KParams& k, const da_params* p) {
   k.softcap2 = p->softcap > 0.f ? p->softcap * 1.4426950408889634f : 0.f;
   k.window = p->sliding_window;
   k.causal = p->causal;
+  k.KVB = da::decode_kvb(da::KIND_PAGED, p->head_dim, p->num_kv_heads);
 }
 
-// 3-D map over a [rows, Hkv, inner] array (inner contiguous): box
-// {box_inner, 1, box_rows}, 128-byte swizzle.
-int encode_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
-                    long long inner, long long heads, long long rows, int box_inner,
-                    int box_rows) {
+int encode_pool_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+                    long long D, long long heads, long long rows, int box_rows, int kvb);
+
+// K/V pool maps of a paged (f16) or cold (int8) cache for the chosen KVB.
+int encode_paged_maps(KParams& k, int kind, const void* kp, const void* vp, const da_params* p) {
+  const da::GeoInfo g = da::decode_geo(kind, p->head_dim, k.KVB);
+  if (g.W == 0) return DA_ERR_UNSUPPORTED;
+  const int box_rows = p->block_size < g.TOK ? p->block_size : g.TOK;
+  const long long rows = (long long)p->num_blocks * p->block_size;
+  const CUtensorMapDataType dt =
+      kind == da::KIND_PAGED ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const int esize = kind == da::KIND_PAGED ? 2 : 1;
+  int st = encode_pool_map(&k.tm_k, kp, dt, esize, p->head_dim, p->num_kv_heads, rows, box_rows,
+                           k.KVB);
+  if (st != DA_OK) return st;
+  return encode_pool_map(&k.tm_v, vp, dt, esize, p->head_dim, p->num_kv_heads, rows, box_rows,
+                         k.KVB);
+}
+
+// 4-D map over a paged pool [rows, Hkv, D] of esize-byte elements with the
+// token dimension inside the (128-byte slice, kv head) dimensions:
+//   dims {128/esize, rows, D*esize/128, Hkv}, strides {Hkv*D*esize, 128, D*esize},
+//   box  {128/esize, box_rows, D*esize/128, kvb},
+// so one box holds box_rows keys of kvb heads and all of D, laid out
+// [head][slice][key][128 bytes] with the 128-byte swizzle.
+int encode_pool_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+                    long long D, long long heads, long long rows, int box_rows, int kvb) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return DA_ERR_CUDA;
-  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)(inner * elem_bytes), (cuuint64_t)(inner * heads * elem_bytes)};
-  cuuint32_t box[3] = {(cuuint32_t)box_inner, 1u, (cuuint32_t)box_rows};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const long long row_bytes = D * esize;
+  cuuint64_t dims[4] = {(cuuint64_t)(128 / esize), (cuuint64_t)rows, (cuuint64_t)(row_bytes / 128),
+                        (cuuint64_t)heads};
+  cuuint64_t strides[3] = {(cuuint64_t)(heads * row_bytes), 128, (cuuint64_t)row_bytes};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_rows,
+                       (cuuint32_t)(row_bytes / 128), (cuuint32_t)kvb};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = fn(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
-// 4-D map over the hot ring [B, cap, Hkv, D] f16: box {64, 1, 64, 1}.
+// 5-D map over the hot ring [B, cap, Hkv, D] f16, token dimension inside:
+//   dims {64, cap, D/64, Hkv, B}, box {64, box_rows, D/64, kvb, 1}.
 int encode_ring_map(CUtensorMap* m, const void* base, long long D, long long heads, long long cap,
-                    long long B) {
+                    long long B, int box_rows, int kvb) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return DA_ERR_CUDA;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)cap, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)(D * 2), (cuuint64_t)(D * heads * 2),
-                           (cuuint64_t)(D * heads * cap * 2)};
-  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)da::kTile, 1u};
-  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  cuuint64_t dims[5] = {64, (cuuint64_t)cap, (cuuint64_t)(D / 64), (cuuint64_t)heads,
+                        (cuuint64_t)B};
+  cuuint64_t strides[4] = {(cuuint64_t)(heads * D * 2), 128, (cuuint64_t)(D * 2),
+                           (cuuint64_t)(cap * heads * D * 2)};
+  cuuint32_t box[5] = {64u, (cuuint32_t)box_rows, (cuuint32_t)(D / 64), (cuuint32_t)kvb, 1u};
+  cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
@@ -162,12 +190,11 @@ int max_stages() {
   return da::kMaxStages;
 }
 
-// Largest stage count that fits in shared memory, a multiple of the
-// consumer groups (each group owns every groups-th stage), or 0.
-int pick_stages(int kind, int D, int NH, int Hkv, int nplan, int* smem_out) {
-  const int groups = da::decode_groups(D);
-  for (int s = max_stages() / groups * groups; s >= 2; s -= groups) {
-    SmemLayout L = da::make_layout(kind, D, NH, Hkv, s, nplan, groups);
+// Largest stage count (>= 2) whose layout fits in shared memory, or 0.
+int pick_stages(int kind, int D, int KVB, const da::GeoInfo& g, int NH, int Hkv, int nplan,
+                int* smem_out) {
+  for (int s = max_stages(); s >= 2; --s) {
+    SmemLayout L = da::make_layout(kind, D, KVB, g.W, g.REGION, g.TOK, NH, Hkv, s, nplan);
     if (L.total <= da::kSmemLimit) {
       *smem_out = L.total;
       return s;
@@ -184,14 +211,21 @@ struct WsLayout {
   size_t cnt_off, lse_off, o_off, total;
 };
 
-WsLayout ws_layout(int grid, int D) {
+WsLayout ws_layout(int grid, int D, int kvb) {
   WsLayout w;
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
   w.cnt_off = 0;
   w.lse_off = al((size_t)grid * 4);
-  w.o_off = w.lse_off + al((size_t)grid * 2 * da::kHeadTile * 4);
-  w.total = w.o_off + al((size_t)grid * 2 * da::kHeadTile * D * 4);
+  w.o_off = w.lse_off + al((size_t)grid * 2 * kvb * da::kHeadTile * 4);
+  w.total = w.o_off + al((size_t)grid * 2 * kvb * da::kHeadTile * D * 4);
   return w;
+}
+
+// kv heads per unit the workspace must serve (either cache kind).
+int ws_kvb(const da_params* p) {
+  const int a = da::decode_kvb(da::KIND_PAGED, p->head_dim, p->num_kv_heads);
+  const int b = da::decode_kvb(da::KIND_TIERED, p->head_dim, p->num_kv_heads);
+  return a > b ? a : b;
 }
 
 struct Launch {
@@ -219,16 +253,18 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
     return DA_ERR_INVALID;
   }
   const int grid_max = sms;
-  const WsLayout w = ws_layout(grid_max, p->head_dim);
+  const WsLayout w = ws_layout(grid_max, p->head_dim, ws_kvb(p));
   for (int b0 = 0; b0 < p->batch; b0 += da::kMaxBatchPerLaunch) {
     const int nb = (p->batch - b0) < da::kMaxBatchPerLaunch ? (p->batch - b0)
                                                              : da::kMaxBatchPerLaunch;
     KParams k = base;
     k.B = nb;
     offset_chunk(k, b0);
-    const int units = nb * k.Hkv * k.HG;
+    const int units = nb * (k.Hkv / k.KVB) * k.HG;
+    const da::GeoInfo g = da::decode_geo(lc.kind, k.D, k.KVB);
+    if (g.W == 0) return DA_ERR_UNSUPPORTED;
     int smem = 0;
-    k.stages = pick_stages(lc.kind, k.D, k.NH, k.Hkv, nb, &smem);
+    k.stages = pick_stages(lc.kind, k.D, k.KVB, g, k.NH, k.Hkv, nb, &smem);
     if (k.stages == 0) return DA_ERR_UNSUPPORTED;
     int grid;
     if (use_ws) {
@@ -236,7 +272,7 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
       grid = grid_max;
       if (p->max_seq_len > 0) {
         // never more CTAs than key tiles
-        const long long tiles = (long long)units * ((p->max_seq_len + da::kTile - 1) / da::kTile + 1);
+        const long long tiles = (long long)units * ((p->max_seq_len + g.TOK - 1) / g.TOK + 1);
         if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
       }
       k.ws_o = reinterpret_cast<float*>(static_cast<char*>(lc.workspace) + w.o_off);
@@ -248,7 +284,7 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
       if (grid < 1) grid = 1;
     }
     k.grid = grid;
-    cudaError_t e = da::launch_decode(lc.kind, k.D, k, dim3(grid), smem, stream);
+    cudaError_t e = da::launch_decode(lc.kind, k.D, k.KVB, k, dim3(grid), smem, stream);
     if (e != cudaSuccess) return DA_ERR_CUDA;
   }
   return DA_OK;
@@ -273,7 +309,7 @@ size_t decode_attn_workspace_size(const da_params* p) {
   if (check_params(p, false) != DA_OK && check_params(p, true) != DA_OK) return 0;
   int sms = 0;
   if (device_sms(&sms) != DA_OK) return 0;
-  return ws_layout(sms, p->head_dim).total;
+  return ws_layout(sms, p->head_dim, ws_kvb(p)).total;
 }
 
 int decode_attn_workspace_init(void* workspace, size_t bytes, void* stream) {
@@ -301,13 +337,7 @@ int decode_attn_paged(const da_params* p, const float* q, const uint16_t* k_pool
   KParams k;
   memset(&k, 0, sizeof(k));
   fill_common(k, p);
-  const int rows_box = p->block_size < da::kTile ? p->block_size : da::kTile;
-  const long long rows = (long long)p->num_blocks * p->block_size;
-  st = encode_rows_map(&k.tm_k, k_pool, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p->head_dim,
-                       p->num_kv_heads, rows, 64, rows_box);
-  if (st != DA_OK) return st;
-  st = encode_rows_map(&k.tm_v, v_pool, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p->head_dim,
-                       p->num_kv_heads, rows, 64, rows_box);
+  st = encode_paged_maps(k, da::KIND_PAGED, k_pool, v_pool, p);
   if (st != DA_OK) return st;
   k.dev_status = dev_status;
   Launch lc{da::KIND_PAGED, p, workspace, workspace_bytes};
@@ -344,25 +374,21 @@ int decode_attn_split_partial(const da_params* p, int32_t split_tokens, int32_t 
   KParams k;
   memset(&k, 0, sizeof(k));
   fill_common(k, p);
-  const int rows_box = p->block_size < da::kTile ? p->block_size : da::kTile;
-  const long long rows = (long long)p->num_blocks * p->block_size;
-  st = encode_rows_map(&k.tm_k, k_pool, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p->head_dim,
-                       p->num_kv_heads, rows, 64, rows_box);
-  if (st != DA_OK) return st;
-  st = encode_rows_map(&k.tm_v, v_pool, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p->head_dim,
-                       p->num_kv_heads, rows, 64, rows_box);
+  st = encode_paged_maps(k, da::KIND_PAGED, k_pool, v_pool, p);
   if (st != DA_OK) return st;
   k.dev_status = dev_status;
   k.sched = da::SCHED_SPLIT;
   k.split_tokens = split_tokens;
   k.max_splits = max_splits;
+  const da::GeoInfo g = da::decode_geo(da::KIND_PAGED, k.D, k.KVB);
+  if (g.W == 0) return DA_ERR_UNSUPPORTED;
   int smem = 0;
-  k.stages = pick_stages(da::KIND_PAGED, k.D, k.NH, k.Hkv, 1, &smem);
+  k.stages = pick_stages(da::KIND_PAGED, k.D, k.KVB, g, k.NH, k.Hkv, 1, &smem);
   if (k.stages == 0) return DA_ERR_UNSUPPORTED;
-  const long long units_total = (long long)p->batch * k.Hkv * k.HG;
+  const long long units_total = (long long)p->batch * (k.Hkv / k.KVB) * k.HG;
   const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
   // grid.y is limited to 65535 units per launch: chunk whole sequences
-  const int upb = k.Hkv * k.HG;
+  const int upb = (k.Hkv / k.KVB) * k.HG;
   const int seqs_per_launch = 65535 / upb > 0 ? 65535 / upb : 1;
   if (upb > 65535) return DA_ERR_UNSUPPORTED;
   (void)units_total;
@@ -377,7 +403,7 @@ int decode_attn_split_partial(const da_params* p, int32_t split_tokens, int32_t 
     kk.o_part = o_part + (long long)b0 * Hq * max_splits * D;
     kk.lse_part = lse_part + (long long)b0 * Hq * max_splits;
     kk.grid = max_splits;
-    cudaError_t e = da::launch_decode(da::KIND_PAGED, kk.D, kk, dim3(max_splits, nb * upb), smem,
+    cudaError_t e = da::launch_decode(da::KIND_PAGED, kk.D, kk.KVB, kk, dim3(max_splits, nb * upb), smem,
                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return DA_ERR_CUDA;
   }
@@ -430,18 +456,19 @@ int decode_attn_tiered_int8(const da_params* p, const da_tier_params* t, const f
   KParams k;
   memset(&k, 0, sizeof(k));
   fill_common(k, p);
-  const int rows_box = p->block_size < da::kTile ? p->block_size : da::kTile;
-  const long long rows = (long long)p->num_blocks * p->block_size;
-  st = encode_rows_map(&k.tm_k, k_cold, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->head_dim,
-                       p->num_kv_heads, rows, 128, rows_box);
+  k.KVB = da::decode_kvb(da::KIND_TIERED, p->head_dim, p->num_kv_heads);
+  st = encode_paged_maps(k, da::KIND_TIERED, k_cold, v_cold, p);
   if (st != DA_OK) return st;
-  st = encode_rows_map(&k.tm_v, v_cold, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->head_dim,
-                       p->num_kv_heads, rows, 128, rows_box);
-  if (st != DA_OK) return st;
-  st = encode_ring_map(&k.tm_kh, k_hot, p->head_dim, p->num_kv_heads, t->hot_capacity, p->batch);
-  if (st != DA_OK) return st;
-  st = encode_ring_map(&k.tm_vh, v_hot, p->head_dim, p->num_kv_heads, t->hot_capacity, p->batch);
-  if (st != DA_OK) return st;
+  {
+    const da::GeoInfo g = da::decode_geo(da::KIND_TIERED, k.D, k.KVB);
+    if (g.W == 0) return DA_ERR_UNSUPPORTED;
+    st = encode_ring_map(&k.tm_kh, k_hot, p->head_dim, p->num_kv_heads, t->hot_capacity,
+                         p->batch, g.TOKH, k.KVB);
+    if (st != DA_OK) return st;
+    st = encode_ring_map(&k.tm_vh, v_hot, p->head_dim, p->num_kv_heads, t->hot_capacity,
+                         p->batch, g.TOKH, k.KVB);
+    if (st != DA_OK) return st;
+  }
   k.dev_status = dev_status;
   k.k_scale = k_scale;
   k.v_scale = v_scale;

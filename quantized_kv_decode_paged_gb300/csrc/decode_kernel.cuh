@@ -13,21 +13,24 @@
 //   read_cold_k / get_hot_pos).
 //
 // How (GB300 design, not the pages' WGSL):
-//   * A work unit is (sequence, kv head, group of <= 8 query heads).  All
-//     heads of the group share every K/V byte read from HBM: the group is the
-//     n = 8 dimension of mma.m16n8k16, so QK^T is S^T[16 keys x 8 heads] =
+//   * A work unit is (sequence, block of KVB kv heads, group of <= 8 query
+//     heads per kv head).  The KVB heads make every token row read from the
+//     pool at least 512 contiguous bytes (Geo in kernel_params.h), and the
+//     query heads of one kv head share each K/V byte: they are the n = 8
+//     dimension of mma.m16n8k16, so QK^T is S^T[16 keys x 8 heads] =
 //     K[16 x D] * Q^T and PV is O^T[D x 8] += V^T[D x 16] * P^T[16 x 8].
 //   * f32 Q and P enter the f16 tensor cores as hi + lo f16 pairs, so the
 //     products keep ~22 bits; accumulation is f32.  int8 values become exact
 //     f16 integers (byte bias + magic-number subtraction); the per-key
 //     scales multiply the score (K) and fold into the weight (V).
-//   * One producer warp streams 64-key stages through TMA (3-D tensor maps
-//     over the pool, one box per page and 128-byte slice of a row, 128-byte
-//     swizzle) into a ring of shared-memory stages guarded by mbarriers.
-//     GROUPS groups of four consumer warps alternate stages (group g owns
-//     the stages s with s % GROUPS == g); in a stage each warp takes 16 keys
-//     and keeps its own online-softmax state, merged through shared memory
-//     at the end of a unit.  Q arrives through its own two-slot ring.
+//   * One producer warp streams tiles through TMA into a ring of shared-
+//     memory stages guarded by mbarriers.  The tensor maps put the token
+//     dimension inside the (128-byte slice, kv head) dimensions, so one box
+//     per page covers KVB heads x all of D, and the 128-byte swizzle keeps
+//     eight consecutive keys of one slice in distinct banks.  Each consumer
+//     warp owns one kv head of the block and 16-key groups of every tile,
+//     with its own online-softmax state; the warps of a head merge their
+//     states through a register-level tree at the end of a unit.
 //   * Stream-K split-KV: the key tiles of all units are concatenated and cut
 //     into one equal share per CTA.  A unit cut between CTAs leaves partial
 //     (o, lse) states in the workspace; the last CTA to finish the unit
@@ -47,11 +50,11 @@ enum { DEST_OUT = 0, DEST_PARTIAL = 1, DEST_SPLIT = 2 };
 enum { TK_PAGED = 0, TK_COLD = 1, TK_HOT = 2 };
 
 struct Seg {
-  int b, kv, hg, unit;
-  int i0, i1;    // unit-local tile range
-  int vlo, vhi;  // visible absolute key positions of this segment
+  int b, kvb, hg, unit;  // kvb: index of the kv-head block
+  int i0, i1;            // unit-local tile range
+  int vlo, vhi;          // visible absolute key positions of this segment
   int dest, slot;
-  int pidx;      // index of b's plan entry
+  int pidx;              // index of b's plan entry
 };
 
 struct SegIter {
@@ -62,7 +65,6 @@ struct SegIter {
 struct Misc {
   int flags;
   int ticket;
-  int abort;
 };
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -77,20 +79,23 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ float lds_f32(uint32_t addr) { return __uint_as_float(lds32(addr)); }
-
 __device__ __forceinline__ uint16_t lds16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
   return v;
 }
 
+__device__ __forceinline__ void sts128_zero(uint32_t addr) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
 // ------------------------------------------------------------------ plan
 __device__ __forceinline__ int ceil_div_i(long long a, int b) { return (int)((a + b - 1) / b); }
 
-// Fills plan entry `e` for sequence b (lengths validated, visible range,
-// tile counts); returns device-status bits.
-template <int KIND>
+// Plan of sequence b (lengths validated, visible range, tile counts for
+// paged / cold tiles of TOK keys and hot tiles of TOKH slots); returns
+// device-status bits.
+template <int KIND, int TOK, int TOKH>
 __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e) {
   int flags = 0;
   const long long cap = (long long)p.max_blocks * p.bs;
@@ -138,8 +143,8 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
     long long vh = hi < L ? hi : L;
     e.hi = (int)vh;
     if (vh > lo) {
-      e.t0 = (int)(lo / kTile);
-      e.ntiles = ceil_div_i(vh, kTile) - e.t0;
+      e.t0 = (int)(lo / TOK);
+      e.ntiles = ceil_div_i(vh, TOK) - e.t0;
     }
   } else {
     e.cold_len = (int)cl;
@@ -147,8 +152,8 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
     e.hot_len = (int)hl;
     long long ch = hi < cl ? hi : cl;
     if (ch > lo) {
-      e.t0 = (int)(lo / kTile);
-      e.ncold = ceil_div_i(ch, kTile) - e.t0;
+      e.t0 = (int)(lo / TOK);
+      e.ncold = ceil_div_i(ch, TOK) - e.t0;
     }
     long long j0 = lo - hs > 0 ? lo - hs : 0;
     long long j1 = hi - hs < hl ? hi - hs : hl;
@@ -157,15 +162,15 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
       if (p.hot_window > 0) {
         // visible ring slots: [s0, s0 + n) modulo W, as one or two tile runs
         const int W = p.hot_window;
-        const int nT = ceil_div_i(W, kTile);
+        const int nT = ceil_div_i(W, TOKH);
         long long s0 = (hs + j0) % W;
         long long n = j1 - j0;
         if (s0 + n <= W) {
-          e.ha0 = (int)(s0 / kTile);
-          e.ha1 = ceil_div_i(s0 + n, kTile);
+          e.ha0 = (int)(s0 / TOKH);
+          e.ha1 = ceil_div_i(s0 + n, TOKH);
         } else {
-          int te = ceil_div_i(s0 + n - W, kTile);
-          int ts = (int)(s0 / kTile);
+          int te = ceil_div_i(s0 + n - W, TOKH);
+          int ts = (int)(s0 / TOKH);
           if (te > ts) {
             e.ha0 = 0;
             e.ha1 = nT;
@@ -177,8 +182,8 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
           }
         }
       } else {
-        e.ha0 = (int)(j0 / kTile);
-        e.ha1 = ceil_div_i(j1, kTile);
+        e.ha0 = (int)(j0 / TOKH);
+        e.ha1 = ceil_div_i(j1, TOKH);
       }
       nhot = (e.ha1 - e.ha0) + (e.hb1 - e.hb0);
     }
@@ -187,14 +192,51 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
   return flags;
 }
 
+// Shared-memory plan storage: 4 ints per sequence for paged kernels, the
+// whole SeqPlan for tiered ones.
+template <int KIND>
+struct PlanStore {
+  uint8_t* base;
+  __device__ __forceinline__ void put(int b, const SeqPlan& e) const {
+    if constexpr (KIND == KIND_PAGED) {
+      reinterpret_cast<SeqPlanPaged*>(base)[b] = SeqPlanPaged{e.lo, e.hi, e.t0, e.ntiles};
+    } else {
+      reinterpret_cast<SeqPlan*>(base)[b] = e;
+    }
+  }
+  __device__ __forceinline__ SeqPlan get(int b) const {
+    SeqPlan e;
+    if constexpr (KIND == KIND_PAGED) {
+      const SeqPlanPaged s = reinterpret_cast<const SeqPlanPaged*>(base)[b];
+      e.lo = s.lo;
+      e.hi = s.hi;
+      e.t0 = s.t0;
+      e.ntiles = s.ntiles;
+      e.ncold = s.ntiles;
+      e.hot_start = e.hot_len = e.ha0 = e.ha1 = e.hb0 = e.hb1 = e.cold_len = 0;
+    } else {
+      e = reinterpret_cast<const SeqPlan*>(base)[b];
+    }
+    return e;
+  }
+  __device__ __forceinline__ int ntiles(int b) const {
+    if constexpr (KIND == KIND_PAGED) {
+      return reinterpret_cast<const SeqPlanPaged*>(base)[b].ntiles;
+    } else {
+      return reinterpret_cast<const SeqPlan*>(base)[b].ntiles;
+    }
+  }
+};
+
 // Exclusive prefix of ntiles * units_per_seq over the batch (one warp).
-__device__ __forceinline__ void plan_prefix(const SeqPlan* plan, int* pre, int B, int upb,
+template <int KIND>
+__device__ __forceinline__ void plan_prefix(const PlanStore<KIND>& plan, int* pre, int B, int upb,
                                             int lane) {
   const int per = (B + 31) / 32;
   const int b0 = lane * per;
   long long sum = 0;
   for (int i = 0; i < per; ++i)
-    if (b0 + i < B) sum += (long long)plan[b0 + i].ntiles * upb;
+    if (b0 + i < B) sum += (long long)plan.ntiles(b0 + i) * upb;
   long long incl = sum;
   for (int off = 1; off < 32; off <<= 1) {
     long long v = __shfl_up_sync(0xffffffffu, incl, off);
@@ -204,7 +246,7 @@ __device__ __forceinline__ void plan_prefix(const SeqPlan* plan, int* pre, int B
   for (int i = 0; i < per; ++i) {
     if (b0 + i < B) {
       pre[b0 + i] = (int)run;
-      run += (long long)plan[b0 + i].ntiles * upb;
+      run += (long long)plan.ntiles(b0 + i) * upb;
     }
   }
   if (lane == 31) pre[B] = (int)incl;
@@ -222,6 +264,7 @@ __device__ __forceinline__ long long stream_start(int c, long long T, int grid) 
 __device__ __forceinline__ int stream_grid(const KParams& p, long long T) {
   return (int)(T < p.grid ? T : p.grid);
 }
+__device__ __forceinline__ int units_per_seq(const KParams& p) { return (p.Hkv / p.KVB) * p.HG; }
 
 __device__ __forceinline__ void seg_init(const KParams& p, const int* pre, SegIter& it) {
   it.n = 0;
@@ -235,7 +278,7 @@ __device__ __forceinline__ void seg_init(const KParams& p, const int* pre, SegIt
     it.g = stream_start(blockIdx.x, T, sg);
     it.g_end = stream_start(blockIdx.x + 1, T, sg);
   } else if (p.sched == SCHED_UNITS) {
-    const long long U = (long long)p.B * p.Hkv * p.HG;
+    const long long U = (long long)p.B * units_per_seq(p);
     it.g = (long long)blockIdx.x * U / p.grid;
     it.g_end = (long long)(blockIdx.x + 1) * U / p.grid;
   } else {
@@ -244,9 +287,10 @@ __device__ __forceinline__ void seg_init(const KParams& p, const int* pre, SegIt
   }
 }
 
-__device__ __forceinline__ bool seg_next(const KParams& p, const SeqPlan* plan, const int* pre,
-                                         SegIter& it, Seg& s) {
-  const int upb = p.Hkv * p.HG;
+template <int KIND, int TOK>
+__device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>& plan,
+                                         const int* pre, SegIter& it, Seg& s) {
+  const int upb = units_per_seq(p);
   if (p.sched == SCHED_STREAM) {
     if (it.g >= it.g_end) return false;
     int lo = 0, hi = p.B;  // largest b with pre[b] <= g
@@ -255,19 +299,20 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const SeqPlan* plan, 
       if (pre[mid] <= it.g) lo = mid; else hi = mid;
     }
     const int b = lo;
-    const int nt = plan[b].ntiles;
+    const SeqPlan e = plan.get(b);
+    const int nt = e.ntiles;
     const long long local = it.g - pre[b];
     const int uib = (int)(local / nt);
     s.b = b;
     s.pidx = b;
-    s.kv = uib / p.HG;
+    s.kvb = uib / p.HG;
     s.hg = uib % p.HG;
     s.unit = b * upb + uib;
     s.i0 = (int)(local % nt);
     long long rem = it.g_end - it.g;
     s.i1 = (int)((long long)s.i0 + rem < nt ? s.i0 + rem : nt);
-    s.vlo = plan[b].lo;
-    s.vhi = plan[b].hi;
+    s.vlo = e.lo;
+    s.vhi = e.hi;
     s.dest = (s.i0 == 0 && s.i1 == nt) ? DEST_OUT : DEST_PARTIAL;
     s.slot = it.n == 0 ? 0 : 1;
     it.g += s.i1 - s.i0;
@@ -278,17 +323,18 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const SeqPlan* plan, 
     while (it.g < it.g_end) {
       const int u = (int)it.g++;
       const int b = u / upb;
-      if (plan[b].ntiles == 0) continue;
+      const SeqPlan e = plan.get(b);
+      if (e.ntiles == 0) continue;
       const int uib = u % upb;
       s.b = b;
       s.pidx = b;
-      s.kv = uib / p.HG;
+      s.kvb = uib / p.HG;
       s.hg = uib % p.HG;
       s.unit = u;
       s.i0 = 0;
-      s.i1 = plan[b].ntiles;
-      s.vlo = plan[b].lo;
-      s.vhi = plan[b].hi;
+      s.i1 = e.ntiles;
+      s.vlo = e.lo;
+      s.vhi = e.hi;
       s.dest = DEST_OUT;
       s.slot = 0;
       it.n++;
@@ -296,29 +342,30 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const SeqPlan* plan, 
     }
     return false;
   }
-  // SCHED_SPLIT: one segment, the keys of split blockIdx.x of unit blockIdx.y
+  // SCHED_SPLIT (paged only): one segment, split blockIdx.x of unit blockIdx.y
   if (it.n > 0) return false;
   it.n = 1;
   const int u = blockIdx.y;
   const int b = u / upb;
   const int uib = u % upb;
+  const SeqPlan e = plan.get(0);
   s.b = b;
   s.pidx = 0;
-  s.kv = uib / p.HG;
+  s.kvb = uib / p.HG;
   s.hg = uib % p.HG;
   s.unit = u;
   s.dest = DEST_SPLIT;
   s.slot = blockIdx.x;
   const long long st0 = (long long)blockIdx.x * p.split_tokens;
   const long long st1 = st0 + p.split_tokens;
-  long long vlo = plan[0].lo > st0 ? plan[0].lo : st0;
-  long long vhi = plan[0].hi < st1 ? plan[0].hi : st1;
+  long long vlo = e.lo > st0 ? e.lo : st0;
+  long long vhi = e.hi < st1 ? e.hi : st1;
   s.i0 = s.i1 = 0;
   s.vlo = (int)vlo;
   s.vhi = (int)(vhi > vlo ? vhi : vlo);
-  if (plan[0].ntiles > 0 && vhi > vlo) {
-    s.i0 = (int)(vlo / kTile) - plan[0].t0;
-    s.i1 = ceil_div_i(vhi, kTile) - plan[0].t0;
+  if (e.ntiles > 0 && vhi > vlo) {
+    s.i0 = (int)(vlo / TOK) - e.t0;
+    s.i1 = ceil_div_i(vhi, TOK) - e.t0;
   }
   return true;
 }
@@ -328,31 +375,6 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const SeqPlan* plan, 
 __device__ __forceinline__ int stream_slot(int c, int c0, long long g0, long long T, int grid) {
   const int j = (c == c0 && stream_start(c, T, grid) < g0) ? 1 : 0;
   return c * 2 + j;
-}
-
-// ---------------------------------------------------------- tile geometry
-// Paged / cold tile: absolute tile `at` covers keys [at*64, at*64+64).
-struct PageSpan {
-  int p_first;  // first page of the tile
-  int npg;      // pages in the tile
-  int rows;     // rows per box (min(bs, 64))
-  int row_off;  // row offset inside the page (bs > 64)
-};
-
-__device__ __forceinline__ PageSpan page_span(int bs, int log2_bs, int at) {
-  PageSpan ps;
-  const int tok0 = at * kTile;
-  ps.p_first = tok0 >> log2_bs;
-  if (bs <= kTile) {
-    ps.npg = kTile >> log2_bs;
-    ps.rows = bs;
-    ps.row_off = 0;
-  } else {
-    ps.npg = 1;
-    ps.rows = kTile;
-    ps.row_off = tok0 & (bs - 1);
-  }
-  return ps;
 }
 
 // Absolute tile of unit-local tile i (tiered: hot tiles follow cold ones).
@@ -368,43 +390,59 @@ __device__ __forceinline__ int tile_of(const SeqPlan& e, int i, bool& is_hot) {
   return e.t0 + i;
 }
 
+// Rows of one TMA box of a paged / cold tile and its page split.
+struct BoxGeo {
+  int R;         // rows (keys) per box: min(block_size, TOK)
+  int log2R;
+  int npg;       // boxes (pages) per tile
+  int box_bytes; // bytes of one box (KVB heads x all slices x R rows)
+};
+
 // ============================================================== producer
-template <int KIND, int D>
-__device__ __forceinline__ void producer_loop(const KParams& p, const SeqPlan* plan,
-                                              const int* pre, uint8_t* stages, uint8_t* qring,
-                                              const SmemLayout& L, uint64_t* full,
-                                              uint64_t* empty, uint64_t* qfull, uint64_t* qempty,
-                                              Misc* misc) {
+template <int KIND, int D, int KVB>
+__device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<KIND>& plan,
+                                              const int* pre, uint8_t* stages, uint8_t* hdrs,
+                                              uint8_t* qslot, const SmemLayout& L,
+                                              const BoxGeo& bg, uint64_t* full, uint64_t* empty,
+                                              uint64_t* qfull, uint64_t* qempty, Misc* misc) {
+  using Gm = Geo<KIND, D, KVB>;
+  constexpr int OPS = (KIND == KIND_PAGED) ? 2 : 4;  // copies per page: K, V (+ 2 scale slabs)
   const int lane = threadIdx.x & 31;
-  constexpr int CH = D / 64;  // 128-byte slices of an f16 row
-  constexpr int CC = D / 128;  // 128-byte slices of an int8 row
-  constexpr int OPS = (KIND == KIND_PAGED) ? 2 * CH : 2 * CC + 2;  // copies per page
   const int nstages = p.stages;
   const int bs = p.bs, log2_bs = p.log2_bs, max_blocks = p.max_blocks, nblocks = p.num_blocks;
-  const uint32_t q_bytes = (uint32_t)(p.NH * D * 4);
+  const int Hkv = p.Hkv;
+  const uint32_t page_bytes =
+      (uint32_t)(2 * bg.box_bytes + (KIND == KIND_TIERED ? 2 * bg.R * Hkv * 2 : 0));
   SegIter it;
   seg_init(p, pre, it);
   Seg s;
   int stage = 0;
   uint32_t round = 0;
-  int qn = 0;  // non-empty segments so far (Q ring position)
+  int qn = 0;  // non-empty segments so far (Q slot phase)
   int bt_b = -1, bt_base = 0, bt_cur = -1, bt_nxt = -1;
   int flags = 0;
-  while (seg_next(p, plan, pre, it, s)) {
+  while (seg_next<KIND, Gm::TOK>(p, plan, pre, it, s)) {
     if (s.i0 >= s.i1) continue;
-    const SeqPlan e = plan[s.pidx];
+    const SeqPlan e = plan.get(s.pidx);
+    const int kv0 = s.kvb * KVB;
     const int* bt_row = p.block_table + (long long)s.b * max_blocks;
-    // ---- Q rows of the head group into the Q ring
+    // ---- Q rows of the unit (KVB x NH heads) into the Q slot
     {
-      const int slot = qn & 1;
-      if (!mbar_wait(&qempty[slot], ((qn >> 1) & 1) ^ 1)) {
+      if (!mbar_wait(qempty, (qn & 1) ^ 1)) {
         if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
         return;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&qfull[slot], q_bytes);
-        const float* src = p.q + ((long long)s.b * p.Hq + s.kv * p.G + s.hg * kHeadTile) * D;
-        bulk_load(qring + slot * L.q_slot_bytes, src, q_bytes, &qfull[slot]);
+        const uint32_t per = (uint32_t)(p.NH * D * 4);
+        mbar_arrive_expect_tx(qfull, per * KVB);
+        const float* qb = p.q + (long long)s.b * p.Hq * D;
+        if (p.HG == 1) {
+          bulk_load(qslot, qb + (long long)kv0 * p.G * D, per * KVB, qfull);
+        } else {
+          for (int j = 0; j < KVB; ++j)
+            bulk_load(qslot + j * per, qb + ((long long)(kv0 + j) * p.G + s.hg * kHeadTile) * D, per,
+                      qfull);
+        }
       }
       ++qn;
     }
@@ -418,14 +456,16 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const SeqPlan* p
       const int at = tile_of<KIND>(e, i, is_hot);
       if (!is_hot) {
         // ----- pages through the block table
-        const PageSpan ps = page_span(bs, log2_bs, at);
+        const int tok0 = at * Gm::TOK;
+        const int p_first = tok0 >> log2_bs;
+        const int row_off = (bs > Gm::TOK) ? (tok0 & (bs - 1)) : 0;
         // keep a 64-entry window of block-table entries in two registers
-        if (s.b != bt_b || ps.p_first < bt_base || ps.p_first + ps.npg > bt_base + 64) {
-          if (s.b == bt_b && ps.p_first >= bt_base + 32 && ps.p_first + ps.npg <= bt_base + 96) {
+        if (s.b != bt_b || p_first < bt_base || p_first + bg.npg > bt_base + 64) {
+          if (s.b == bt_b && p_first >= bt_base + 32 && p_first + bg.npg <= bt_base + 96) {
             bt_cur = bt_nxt;
             bt_base += 32;
           } else {
-            bt_base = ps.p_first;
+            bt_base = p_first;
             const int pc = bt_base + lane;
             bt_cur = pc < max_blocks ? __ldg(bt_row + pc) : -1;
           }
@@ -433,78 +473,53 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const SeqPlan* p
           bt_nxt = pn < max_blocks ? __ldg(bt_row + pn) : -1;
           bt_b = s.b;
         }
+        // lane j < npg: page j of the tile
+        const int idx = p_first + lane - bt_base;
+        const int vc = __shfl_sync(0xffffffffu, bt_cur, idx & 31);
+        const int vn = __shfl_sync(0xffffffffu, bt_nxt, idx & 31);
+        const int pg = p_first + lane;
+        const int blk = (lane < bg.npg && pg < max_blocks) ? (idx < 32 ? vc : vn) : -1;
         const int vhi_keys = (KIND == KIND_TIERED) ? min(s.vhi, e.cold_len) : s.vhi;
-        int my_blk0 = -1, my_blk1 = -1;
-        uint32_t need_mask = 0, bad_mask = 0, bytes = 0;
-        for (int j = 0; j < ps.npg; ++j) {
-          const int pg = ps.p_first + j;
-          const int idx = pg - bt_base;
-          const int vc = __shfl_sync(0xffffffffu, bt_cur, idx & 31);
-          const int vn = __shfl_sync(0xffffffffu, bt_nxt, idx & 31);
-          const int blk = pg < max_blocks ? (idx < 32 ? vc : vn) : -1;
-          const int r0 = at * kTile + j * ps.rows;
-          const bool needed = (r0 < vhi_keys) && (r0 + ps.rows > s.vlo);
-          if (!needed) continue;
-          if (blk < 0 || blk >= nblocks) {
-            bad_mask |= 1u << j;
-            continue;
-          }
-          need_mask |= 1u << j;
-          if constexpr (KIND == KIND_PAGED) {
-            bytes += (uint32_t)(2 * CH * ps.rows * 128);
-          } else {
-            bytes += (uint32_t)(2 * CC * ps.rows * 128 + 2 * ps.rows * p.Hkv * 2);
-          }
-          if (lane / OPS == j) my_blk0 = blk;
-          if ((lane + 32) / OPS == j) my_blk1 = blk;
-        }
+        const int r0 = tok0 + lane * bg.R;
+        const bool needed = lane < bg.npg && (r0 < vhi_keys) && (r0 + bg.R > s.vlo);
+        const bool ok = needed && blk >= 0 && blk < nblocks;
+        const uint32_t need_mask = __ballot_sync(0xffffffffu, ok);
+        const uint32_t bad_mask = __ballot_sync(0xffffffffu, needed && !ok);
         if (bad_mask) flags |= DEV_BAD_BLOCK;
         if (lane == 0) {
-          *reinterpret_cast<volatile uint32_t*>(st + L.off_hdr) = bad_mask;
-          mbar_arrive_expect_tx(&full[stage], bytes);
+          *reinterpret_cast<volatile uint32_t*>(hdrs + stage * 16) = bad_mask;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)__popc(need_mask) * page_bytes);
         }
         __syncwarp();
-#pragma unroll
-        for (int rep = 0; rep < 2; ++rep) {
-          const int op = lane + rep * 32;
+        for (int base = 0; base < bg.npg * OPS; base += 32) {
+          const int op = base + lane;
           const int j = op / OPS;
-          const int blk = rep ? my_blk1 : my_blk0;
-          if (j < ps.npg && ((need_mask >> j) & 1u)) {
+          const int bj = __shfl_sync(0xffffffffu, blk, j & 31);
+          if (op < bg.npg * OPS && ((need_mask >> j) & 1u)) {
             const int r = op % OPS;
-            const int row = blk * bs + ps.row_off;
-            if constexpr (KIND == KIND_PAGED) {
-              const int isv = r / CH;
-              const int ch = r % CH;
-              uint8_t* dst = st + (isv ? L.off_v : L.off_k) + ch * (kTile * 128) + j * ps.rows * 128;
-              tma_load_3d(dst, isv ? &p.tm_v : &p.tm_k, &full[stage], ch * 64, s.kv, row);
-            } else {
-              if (r < 2 * CC) {
-                const int isv = r / CC;
-                const int ch = r % CC;
-                uint8_t* dst = st + (isv ? L.off_v : L.off_k) + ch * (kTile * 128) + j * ps.rows * 128;
-                tma_load_3d(dst, isv ? &p.tm_v : &p.tm_k, &full[stage], ch * 128, s.kv, row);
-              } else {
-                // the tile's rows of the page's [rows, Hkv] f16 scale slab
-                const int isv = r - 2 * CC;
-                const uint16_t* src = (isv ? p.v_scale : p.k_scale) + (long long)row * p.Hkv;
-                uint8_t* dst = st + L.off_sc + isv * (kTile * p.Hkv * 2) + j * ps.rows * p.Hkv * 2;
-                bulk_load(dst, src, (uint32_t)(ps.rows * p.Hkv * 2), &full[stage]);
-              }
+            const int row = bj * bs + row_off;
+            if (r < 2) {
+              uint8_t* dst = st + (r ? L.off_v : L.off_k) + j * bg.box_bytes;
+              tma_load_4d(dst, r ? &p.tm_v : &p.tm_k, &full[stage], 0, row, 0, kv0);
+            } else if constexpr (KIND == KIND_TIERED) {
+              // the box's rows of the page's [rows, Hkv] f16 scale slab
+              const int isv = r - 2;
+              const uint16_t* src = (isv ? p.v_scale : p.k_scale) + (long long)row * Hkv;
+              uint8_t* dst = st + L.off_sc + isv * (Gm::TOK * Hkv * 2) + j * bg.R * Hkv * 2;
+              bulk_load(dst, src, (uint32_t)(bg.R * Hkv * 2), &full[stage]);
             }
           }
         }
-      } else {
-        // ----- hot ring tile: slots [at*64, at*64+64) of sequence b
+      } else if constexpr (KIND == KIND_TIERED) {
+        // ----- hot ring tile: slots [at*TOKH, at*TOKH + TOKH) of sequence b
         if (lane == 0) {
-          *reinterpret_cast<volatile uint32_t*>(st + L.off_hdr) = 0u;
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * CH * kTile * 128));
+          *reinterpret_cast<volatile uint32_t*>(hdrs + stage * 16) = 0u;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * Gm::REGION));
         }
         __syncwarp();
-        if (lane < 2 * CH) {
-          const int isv = lane / CH;
-          const int ch = lane % CH;
-          uint8_t* dst = st + (isv ? L.off_v : L.off_k) + ch * (kTile * 128);
-          tma_load_4d(dst, isv ? &p.tm_vh : &p.tm_kh, &full[stage], ch * 64, s.kv, at * kTile,
+        if (lane < 2) {
+          uint8_t* dst = st + (lane ? L.off_v : L.off_k);
+          tma_load_5d(dst, lane ? &p.tm_vh : &p.tm_kh, &full[stage], 0, at * Gm::TOKH, 0, kv0,
                       s.b + p.hot_b0);
         }
       }
@@ -584,33 +599,46 @@ __device__ __forceinline__ uint32_t biased_i8x2_to_h2(uint32_t wb, uint32_t sel)
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Where the rows of one kv head live in a stage.  Row of key k:
+//   base + (k >> log2R) * box_bytes + (k & (R-1)) * 128, slice ch adds
+//   ch * R * 128, and 16-byte unit u of a slice sits at (u ^ (k & 7)) * 16.
+struct RowMap {
+  uint32_t base;  // stage region + kv-head offset inside a box
+  int log2R;
+  int box_bytes;
+  int cstride;    // R * 128
+  __device__ __forceinline__ uint32_t row(int k) const {
+    return base + (uint32_t)((k >> log2R) * box_bytes + (k & ((1 << log2R) - 1)) * 128);
+  }
+};
+
 // S^T[16 keys x 8 heads] of keys k0..k0+15.  Four accumulators (hi/lo Q
 // parts x even/odd k-steps) keep the dependency chains short.
 template <int TK, int D>
-__device__ __forceinline__ void tile_qk(uint32_t kbase, int k0, int lane, const QFrag<D>& q,
+__device__ __forceinline__ void tile_qk(const RowMap& km, int k0, int lane, const QFrag<D>& q,
                                         float (&s4)[4][4]) {
   const int r = lane >> 2, c = lane & 3;
   if constexpr (TK == TK_PAGED) {
     const int mat = lane >> 3;
     const int key = k0 + (lane & 7) + ((mat & 1) << 3);
-    const uint32_t rowaddr = kbase + key * 128;
+    const uint32_t rowaddr = km.row(key);
     const int x = lane & 7;
     const int dh = mat >> 1;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       const int ug = 2 * ks + dh;
       uint32_t a0, a1, a2, a3;
-      ldsm_x4(rowaddr + (ug >> 3) * (kTile * 128) + (((ug & 7) ^ x) << 4), a0, a1, a2, a3);
+      ldsm_x4(rowaddr + (ug >> 3) * km.cstride + (((ug & 7) ^ x) << 4), a0, a1, a2, a3);
       mma_f16_16816(s4[(ks & 1)], a0, a1, a2, a3, q.hi[ks][0], q.hi[ks][1]);
       mma_f16_16816(s4[2 + (ks & 1)], a0, a1, a2, a3, q.lo[ks][0], q.lo[ks][1]);
     }
   } else if constexpr (TK == TK_COLD) {
     // int8 rows of D bytes: word c of 16-byte unit ks holds d = 16ks + 4c .. +3
-    const uint32_t rb0 = kbase + (k0 + r) * 128 + 4 * c;
-    const uint32_t rb1 = rb0 + 8 * 128;
+    const uint32_t rb0 = km.row(k0 + r) + 4 * c;
+    const uint32_t rb1 = km.row(k0 + r + 8) + 4 * c;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      const uint32_t off = (ks >> 3) * (kTile * 128) + (((ks & 7) ^ r) << 4);
+      const uint32_t off = (ks >> 3) * km.cstride + (((ks & 7) ^ r) << 4);
       const uint32_t w0 = lds32(rb0 + off) ^ 0x80808080u;
       const uint32_t w1 = lds32(rb1 + off) ^ 0x80808080u;
       const uint32_t a0 = biased_i8x2_to_h2(w0, 0x4140u), a2 = biased_i8x2_to_h2(w0, 0x4342u);
@@ -620,12 +648,12 @@ __device__ __forceinline__ void tile_qk(uint32_t kbase, int k0, int lane, const 
     }
   } else {
     // f16 rows: 8 bytes at d = 16ks + 4c
-    const uint32_t rb0 = kbase + (k0 + r) * 128 + (c & 1) * 8;
-    const uint32_t rb1 = rb0 + 8 * 128;
+    const uint32_t rb0 = km.row(k0 + r) + (c & 1) * 8;
+    const uint32_t rb1 = km.row(k0 + r + 8) + (c & 1) * 8;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       const int u = 2 * (ks & 3) + (c >> 1);
-      const uint32_t off = (ks >> 2) * (kTile * 128) + ((u ^ r) << 4);
+      const uint32_t off = (ks >> 2) * km.cstride + ((u ^ r) << 4);
       const uint2 v0 = lds64(rb0 + off);
       const uint2 v1 = lds64(rb1 + off);
       mma_f16_16816(s4[(ks & 1)], v0.x, v1.x, v0.y, v1.y, q.hi[ks][0], q.hi[ks][1]);
@@ -636,34 +664,36 @@ __device__ __forceinline__ void tile_qk(uint32_t kbase, int k0, int lane, const 
 
 // O^T += V^T P^T for keys k0..k0+15; b* are the P^T fragments.
 template <int TK, int D>
-__device__ __forceinline__ void tile_pv(uint32_t vbase, int k0, int lane, float (&o)[D / 16][4],
+__device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, float (&o)[D / 16][4],
                                         uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
   const int r = lane >> 2, c = lane & 3;
   if constexpr (TK == TK_PAGED) {
     const int mat = lane >> 3;
     const int key = k0 + (lane & 7) + ((mat >> 1) << 3);
-    const uint32_t rowaddr = vbase + key * 128;
+    const uint32_t rowaddr = vm.row(key);
     const int x = lane & 7;
     const int dh = mat & 1;
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
       const int ug = 2 * mt + dh;
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_trans(rowaddr + (ug >> 3) * (kTile * 128) + (((ug & 7) ^ x) << 4), a0, a1, a2, a3);
+      ldsm_x4_trans(rowaddr + (ug >> 3) * vm.cstride + (((ug & 7) ^ x) << 4), a0, a1, a2, a3);
       mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
       mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
     }
   } else if constexpr (TK == TK_COLD) {
     // word q = 8pp + r (d = 4q .. 4q+3) of keys 2c, 2c+1, 2c+8, 2c+9
     const int tA = k0 + 2 * c;
+    const uint32_t rA = vm.row(tA) + (r & 3) * 4, rB = vm.row(tA + 1) + (r & 3) * 4;
+    const uint32_t rC = vm.row(tA + 8) + (r & 3) * 4, rD = vm.row(tA + 9) + (r & 3) * 4;
 #pragma unroll
     for (int pp = 0; pp < D / 32; ++pp) {
       const int u = 2 * (pp & 3) + (r >> 2);
-      const uint32_t base = vbase + (pp >> 2) * (kTile * 128) + (r & 3) * 4;
-      const uint32_t WA = lds32(base + tA * 128 + ((u ^ (2 * c)) << 4)) ^ 0x80808080u;
-      const uint32_t WB = lds32(base + (tA + 1) * 128 + ((u ^ (2 * c + 1)) << 4)) ^ 0x80808080u;
-      const uint32_t WC = lds32(base + (tA + 8) * 128 + ((u ^ (2 * c)) << 4)) ^ 0x80808080u;
-      const uint32_t WD = lds32(base + (tA + 9) * 128 + ((u ^ (2 * c + 1)) << 4)) ^ 0x80808080u;
+      const uint32_t cs = (pp >> 2) * vm.cstride;
+      const uint32_t WA = lds32(rA + cs + ((u ^ (2 * c)) << 4)) ^ 0x80808080u;
+      const uint32_t WB = lds32(rB + cs + ((u ^ (2 * c + 1)) << 4)) ^ 0x80808080u;
+      const uint32_t WC = lds32(rC + cs + ((u ^ (2 * c)) << 4)) ^ 0x80808080u;
+      const uint32_t WD = lds32(rD + cs + ((u ^ (2 * c + 1)) << 4)) ^ 0x80808080u;
       const uint32_t E = __byte_perm(WA, WB, 0x5140u), F = __byte_perm(WA, WB, 0x7362u);
       const uint32_t E2 = __byte_perm(WC, WD, 0x5140u), F2 = __byte_perm(WC, WD, 0x7362u);
       {
@@ -682,14 +712,16 @@ __device__ __forceinline__ void tile_pv(uint32_t vbase, int k0, int lane, float 
   } else {
     // f16 rows, 8 bytes (d = 4q .. 4q+3, q = 8pp + r) of keys 2c, 2c+1, 2c+8, 2c+9
     const int tA = k0 + 2 * c;
+    const uint32_t rA = vm.row(tA) + (r & 1) * 8, rB = vm.row(tA + 1) + (r & 1) * 8;
+    const uint32_t rC = vm.row(tA + 8) + (r & 1) * 8, rD = vm.row(tA + 9) + (r & 1) * 8;
 #pragma unroll
     for (int pp = 0; pp < D / 32; ++pp) {
       const int u = 4 * (pp & 1) + (r >> 1);
-      const uint32_t base = vbase + (pp >> 1) * (kTile * 128) + (r & 1) * 8;
-      const uint2 A = lds64(base + tA * 128 + ((u ^ (2 * c)) << 4));
-      const uint2 B = lds64(base + (tA + 1) * 128 + ((u ^ (2 * c + 1)) << 4));
-      const uint2 C = lds64(base + (tA + 8) * 128 + ((u ^ (2 * c)) << 4));
-      const uint2 E = lds64(base + (tA + 9) * 128 + ((u ^ (2 * c + 1)) << 4));
+      const uint32_t cs = (pp >> 1) * vm.cstride;
+      const uint2 A = lds64(rA + cs + ((u ^ (2 * c)) << 4));
+      const uint2 B = lds64(rB + cs + ((u ^ (2 * c + 1)) << 4));
+      const uint2 C = lds64(rC + cs + ((u ^ (2 * c)) << 4));
+      const uint2 E = lds64(rD + cs + ((u ^ (2 * c + 1)) << 4));
       {
         const uint32_t a0 = __byte_perm(A.x, B.x, 0x5410u), a1 = __byte_perm(A.x, B.x, 0x7632u);
         const uint32_t a2 = __byte_perm(C.x, E.x, 0x5410u), a3 = __byte_perm(C.x, E.x, 0x7632u);
@@ -706,20 +738,18 @@ __device__ __forceinline__ void tile_pv(uint32_t vbase, int k0, int lane, float 
   }
 }
 
-// One stage for this warp's 16 keys: QK, mask, online softmax, PV.
+// One 16-key group of this warp: QK, mask, online softmax, PV.
 // vA / vB: validity of keys k0+r and k0+r+8.  ksA.. / vsA..: per-key K and
 // V scales of the int8 tier (rows r and r+8), 1 otherwise.
 template <int TK, int D>
-__device__ __forceinline__ void tile_compute(uint8_t* st, const SmemLayout& L, float softcap2,
-                                             int k0, int lane, const QFrag<D>& q, Acc<D>& a,
-                                             bool vA, bool vB, float ksA, float ksB, float vsA,
-                                             float vsB) {
-  const uint32_t kbase = smem_u32(st + L.off_k);
-  const uint32_t vbase = smem_u32(st + L.off_v);
+__device__ __forceinline__ void group_compute(const RowMap& km, const RowMap& vm, float softcap2,
+                                              int k0, int lane, const QFrag<D>& q, Acc<D>& a,
+                                              bool vA, bool vB, float ksA, float ksB, float vsA,
+                                              float vsB) {
   float s4[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) s4[i][0] = s4[i][1] = s4[i][2] = s4[i][3] = 0.f;
-  tile_qk<TK, D>(kbase, k0, lane, q, s4);
+  tile_qk<TK, D>(km, k0, lane, q, s4);
   float sc[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -770,33 +800,21 @@ __device__ __forceinline__ void tile_compute(uint8_t* st, const SmemLayout& L, f
   split_half2(p2, p3, h23, l23);
   const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
   const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-  tile_pv<TK, D>(vbase, k0, lane, a.o, bh0, bh1, bl0, bl1);
+  tile_pv<TK, D>(vm, k0, lane, a.o, bh0, bh1, bl0, bl1);
 }
 
-// Zeroes the V rows of masked keys among k0..k0+15 (f16 tiles), so that a
-// zero weight never meets a stale or non-finite value.
+// Zeroes the f16 V rows of masked keys among k0..k0+15 of this warp's head,
+// so that a zero weight never meets a stale or non-finite value.
 template <int D, typename OkFn>
-__device__ __forceinline__ void zero_masked_v_rows(uint8_t* vst, int k0, int lane, OkFn ok) {
+__device__ __forceinline__ void zero_masked_v_rows(const RowMap& vm, int k0, int lane, OkFn ok) {
   constexpr int UPR = D / 8;  // 16-byte units per f16 row
   for (int u = lane; u < 16 * UPR; u += 32) {
     const int row = u / UPR, ug = u % UPR;
     const int k = k0 + row;
-    if (!ok(k)) {
-      uint8_t* dst = vst + (ug >> 3) * (kTile * 128) + k * 128 + (((ug & 7) ^ (k & 7)) << 4);
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
+    if (!ok(k)) sts128_zero(vm.row(k) + (ug >> 3) * vm.cstride + (((ug & 7) ^ (k & 7)) << 4));
   }
   fence_proxy_async_smem();
   __syncwarp();
-}
-
-// Key validity of row k (0..63) of a paged / cold tile.
-__device__ __forceinline__ bool key_ok_paged(int bs, int log2_bs, int at, int k, int vlo, int vhi,
-                                             uint32_t bad_mask) {
-  const int t = at * kTile + k;
-  if (t < vlo || t >= vhi) return false;
-  const int j = bs <= kTile ? (k >> log2_bs) : 0;
-  return ((bad_mask >> j) & 1u) == 0;
 }
 
 // What a hot-ring tile can see: ring slot s holds hot key
@@ -807,22 +825,64 @@ struct HotView {
   long long j0, j1;
 };
 
-__device__ __forceinline__ bool key_ok_hot(const HotView& hv, int at, int k) {
-  const int sl = at * kTile + k;
+__device__ __forceinline__ bool key_ok_hot(const HotView& hv, int slot0, int k) {
+  const int sl = slot0 + k;
   if (sl >= hv.cap_eff) return false;
   const int j = hv.W > 0 ? (sl - hv.hs_mod + hv.W) % hv.W : sl;
   return j >= hv.j0 && j < hv.j1;
 }
 
-// Merges the consumer warps' states for segment s and writes the result.
-template <int KIND, int D, int GROUPS>
+// Combines two online-softmax states of the same heads (this warp's and a
+// partner's, read back from shared memory in the same fragment layout).
+template <int D>
+__device__ __forceinline__ void merge_state(Acc<D>& a, const float* red, int lane) {
+  constexpr int NO = D / 4;
+  const float mb0 = red[(NO + 0) * 32 + lane], mb1 = red[(NO + 1) * 32 + lane];
+  const float lb0 = red[(NO + 2) * 32 + lane], lb1 = red[(NO + 3) * 32 + lane];
+  const float mn0 = fmaxf(a.m[0], mb0), mn1 = fmaxf(a.m[1], mb1);
+  const float fa0 = (a.m[0] == kNegInf) ? 0.f : exp2f(a.m[0] - mn0);
+  const float fb0 = (mb0 == kNegInf) ? 0.f : exp2f(mb0 - mn0);
+  const float fa1 = (a.m[1] == kNegInf) ? 0.f : exp2f(a.m[1] - mn1);
+  const float fb1 = (mb1 == kNegInf) ? 0.f : exp2f(mb1 - mn1);
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    a.o[mt][0] = a.o[mt][0] * fa0 + red[(4 * mt + 0) * 32 + lane] * fb0;
+    a.o[mt][1] = a.o[mt][1] * fa1 + red[(4 * mt + 1) * 32 + lane] * fb1;
+    a.o[mt][2] = a.o[mt][2] * fa0 + red[(4 * mt + 2) * 32 + lane] * fb0;
+    a.o[mt][3] = a.o[mt][3] * fa1 + red[(4 * mt + 3) * 32 + lane] * fb1;
+  }
+  a.l[0] = a.l[0] * fa0 + lb0 * fb0;
+  a.l[1] = a.l[1] * fa1 + lb1 * fb1;
+  a.m[0] = mn0;
+  a.m[1] = mn1;
+}
+
+template <int D>
+__device__ __forceinline__ void store_state(const Acc<D>& a, float* red, int lane) {
+  constexpr int NO = D / 4;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) red[(4 * mt + k) * 32 + lane] = a.o[mt][k];
+  }
+  red[(NO + 0) * 32 + lane] = a.m[0];
+  red[(NO + 1) * 32 + lane] = a.m[1];
+  red[(NO + 2) * 32 + lane] = a.l[0];
+  red[(NO + 3) * 32 + lane] = a.l[1];
+}
+
+// Merges the warps of each kv head of segment s and writes the result.
+template <int KIND, int D, int KVB>
 __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, Acc<D>& a,
-                                               float* red_o, float* red_ml, Misc* misc,
-                                               const int* pre, const SeqPlan* plan) {
-  constexpr int NCW = consumer_warps(GROUPS);
+                                               float* red, Misc* misc, const int* pre,
+                                               const PlanStore<KIND>& plan) {
+  using Gm = Geo<KIND, D, KVB>;
+  constexpr int TG = Gm::TG;
+  constexpr int NCW = Gm::W;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
+  const int kvs = warp / TG, tg = warp % TG;
   const int NH = p.NH;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
@@ -832,63 +892,57 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     l += __shfl_xor_sync(0xffffffffu, l, 16);
     a.l[j] = l;
   }
+  // tree merge of the TG warps of each kv head; warp tg = 0 ends with the sum
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int h = 2 * c + j;
-    if (h < NH) {
-      float* ro = red_o + (warp * NH + h) * D;
+  for (int st = TG / 2; st >= 1; st >>= 1) {
+    if (tg >= st && tg < 2 * st) store_state<D>(a, red + (kvs * (TG / 2) + (tg - st)) * red_floats(D), lane);
+    named_bar_sync(kRedBarrier, NCW * 32);
+    if (tg < st) merge_state<D>(a, red + (kvs * (TG / 2) + tg) * red_floats(D), lane);
+    named_bar_sync(kRedBarrier, NCW * 32);
+  }
+  const int kv = s.kvb * KVB + kvs;
+  const long long row0 = (long long)s.b * p.Hq + (long long)kv * p.G + s.hg * kHeadTile;
+  if (tg == 0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = 2 * c + j;
+      if (h >= NH) continue;
+      const float L = a.l[j];
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const float lse = (a.m[j] == kNegInf) ? kNegInf : (a.m[j] + log2f(L)) * kLn2;
+      float* dst;
+      float* ldst;
+      long long ostride = 1;
+      if (s.dest == DEST_OUT) {
+        dst = p.out + (row0 + h) * D;
+        ldst = p.lse ? p.lse + row0 + h : nullptr;
+      } else if (s.dest == DEST_SPLIT) {
+        const long long pr = (row0 + h) * p.max_splits + s.slot;
+        dst = p.o_part + pr * D;
+        ldst = p.lse_part + pr;
+      } else {
+        const long long sl = ((long long)blockIdx.x * 2 + s.slot) * (KVB * kHeadTile) +
+                             kvs * kHeadTile + h;
+        dst = p.ws_o + sl * D;
+        ldst = p.ws_lse + sl;
+      }
+      (void)ostride;
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
-        ro[o_row_d<KIND>(mt, r, 0)] = a.o[mt][j];
-        ro[o_row_d<KIND>(mt, r, 1)] = a.o[mt][2 + j];
+        dst[o_row_d<KIND>(mt, r, 0)] = a.o[mt][j] * inv;
+        dst[o_row_d<KIND>(mt, r, 1)] = a.o[mt][2 + j] * inv;
       }
-      if (r == 0) {
-        red_ml[(warp * NH + h) * 2 + 0] = a.m[j];
-        red_ml[(warp * NH + h) * 2 + 1] = a.l[j];
-      }
+      if (r == 0 && ldst) *ldst = lse;
     }
   }
-  named_bar_sync(kRedBarrier, NCW * 32);
-  const int h0 = s.kv * p.G + s.hg * kHeadTile;
-  const long long row0 = (long long)s.b * p.Hq + h0;
-  for (int idx = tid; idx < NH * D; idx += NCW * 32) {
-    const int h = idx / D, d = idx % D;
-    float M = kNegInf;
-#pragma unroll
-    for (int w = 0; w < NCW; ++w) M = fmaxf(M, red_ml[(w * NH + h) * 2]);
-    float o = 0.f, lse = kNegInf;
-    if (M != kNegInf) {
-      float Ls = 0.f, Os = 0.f;
-#pragma unroll
-      for (int w = 0; w < NCW; ++w) {
-        const float f = exp2f(red_ml[(w * NH + h) * 2] - M);
-        Ls += f * red_ml[(w * NH + h) * 2 + 1];
-        Os += f * red_o[(w * NH + h) * D + d];
-      }
-      o = Os / Ls;
-      lse = (M + log2f(Ls)) * kLn2;
-    }
-    if (s.dest == DEST_OUT) {
-      p.out[(row0 + h) * D + d] = o;
-      if (d == 0 && p.lse) p.lse[row0 + h] = lse;
-    } else if (s.dest == DEST_SPLIT) {
-      const long long pr = (row0 + h) * p.max_splits + s.slot;
-      p.o_part[pr * D + d] = o;
-      if (d == 0) p.lse_part[pr] = lse;
-    } else {
-      const long long sl = ((long long)blockIdx.x * 2 + s.slot) * kHeadTile + h;
-      p.ws_o[sl * D + d] = o;
-      if (d == 0) p.ws_lse[sl] = lse;
-    }
-  }
-  if (s.dest == DEST_PARTIAL) __threadfence();
-  named_bar_sync(kRedBarrier, NCW * 32);
   if (s.dest != DEST_PARTIAL) return;
+  __threadfence();
+  named_bar_sync(kRedBarrier, NCW * 32);
   // ---- last-arriver merge of the unit's partial states
   const long long T = pre[p.B];
   const int sg = stream_grid(p, T);
-  const int nt = plan[s.pidx].ntiles;
-  const int uib = s.unit - s.b * p.Hkv * p.HG;
+  const int nt = plan.ntiles(s.pidx);
+  const int uib = s.unit - s.b * units_per_seq(p);
   const long long g0 = pre[s.b] + (long long)uib * nt;
   const long long g1 = g0 + nt - 1;
   const int c0 = stream_cta_of(g0, T, sg);
@@ -900,18 +954,23 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   const int ticket = misc->ticket;
   if (ticket == c1 - c0) {
     __threadfence();
-    for (int idx = tid; idx < NH * D; idx += NCW * 32) {
-      const int h = idx / D, d = idx % D;
+    const long long urow0 = (long long)s.b * p.Hq + s.hg * kHeadTile;
+    for (int idx = tid; idx < KVB * NH * D; idx += NCW * 32) {
+      const int d = idx % D;
+      const int hh = idx / D;
+      const int ks = hh / NH, h = hh % NH;
       float M = kNegInf;
       for (int cc = c0; cc <= c1; ++cc) {
-        const long long sl = (long long)stream_slot(cc, c0, g0, T, sg) * kHeadTile + h;
+        const long long sl = (long long)stream_slot(cc, c0, g0, T, sg) * (KVB * kHeadTile) +
+                             ks * kHeadTile + h;
         M = fmaxf(M, __ldcg(p.ws_lse + sl));
       }
       float o = 0.f, lse = kNegInf;
       if (M != kNegInf) {
         float Ws = 0.f, Os = 0.f;
         for (int cc = c0; cc <= c1; ++cc) {
-          const long long sl = (long long)stream_slot(cc, c0, g0, T, sg) * kHeadTile + h;
+          const long long sl = (long long)stream_slot(cc, c0, g0, T, sg) * (KVB * kHeadTile) +
+                               ks * kHeadTile + h;
           const float ls = __ldcg(p.ws_lse + sl);
           const float w = (ls == kNegInf) ? 0.f : expf(ls - M);
           Ws += w;
@@ -920,35 +979,39 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
         o = Os / Ws;
         lse = M + logf(Ws);
       }
-      p.out[(row0 + h) * D + d] = o;
-      if (d == 0 && p.lse) p.lse[row0 + h] = lse;
+      const long long orow = urow0 + (long long)(s.kvb * KVB + ks) * p.G + h;
+      p.out[orow * D + d] = o;
+      if (d == 0 && p.lse) p.lse[orow] = lse;
     }
     if (tid == 0) p.ws_cnt[c0] = 0;
   }
   named_bar_sync(kRedBarrier, NCW * 32);
 }
 
-template <int KIND, int D, int GROUPS>
-__device__ __forceinline__ void consumer_loop(const KParams& p, const SeqPlan* plan,
-                                              const int* pre, uint8_t* stages, uint8_t* qring,
-                                              const SmemLayout& L, uint64_t* full,
-                                              uint64_t* empty, uint64_t* qfull, uint64_t* qempty,
-                                              float* red_o, float* red_ml, Misc* misc) {
-  constexpr int NCW = consumer_warps(GROUPS);
+template <int KIND, int D, int KVB>
+__device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<KIND>& plan,
+                                              const int* pre, uint8_t* stages, uint8_t* hdrs,
+                                              uint8_t* qslot, const SmemLayout& L,
+                                              const BoxGeo& bg, uint64_t* full, uint64_t* empty,
+                                              uint64_t* qfull, uint64_t* qempty, float* red,
+                                              Misc* misc) {
+  using Gm = Geo<KIND, D, KVB>;
+  constexpr int TG = Gm::TG;
+  constexpr int NCW = Gm::W;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
-  const int group = warp / kGroupWarps;
-  const int k0 = (warp % kGroupWarps) * 16;
+  const int kvs = warp / TG, tg = warp % TG;
   const int nstages = p.stages;
-  const int bs = p.bs, log2_bs = p.log2_bs;
+  const int bs = p.bs;
   const float softcap2 = p.softcap2, qscale = p.qscale;
   const int NH = p.NH;
+  const int Hkv = p.Hkv;
 
   // Sequences with no visible key: out = 0, lse = -inf.
   if (p.sched != SCHED_SPLIT) {
     for (int b = blockIdx.x; b < p.B; b += p.grid) {
-      if (plan[b].ntiles != 0) continue;
+      if (plan.ntiles(b) != 0) continue;
       for (int idx = tid; idx < p.Hq * D; idx += NCW * 32)
         p.out[(long long)b * p.Hq * D + idx] = 0.f;
       if (p.lse)
@@ -965,28 +1028,30 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const SeqPlan* p
   Acc<D> a;
   QFrag<D> q;
 
-  while (seg_next(p, plan, pre, it, s)) {
+  while (seg_next<KIND, Gm::TOK>(p, plan, pre, it, s)) {
     if (s.i0 >= s.i1) {
       // SPLIT with no visible key: o = 0, lse = -inf
-      const int h0 = s.kv * p.G + s.hg * kHeadTile;
-      for (int idx = tid; idx < NH * D; idx += NCW * 32) {
-        const int h = idx / D, d = idx % D;
-        const long long pr = ((long long)s.b * p.Hq + h0 + h) * p.max_splits + s.slot;
+      for (int idx = tid; idx < KVB * NH * D; idx += NCW * 32) {
+        const int d = idx % D, hh = idx / D;
+        const int kv = s.kvb * KVB + hh / NH, h = hh % NH;
+        const long long pr =
+            ((long long)s.b * p.Hq + (long long)kv * p.G + s.hg * kHeadTile + h) * p.max_splits +
+            s.slot;
         p.o_part[pr * D + d] = 0.f;
         if (d == 0) p.lse_part[pr] = kNegInf;
       }
       continue;
     }
-    const SeqPlan e = plan[s.pidx];
+    const SeqPlan e = plan.get(s.pidx);
+    const int kv = s.kvb * KVB + kvs;
     {
-      const int slot = qn & 1;
-      if (!mbar_wait(&qfull[slot], (qn >> 1) & 1)) {
+      if (!mbar_wait(qfull, qn & 1)) {
         if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
         return;
       }
-      load_q<KIND, D>(smem_u32(qring + slot * L.q_slot_bytes), NH, qscale, r, c, q);
+      load_q<KIND, D>(smem_u32(qslot + kvs * NH * D * 4), NH, qscale, r, c, q);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&qempty[slot]);
+      if (lane == 0) mbar_arrive(qempty);
       ++qn;
     }
 #pragma unroll
@@ -1003,97 +1068,123 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const SeqPlan* p
       hv.j0 = j0 > 0 ? j0 : 0;
       hv.j1 = j1 < e.hot_len ? j1 : e.hot_len;
     }
+    const int vhc = (KIND == KIND_TIERED) ? min(s.vhi, e.cold_len) : s.vhi;
 
     for (int i = s.i0; i < s.i1; ++i) {
-      if (stage % GROUPS == group) {
-        if (!mbar_wait(&full[stage], round & 1)) {
-          if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
-          return;
-        }
-        uint8_t* st = stages + (size_t)stage * L.stage_bytes;
-        const uint32_t bad_mask = lds32(smem_u32(st + L.off_hdr));
-        bool is_hot;
-        const int at = tile_of<KIND>(e, i, is_hot);
-        if (!is_hot) {
-          const int vhc = (KIND == KIND_TIERED) ? min(s.vhi, e.cold_len) : s.vhi;
-          auto ok = [&](int k) { return key_ok_paged(bs, log2_bs, at, k, s.vlo, vhc, bad_mask); };
-          const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
-          if (__any_sync(0xffffffffu, vA || vB)) {
-            if constexpr (KIND == KIND_PAGED) {
-              if (!__all_sync(0xffffffffu, vA && vB))
-                zero_masked_v_rows<D>(st + L.off_v, k0, lane, ok);
-              tile_compute<TK_PAGED, D>(st, L, softcap2, k0, lane, q, a, vA, vB, 1.f, 1.f, 1.f,
-                                        1.f);
-            } else {
-              const uint32_t sck = smem_u32(st + L.off_sc);
-              const uint32_t scv = sck + kTile * p.Hkv * 2;
-              const uint32_t iA = ((k0 + r) * p.Hkv + s.kv) * 2, iB = iA + 8 * p.Hkv * 2;
-              tile_compute<TK_COLD, D>(
-                  st, L, softcap2, k0, lane, q, a, vA, vB,
-                  __half2float(__ushort_as_half(lds16(sck + iA))),
-                  __half2float(__ushort_as_half(lds16(sck + iB))),
-                  __half2float(__ushort_as_half(lds16(scv + iA))),
-                  __half2float(__ushort_as_half(lds16(scv + iB))));
-            }
-          }
-        } else if constexpr (KIND == KIND_TIERED) {
-          auto ok = [&](int k) { return key_ok_hot(hv, at, k); };
-          const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
-          if (__any_sync(0xffffffffu, vA || vB)) {
-            if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(st + L.off_v, k0, lane, ok);
-            tile_compute<TK_HOT, D>(st, L, softcap2, k0, lane, q, a, vA, vB, 1.f, 1.f, 1.f, 1.f);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
+      if (!mbar_wait(&full[stage], round & 1)) {
+        if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
+        return;
       }
+      uint8_t* st = stages + (size_t)stage * L.stage_bytes;
+      const uint32_t bad_mask = lds32(smem_u32(hdrs + stage * 16));
+      bool is_hot;
+      const int at = tile_of<KIND>(e, i, is_hot);
+      if (!is_hot) {
+        RowMap km, vm;
+        km.log2R = bg.log2R;
+        km.box_bytes = bg.box_bytes;
+        km.cstride = bg.R * 128;
+        km.base = smem_u32(st + L.off_k) + (uint32_t)(kvs * Gm::CHN * bg.R * 128);
+        vm = km;
+        vm.base = smem_u32(st + L.off_v) + (uint32_t)(kvs * Gm::CHN * bg.R * 128);
+        const int tok0 = at * Gm::TOK;
+        auto ok = [&](int k) {
+          const int t = tok0 + k;
+          if (t < s.vlo || t >= vhc) return false;
+          const int j = bs <= Gm::TOK ? (k >> bg.log2R) : 0;
+          return ((bad_mask >> j) & 1u) == 0;
+        };
+#pragma unroll
+        for (int gp = 0; gp < Gm::GPW; ++gp) {
+          const int k0 = 16 * (tg + gp * TG);
+          const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
+          if (!__any_sync(0xffffffffu, vA || vB)) continue;
+          if constexpr (KIND == KIND_PAGED) {
+            if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
+            group_compute<TK_PAGED, D>(km, vm, softcap2, k0, lane, q, a, vA, vB, 1.f, 1.f, 1.f,
+                                       1.f);
+          } else {
+            const uint32_t sck = smem_u32(st + L.off_sc);
+            const uint32_t scv = sck + Gm::TOK * Hkv * 2;
+            const uint32_t iA = ((k0 + r) * Hkv + kv) * 2, iB = iA + 8 * Hkv * 2;
+            group_compute<TK_COLD, D>(km, vm, softcap2, k0, lane, q, a, vA, vB,
+                                      __half2float(__ushort_as_half(lds16(sck + iA))),
+                                      __half2float(__ushort_as_half(lds16(sck + iB))),
+                                      __half2float(__ushort_as_half(lds16(scv + iA))),
+                                      __half2float(__ushort_as_half(lds16(scv + iB))));
+          }
+        }
+      } else if constexpr (KIND == KIND_TIERED) {
+        RowMap km, vm;
+        km.log2R = 31 - __clz(Gm::TOKH);
+        km.box_bytes = 0;
+        km.cstride = Gm::TOKH * 128;
+        km.base = smem_u32(st + L.off_k) + (uint32_t)(kvs * Gm::CHH * Gm::TOKH * 128);
+        vm = km;
+        vm.base = smem_u32(st + L.off_v) + (uint32_t)(kvs * Gm::CHH * Gm::TOKH * 128);
+        const int slot0 = at * Gm::TOKH;
+        auto ok = [&](int k) { return key_ok_hot(hv, slot0, k); };
+        const int k0 = 16 * tg;
+        const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
+        if (__any_sync(0xffffffffu, vA || vB)) {
+          if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
+          group_compute<TK_HOT, D>(km, vm, softcap2, k0, lane, q, a, vA, vB, 1.f, 1.f, 1.f, 1.f);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
       if (++stage == nstages) {
         stage = 0;
         ++round;
       }
     }
-    finish_segment<KIND, D, GROUPS>(p, s, a, red_o, red_ml, misc, pre, plan);
+    finish_segment<KIND, D, KVB>(p, s, a, red, misc, pre, plan);
   }
 }
 
 // ================================================================ kernel
-template <int KIND, int D, int GROUPS>
-__global__ void __launch_bounds__(cta_threads(GROUPS), 1)
+template <int KIND, int D, int KVB>
+__global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
     decode_attn_kernel(const __grid_constant__ KParams p) {
+  using Gm = Geo<KIND, D, KVB>;
+  constexpr int NCW = Gm::W;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   // 1024-aligned base (128-byte TMA swizzle atoms), by pointer arithmetic so
   // the compiler keeps the shared address space.
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int nplan = (p.sched == SCHED_SPLIT) ? 1 : p.B;
-  const SmemLayout L = make_layout(KIND, D, p.NH, p.Hkv, p.stages, nplan, GROUPS);
+  const SmemLayout L = make_layout(KIND, D, KVB, NCW, Gm::REGION, Gm::TOK, p.NH, p.Hkv, p.stages,
+                                   nplan);
   uint8_t* stages = base + L.off_stages;
-  uint8_t* qring = base + L.off_q;
-  float* red_o = reinterpret_cast<float*>(base + L.off_red_o);
-  float* red_ml = reinterpret_cast<float*>(base + L.off_red_ml);
-  SeqPlan* plan = reinterpret_cast<SeqPlan*>(base + L.off_plan);
+  uint8_t* hdrs = base + L.off_hdr;
+  uint8_t* qslot = base + L.off_q;
+  float* red = reinterpret_cast<float*>(base + L.off_red);
+  PlanStore<KIND> plan{base + L.off_plan};
   int* pre = reinterpret_cast<int*>(base + L.off_pre);
   uint64_t* full = reinterpret_cast<uint64_t*>(base + L.off_bar);
   uint64_t* empty = full + p.stages;
   uint64_t* qfull = empty + p.stages;
-  uint64_t* qempty = qfull + 2;
+  uint64_t* qempty = qfull + 1;
   Misc* misc = reinterpret_cast<Misc*>(base + L.off_misc);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  constexpr int NCW = consumer_warps(GROUPS);
+
+  BoxGeo bg;
+  bg.R = p.bs < Gm::TOK ? p.bs : Gm::TOK;
+  bg.log2R = 31 - __clz(bg.R);
+  bg.npg = Gm::TOK / bg.R;
+  bg.box_bytes = bg.R * Gm::CHN * KVB * 128;
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kGroupWarps);
+      mbar_init(&empty[s], NCW);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], NCW);
-    }
+    mbar_init(qfull, 1);
+    mbar_init(qempty, NCW);
     fence_mbarrier_init();
     misc->flags = 0;
     misc->ticket = 0;
-    misc->abort = 0;
   }
   if (warp == NCW && (tid & 31) == 0) {
     prefetch_tensormap(&p.tm_k);
@@ -1107,28 +1198,33 @@ __global__ void __launch_bounds__(cta_threads(GROUPS), 1)
   int fl = 0;
   if (p.sched == SCHED_SPLIT) {
     if (tid == 0) {
-      const int b = blockIdx.y / (p.Hkv * p.HG);
-      fl |= plan_sequence<KIND>(p, b, plan[0]);
-      if (blockIdx.x == 0 && plan[0].ntiles > 0 &&
-          (long long)plan[0].hi > (long long)p.max_splits * p.split_tokens)
+      const int b = blockIdx.y / units_per_seq(p);
+      SeqPlan e;
+      fl |= plan_sequence<KIND, Gm::TOK, Gm::TOKH>(p, b, e);
+      plan.put(0, e);
+      if (blockIdx.x == 0 && e.ntiles > 0 &&
+          (long long)e.hi > (long long)p.max_splits * p.split_tokens)
         fl |= DEV_SPLIT_OVERFLOW;
     }
   } else {
-    for (int b = tid; b < p.B; b += cta_threads(GROUPS)) {
-      int f = plan_sequence<KIND>(p, b, plan[b]);
+    for (int b = tid; b < p.B; b += Gm::THREADS) {
+      SeqPlan e;
+      const int f = plan_sequence<KIND, Gm::TOK, Gm::TOKH>(p, b, e);
+      plan.put(b, e);
       if (b % p.grid == (int)blockIdx.x) fl |= f;  // report once per sequence
     }
   }
   if (fl) atomicOr(&misc->flags, fl);
   __syncthreads();
-  if (p.sched != SCHED_SPLIT && warp == 0) plan_prefix(plan, pre, p.B, p.Hkv * p.HG, tid & 31);
+  if (p.sched != SCHED_SPLIT && warp == 0) plan_prefix<KIND>(plan, pre, p.B, units_per_seq(p), tid & 31);
   __syncthreads();
 
   if (warp == NCW) {
-    producer_loop<KIND, D>(p, plan, pre, stages, qring, L, full, empty, qfull, qempty, misc);
+    producer_loop<KIND, D, KVB>(p, plan, pre, stages, hdrs, qslot, L, bg, full, empty, qfull,
+                                qempty, misc);
   } else {
-    consumer_loop<KIND, D, GROUPS>(p, plan, pre, stages, qring, L, full, empty, qfull, qempty,
-                                   red_o, red_ml, misc);
+    consumer_loop<KIND, D, KVB>(p, plan, pre, stages, hdrs, qslot, L, bg, full, empty, qfull,
+                                qempty, red, misc);
   }
   __syncthreads();
   if (tid == 0 && misc->flags && p.dev_status) atomicOr(p.dev_status, misc->flags);

@@ -1,5 +1,6 @@
 // kernel_params.h — the parameter block the host launcher hands to the
-// decode kernels, and the shared-memory layout both sides compute.
+// decode kernels, their per-instantiation geometry, and the shared-memory
+// layout both sides compute.
 #pragma once
 
 #include <cuda.h>
@@ -7,20 +8,11 @@
 
 namespace da {
 
-constexpr int kTile = 64;          // keys per pipeline stage
-constexpr int kGroupWarps = 4;     // consumer warps of a group; each takes 16 keys of a stage
-constexpr int kHeadTile = 8;       // query heads per work unit (the MMA n dimension)
+constexpr int kHeadTile = 8;             // query heads per kv head in a unit (the MMA n dim)
 constexpr int kMaxStages = 8;
 constexpr int kMaxBatchPerLaunch = 256;  // per-sequence plan lives in shared memory
 constexpr int kSmemLimit = 232448;       // 227 KB opt-in per block on sm_100-class parts
 constexpr uint32_t kRedBarrier = 1;      // named barrier id for the consumer warps
-
-// Consumer warps and threads of a CTA with `groups` consumer groups (group g
-// takes the stages s with s % groups == g) plus one producer warp.
-__host__ __device__ constexpr int consumer_warps(int groups) { return kGroupWarps * groups; }
-__host__ __device__ constexpr int cta_threads(int groups) {
-  return (consumer_warps(groups) + 1) * 32;
-}
 
 enum Kind : int { KIND_PAGED = 0, KIND_TIERED = 1 };
 // STREAM: every CTA takes an equal share of the concatenated key tiles of all
@@ -40,6 +32,32 @@ enum : int {
   DEV_TIMEOUT = 32
 };
 
+// Geometry of one kernel instantiation.
+//   KVB kv heads are processed together, so every token row read from the
+//   pool is KVB * (row bytes of one head) contiguous bytes: >= 512 B keeps
+//   HBM streaming near its peak, 256-byte pieces at a 2 KB stride do not.
+//   W consumer warps; warp w takes kv head w / TG of the block and the
+//   16-key groups g of a tile with g % TG == w % TG, TG = W / KVB.
+//   A paged tile holds TOK = 16*TG keys of each of the KVB heads (one group
+//   per warp); an int8 cold tile 2*16*TG keys (two groups per warp) and a
+//   hot-ring tile 16*TG keys, so every tile moves 32*W*D bytes of K and of V.
+template <int KIND, int D, int KVB>
+struct Geo {
+  static constexpr int W = (D >= 256) ? 4 : 8;
+  static constexpr int TG = W / KVB;
+  static constexpr int ESZ = (KIND == KIND_PAGED) ? 2 : 1;  // bytes of a paged / cold element
+  static constexpr int ROWB = D * ESZ;                        // bytes of one (token, head) row
+  static constexpr int CHN = ROWB / 128;                      // 128-byte slices of such a row
+  static constexpr int CHH = D * 2 / 128;                     // slices of an f16 hot row
+  static constexpr int GPW = (KIND == KIND_PAGED) ? 1 : 2;    // key groups per warp, cold tile
+  static constexpr int TOK = 16 * TG * GPW;                   // keys per paged / cold tile
+  static constexpr int TOKH = 16 * TG;                        // keys per hot-ring tile
+  static constexpr int REGION = 32 * W * D;                   // K (or V) bytes of a stage
+  static constexpr int THREADS = (W + 1) * 32;
+  static_assert(W % KVB == 0, "warps per head");
+  static_assert(TOK * KVB * ROWB == REGION && TOKH * KVB * D * 2 == REGION, "stage fill");
+};
+
 struct alignas(128) KParams {
   CUtensorMap tm_k;   // paged: f16 K pool; tiered: int8 cold K words (as bytes)
   CUtensorMap tm_v;
@@ -48,8 +66,9 @@ struct alignas(128) KParams {
 
   int B, Hq, Hkv, D;
   int G;        // Hq / Hkv
-  int NH;       // heads per unit: min(G, kHeadTile)
+  int NH;       // heads per kv head in a unit: min(G, kHeadTile)
   int HG;       // head groups per kv head: ceil(G / kHeadTile)
+  int KVB;      // kv heads per unit (equals the instantiation's KVB)
   int bs, log2_bs, max_blocks, num_blocks;
   float qscale;     // scale * log2(e): scores are kept in base-2 units
   float softcap2;   // softcap * log2(e) (0 = off)
@@ -67,8 +86,8 @@ struct alignas(128) KParams {
   int* dev_status;
 
   // STREAM workspace
-  float* ws_o;      // [grid][2][kHeadTile][D]
-  float* ws_lse;    // [grid][2][kHeadTile]
+  float* ws_o;      // [grid][2][KVB * kHeadTile][D]
+  float* ws_lse;    // [grid][2][KVB * kHeadTile]
   int* ws_cnt;      // [grid] tickets (one per CTA that starts a cut unit), zero between calls
 
   // SPLIT outputs
@@ -87,10 +106,11 @@ struct alignas(128) KParams {
   const int* hot_starts;
 };
 
-// Per-sequence plan entries kept in shared memory.
+// Per-sequence plan entries kept in shared memory (paged kernels use the
+// first four fields only).
 struct SeqPlan {
   int lo, hi;    // visible absolute key positions [lo, hi)
-  int t0;        // paged: first absolute tile; tiered: first cold tile
+  int t0;        // first paged / cold tile
   int ntiles;    // tiles per unit
   // tiered only
   int ncold;     // cold tiles (they come first)
@@ -98,13 +118,17 @@ struct SeqPlan {
   int ha0, ha1, hb0, hb1;  // hot slot tiles: [ha0, ha1) then [hb0, hb1)
   int cold_len;
 };
+struct SeqPlanPaged {
+  int lo, hi, t0, ntiles;
+};
 
 struct SmemLayout {
   int stage_bytes;
-  int off_k, off_v, off_sc, off_hdr;  // inside a stage
-  int off_stages;                     // from the 1024-aligned base
-  int q_slot_bytes, off_q;            // two-slot Q ring
-  int off_red_o, off_red_ml;
+  int off_k, off_v, off_sc;  // inside a stage
+  int off_stages;            // from the 1024-aligned base
+  int off_hdr;               // per-stage 16-byte headers
+  int off_q;                 // one Q slot: [KVB][NH][D] f32
+  int off_red;               // tree-merge buffer: [W/2][red_floats(D)] f32
   int off_plan, off_pre;
   int off_bar, off_misc;
   int total;  // bytes to request (includes 1 KB of alignment slack)
@@ -112,33 +136,34 @@ struct SmemLayout {
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout make_layout(int kind, int D, int NH, int Hkv, int stages,
-                                                  int B, int groups) {
+// Floats one warp stores to hand its merge state to a partner warp: the
+// O^T fragments (D/4 per lane) plus m and l of its two heads, per lane.
+__host__ __device__ constexpr int red_floats(int D) { return (D / 4 + 4) * 32; }
+
+__host__ __device__ inline SmemLayout make_layout(int kind, int D, int KVB, int W, int region,
+                                                  int tok, int NH, int Hkv, int stages, int B) {
   SmemLayout L;
-  const int kv_region = kTile * D * 2;  // f16 rows (int8 cold rows use the first half)
   L.off_k = 0;
-  L.off_v = kv_region;
-  L.off_sc = 2 * kv_region;
-  const int sc_bytes = (kind == KIND_TIERED) ? align_up(2 * kTile * Hkv * 2, 128) : 0;
-  L.off_hdr = L.off_sc + sc_bytes;
-  L.stage_bytes = align_up(L.off_hdr + 16, 1024);
+  L.off_v = region;
+  L.off_sc = 2 * region;
+  const int sc_bytes = (kind == KIND_TIERED) ? align_up(2 * tok * Hkv * 2, 128) : 0;
+  L.stage_bytes = align_up(L.off_sc + sc_bytes, 1024);
   L.off_stages = 0;
   int off = stages * L.stage_bytes;
-  L.q_slot_bytes = align_up(NH * D * 4, 128);
+  L.off_hdr = off;
+  off += stages * 16;
+  off = align_up(off, 128);
   L.off_q = off;
-  off += 2 * L.q_slot_bytes;
-  L.off_red_o = off;
-  off += consumer_warps(groups) * NH * D * 4;
-  L.off_red_ml = off;
-  off += consumer_warps(groups) * NH * 2 * 4;
-  off = align_up(off, 16);
+  off += align_up(KVB * NH * D * 4, 128);
+  L.off_red = off;
+  off += (W / 2) * red_floats(D) * 4;
   L.off_plan = off;
-  off += B * (int)sizeof(SeqPlan);
+  off += B * (kind == KIND_TIERED ? (int)sizeof(SeqPlan) : (int)sizeof(SeqPlanPaged));
   L.off_pre = off;
   off += (B + 1) * 4;
   off = align_up(off, 8);
   L.off_bar = off;
-  off += (2 * stages + 4) * 8;  // full[stages], empty[stages], qfull[2], qempty[2]
+  off += (2 * stages + 2) * 8;  // full[stages], empty[stages], qfull, qempty
   L.off_misc = off;
   off += 64;
   L.total = off + 1024;

@@ -7,14 +7,24 @@
 
 namespace da {
 
-// Consumer groups of the decode kernel for head dimension D (two groups
-// need about 180 registers per thread; D = 256 keeps one).
-inline int decode_groups(int D) { return D <= 128 ? 2 : 1; }
+// kv heads per work unit for a cache of `kind` with head dimension D and
+// Hkv kv heads: enough that one token row of the block is >= 512
+// contiguous bytes, and a divisor of Hkv.
+inline int decode_kvb(int kind, int D, int Hkv) {
+  int pref = (kind == KIND_PAGED) ? (D == 64 ? 4 : D == 128 ? 2 : 1) : (D == 128 ? 4 : 2);
+  while (pref > 1 && Hkv % pref != 0) pref /= 2;
+  return pref;
+}
 
-// Launches the decode kernel of `kind` for head dimension D (64/128/256 for
-// paged, 128/256 for tiered) with decode_groups(D) consumer groups.  Returns
-// cudaErrorInvalidValue for a D that has no instantiation.
-cudaError_t launch_decode(int kind, int D, const KParams& p, dim3 grid, int smem_bytes,
+// Geometry numbers of the instantiation (kind, D, KVB) for the host.
+struct GeoInfo {
+  int W, TOK, TOKH, REGION, THREADS;
+};
+GeoInfo decode_geo(int kind, int D, int KVB);
+
+// Launches the decode kernel of (kind, D, KVB).  Returns
+// cudaErrorInvalidValue for a combination that has no instantiation.
+cudaError_t launch_decode(int kind, int D, int KVB, const KParams& p, dim3 grid, int smem_bytes,
                           cudaStream_t stream);
 
 // out/lse from max_splits partial states per (b, h).
