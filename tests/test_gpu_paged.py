@@ -190,11 +190,12 @@ def test_workspace_reuse_across_shapes():
     batch shapes: only its leading ticket counters must stay zero."""
     import torch
     big = _case(1200, 256, 8, 2, 16, [777, 511, 129, 64, 3])
-    params = qk.make_params(torch.empty(big.B, big.Hq, big.D), big.block_size, big.Hkv,
-                            big.max_blocks, big.num_blocks, max_seq_len=big.max_seq_len)
-    ws = torch.zeros(qk.decode_attn_workspace_size(params), dtype=torch.uint8, device="cuda")
     cases = [big, _case(1201, 64, 8, 2, 16, EDGE_LENS), _case(1202, 128, 8, 4, 32, [900, 5, 300]),
              big]
+    nbytes = max(qk.decode_attn_workspace_size(
+        qk.make_params(torch.empty(c.B, c.Hq, c.D), c.block_size, c.Hkv, c.max_blocks,
+                       c.num_blocks, max_seq_len=c.max_seq_len)) for c in cases)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
     for case in cases:
         t = case.device_tensors("cuda")
         out, lse = qk.decode_attn_paged(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
