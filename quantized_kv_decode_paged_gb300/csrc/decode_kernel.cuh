@@ -954,34 +954,59 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   const int ticket = misc->ticket;
   if (ticket == c1 - c0) {
     __threadfence();
+    // One float4 of one head row per thread; the participants' states are
+    // read in batches of eight (all loads in flight together) and folded
+    // with a running log-sum-exp.
     const long long urow0 = (long long)s.b * p.Hq + s.hg * kHeadTile;
-    for (int idx = tid; idx < KVB * NH * D; idx += NCW * 32) {
-      const int d = idx % D;
-      const int hh = idx / D;
+    constexpr int D4 = D / 4;
+    const int nk = c1 - c0 + 1;
+    for (int idx = tid; idx < KVB * NH * D4; idx += NCW * 32) {
+      const int d4 = idx % D4;
+      const int hh = idx / D4;
       const int ks = hh / NH, h = hh % NH;
-      float M = kNegInf;
-      for (int cc = c0; cc <= c1; ++cc) {
-        const long long sl = (long long)stream_slot(cc, c0, g0, T, sg) * (KVB * kHeadTile) +
-                             ks * kHeadTile + h;
-        M = fmaxf(M, __ldcg(p.ws_lse + sl));
-      }
-      float o = 0.f, lse = kNegInf;
-      if (M != kNegInf) {
-        float Ws = 0.f, Os = 0.f;
-        for (int cc = c0; cc <= c1; ++cc) {
-          const long long sl = (long long)stream_slot(cc, c0, g0, T, sg) * (KVB * kHeadTile) +
-                               ks * kHeadTile + h;
-          const float ls = __ldcg(p.ws_lse + sl);
-          const float w = (ls == kNegInf) ? 0.f : expf(ls - M);
-          Ws += w;
-          Os += w * __ldcg(p.ws_o + sl * D + d);
+      const int rowoff = ks * kHeadTile + h;
+      float M = kNegInf, Wsum = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k0 = 0; k0 < nk; k0 += 8) {
+        float ls[8];
+        float4 ov[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          ls[j] = kNegInf;
+          ov[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (k0 + j < nk) {
+            const long long sl =
+                (long long)stream_slot(c0 + k0 + j, c0, g0, T, sg) * (KVB * kHeadTile) + rowoff;
+            ls[j] = __ldcg(p.ws_lse + sl);
+            ov[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + sl * D) + d4);
+          }
         }
-        o = Os / Ws;
-        lse = M + logf(Ws);
+        float mb = kNegInf;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mb = fmaxf(mb, ls[j]);
+        const float mn = fmaxf(M, mb);
+        if (mn == kNegInf) continue;
+        const float f = (M == kNegInf) ? 0.f : expf(M - mn);
+        Wsum *= f;
+        O.x *= f; O.y *= f; O.z *= f; O.w *= f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float w = (ls[j] == kNegInf) ? 0.f : expf(ls[j] - mn);
+          Wsum += w;
+          O.x += w * ov[j].x; O.y += w * ov[j].y; O.z += w * ov[j].z; O.w += w * ov[j].w;
+        }
+        M = mn;
+      }
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lse = kNegInf;
+      if (M != kNegInf) {
+        const float inv = 1.f / Wsum;
+        o = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+        lse = M + logf(Wsum);
       }
       const long long orow = urow0 + (long long)(s.kvb * KVB + ks) * p.G + h;
-      p.out[orow * D + d] = o;
-      if (d == 0 && p.lse) p.lse[orow] = lse;
+      reinterpret_cast<float4*>(p.out + orow * D)[d4] = o;
+      if (d4 == 0 && p.lse) p.lse[orow] = lse;
     }
     if (tid == 0) p.ws_cnt[c0] = 0;
   }
