@@ -100,6 +100,16 @@ float effective_qscale(const da_params* p) {
   return (float)s * 1.4426950408889634f;
 }
 
+// DA_KVB=n in the environment asks for n kv heads per unit (a tuning knob);
+// it is used only when an instantiation exists and n divides Hkv.
+int kvb_override(int kind, int D, int Hkv, int kvb) {
+  const char* e = getenv("DA_KVB");
+  if (!e) return kvb;
+  const int v = atoi(e);
+  if (v >= 1 && Hkv % v == 0 && da::decode_geo(kind, D, v).W != 0) return v;
+  return kvb;
+}
+
 void fill_common(KParams& k, const da_params* p) {
   k.B = p->batch;
   k.Hq = p->num_q_heads;
@@ -117,6 +127,7 @@ void fill_common(KParams& k, const da_params* p) {
   k.window = p->sliding_window;
   k.causal = p->causal;
   k.KVB = da::decode_kvb(da::KIND_PAGED, p->head_dim, p->num_kv_heads);
+  k.KVB = kvb_override(da::KIND_PAGED, p->head_dim, p->num_kv_heads, k.KVB);
 }
 
 int encode_pool_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
@@ -223,8 +234,9 @@ WsLayout ws_layout(int grid, int D, int kvb) {
 
 // kv heads per unit the workspace must serve (either cache kind).
 int ws_kvb(const da_params* p) {
-  const int a = da::decode_kvb(da::KIND_PAGED, p->head_dim, p->num_kv_heads);
-  const int b = da::decode_kvb(da::KIND_TIERED, p->head_dim, p->num_kv_heads);
+  const int D = p->head_dim, H = p->num_kv_heads;
+  const int a = kvb_override(da::KIND_PAGED, D, H, da::decode_kvb(da::KIND_PAGED, D, H));
+  const int b = kvb_override(da::KIND_TIERED, D, H, da::decode_kvb(da::KIND_TIERED, D, H));
   return a > b ? a : b;
 }
 
@@ -456,7 +468,8 @@ int decode_attn_tiered_int8(const da_params* p, const da_tier_params* t, const f
   KParams k;
   memset(&k, 0, sizeof(k));
   fill_common(k, p);
-  k.KVB = da::decode_kvb(da::KIND_TIERED, p->head_dim, p->num_kv_heads);
+  k.KVB = kvb_override(da::KIND_TIERED, p->head_dim, p->num_kv_heads,
+                       da::decode_kvb(da::KIND_TIERED, p->head_dim, p->num_kv_heads));
   st = encode_paged_maps(k, da::KIND_TIERED, k_cold, v_cold, p);
   if (st != DA_OK) return st;
   {

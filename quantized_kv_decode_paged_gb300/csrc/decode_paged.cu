@@ -42,6 +42,7 @@ GeoInfo decode_geo(int kind, int D, int KVB) {
   if (D == 64 && KVB == 4) return geo_info<KIND_PAGED, 64, 4>();
   if (D == 128 && KVB == 1) return geo_info<KIND_PAGED, 128, 1>();
   if (D == 128 && KVB == 2) return geo_info<KIND_PAGED, 128, 2>();
+  if (D == 128 && KVB == 4) return geo_info<KIND_PAGED, 128, 4>();
   if (D == 256 && KVB == 1) return geo_info<KIND_PAGED, 256, 1>();
   return g;
 }
@@ -54,6 +55,7 @@ cudaError_t launch_decode(int kind, int D, int KVB, const KParams& p, dim3 grid,
   if (D == 64 && KVB == 4) return launch_decode_impl<KIND_PAGED, 64, 4>(p, grid, smem, stream);
   if (D == 128 && KVB == 1) return launch_decode_impl<KIND_PAGED, 128, 1>(p, grid, smem, stream);
   if (D == 128 && KVB == 2) return launch_decode_impl<KIND_PAGED, 128, 2>(p, grid, smem, stream);
+  if (D == 128 && KVB == 4) return launch_decode_impl<KIND_PAGED, 128, 4>(p, grid, smem, stream);
   if (D == 256 && KVB == 1) return launch_decode_impl<KIND_PAGED, 256, 1>(p, grid, smem, stream);
   return cudaErrorInvalidValue;
 }
