@@ -201,6 +201,30 @@ int decode_attn_split_merge(int32_t batch, int32_t num_q_heads, int32_t head_dim
                             int32_t max_splits, const float* o_part, const float* lse_part,
                             float* out, float* lse, void* stream);
 
+/*
+ * decode_attn_paged_static_ws — decode_attn_paged (split path) for callers
+ * that cannot allocate device memory: graph-captured regions, plugins whose
+ * host framework owns every allocation, loops that cannot take
+ * cudaMalloc's implicit synchronisation.  The pages have no counterpart for
+ * this entry point; it only changes where the scratch lives.
+ *
+ * The scratch is a buffer of DECODE_ATTN_STATIC_WS_BYTES bytes compiled into
+ * the library (held by every GPU that loads it, until exit).  The call
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * The first call on a device looks up the buffer's device address
+ * (cudaGetSymbolAddress) and should come before any stream capture.  Each
+ * call clears the buffer's ticket counters on `stream` (cudaMemsetAsync)
+ * and launches on `stream`; calls that overlap on the GPU share the buffer
+ * and race.  Arguments, layouts, outputs and device flags are those of
+ * decode_attn_paged.  Returns DA_ERR_WORKSPACE when
+ * decode_attn_workspace_size(p) exceeds DECODE_ATTN_STATIC_WS_BYTES.
+ */
+#define DECODE_ATTN_STATIC_WS_BYTES (8u << 20)
+int decode_attn_paged_static_ws(const da_params* p, const float* q, const uint16_t* k_pool,
+                                const uint16_t* v_pool, const int32_t* block_table,
+                                const int32_t* seq_lens, const int32_t* q_pos, float* out,
+                                float* lse, int32_t* dev_status, void* stream);
+
 /* Bytes of workspace the split path of decode_attn_paged /
  * decode_attn_tiered_int8 needs for these parameters on the current device;
  * 0 when p is invalid. */

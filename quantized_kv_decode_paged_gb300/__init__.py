@@ -24,8 +24,8 @@ __all__ = [
     "load_library", "library_path", "build",
     "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_status_string",
-    "DecodeAttnError", "DEV_BAD_BLOCK", "DEV_BAD_SEQ_LEN", "DEV_BAD_QPOS",
-    "DEV_SPLIT_OVERFLOW", "DEV_BAD_TIER", "DEV_TIMEOUT",
+    "decode_attn_paged_static_ws", "DecodeAttnError", "DEV_BAD_BLOCK", "DEV_BAD_SEQ_LEN",
+    "DEV_BAD_QPOS", "DEV_SPLIT_OVERFLOW", "DEV_BAD_TIER", "DEV_TIMEOUT",
 ]
 
 DEV_BAD_BLOCK = 1
@@ -44,7 +44,7 @@ DA_ERR_CUDA = -4
 _EXPORTS = (
     "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_workspace_init",
-    "decode_attn_status_string",
+    "decode_attn_status_string", "decode_attn_paged_static_ws",
 )
 
 
@@ -118,6 +118,9 @@ def load_library():
         lib.decode_attn_workspace_size.argtypes = [ctypes.POINTER(DaParams)]
         lib.decode_attn_workspace_init.restype = ctypes.c_int
         lib.decode_attn_workspace_init.argtypes = [P, ctypes.c_size_t, P]
+        lib.decode_attn_paged_static_ws.restype = ctypes.c_int
+        lib.decode_attn_paged_static_ws.argtypes = [ctypes.POINTER(DaParams), P, P, P, P, P,
+                                                    P, P, P, P, P]
         lib.decode_attn_status_string.restype = ctypes.c_char_p
         lib.decode_attn_status_string.argtypes = [ctypes.c_int]
         _lib = lib
@@ -246,6 +249,38 @@ def decode_attn_paged(q, k_pool, v_pool, block_table, seq_lens, q_pos=None, *, s
                                _ptr(lse), ws_ptr, ws_bytes, _ptr(dev_status),
                                _stream(dev, stream))
     _check("decode_attn_paged", st)
+    return out, lse
+
+
+def decode_attn_paged_static_ws(q, k_pool, v_pool, block_table, seq_lens, q_pos=None, *,
+                                scale=0.0, softcap=0.0, sliding_window=0, causal=True,
+                                max_seq_len=0, out=None, lse=None, dev_status=None, stream=None):
+    """decode_attn_paged with its split-KV scratch in the library's own fixed
+    buffer: for callers that must not allocate device memory.  The output
+    tensors are still the caller's (allocated here only when not given)."""
+    torch = _torch()
+    lib = load_library()
+    dev = q.device
+    _req(q, "q", torch.float32, dev, 3)
+    _req(k_pool, "k_pool", torch.float16, dev, 4)
+    _req(v_pool, "v_pool", torch.float16, dev, 4)
+    _req(block_table, "block_table", torch.int32, dev, 2)
+    _req(seq_lens, "seq_lens", torch.int32, dev, 1)
+    if q_pos is not None:
+        _req(q_pos, "q_pos", torch.int32, dev, 1)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    params = make_params(q, bs, Hkv, block_table.shape[1], NB, scale=scale, softcap=softcap,
+                         sliding_window=sliding_window, causal=causal, max_seq_len=max_seq_len)
+    st = lib.decode_attn_paged_static_ws(ctypes.byref(params), _ptr(q), _ptr(k_pool),
+                                         _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
+                                         _ptr(q_pos), _ptr(out), _ptr(lse), _ptr(dev_status),
+                                         _stream(dev, stream))
+    _check("decode_attn_paged_static_ws", st)
     return out, lse
 
 

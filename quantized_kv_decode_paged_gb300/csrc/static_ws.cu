@@ -1,0 +1,75 @@
+// static_ws.cu — decode_attn_paged_static_ws: the split-KV paged decode with
+// its scratch taken from a buffer compiled into the library, for callers
+// that must not allocate device memory themselves.
+//
+// Who needs it: code that runs where cudaMalloc is not an option — inside a
+// region being captured into a CUDA graph, in an inference-server plugin
+// whose host framework owns all device memory, or in a latency-critical
+// loop that cannot afford cudaMalloc's implicit device synchronisation.
+//
+// The buffer is a file-scope __device__ array of DECODE_ATTN_STATIC_WS_BYTES
+// bytes; every GPU that loads this library holds it until the process exits.
+// Host code cannot pass the array's name to a kernel (on the host it is only
+// a stand-in symbol), so the first call on each device looks up its device
+// address with cudaGetSymbolAddress, with that device current, and keeps it.
+// Because of that lookup, the first call on a device should come before any
+// stream capture.
+//
+// Every call uses the same array.  The ticket counters at its start must be
+// zero when a call begins; each call clears them on its stream before the
+// launch.  Calls whose work overlaps on the GPU (different streams without
+// ordering, or several host threads) race on the array.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/decode_attn.h"
+
+namespace {
+
+constexpr size_t kStaticWsBytes = DECODE_ATTN_STATIC_WS_BYTES;
+// Bytes at the start of the buffer that hold the ticket counters (one int
+// per CTA, at most 1024 CTAs); cleared before every call.
+constexpr size_t kTicketBytes = 4096;
+
+__device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+constexpr int kMaxDevices = 128;
+void* g_ws_addr[kMaxDevices] = {nullptr};
+std::mutex g_ws_mu;
+
+// Device address of g_static_ws on the current device (looked up once).
+int static_ws_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  if (!g_ws_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) return DA_ERR_CUDA;
+    g_ws_addr[dev] = ptr;
+  }
+  *out = g_ws_addr[dev];
+  return DA_OK;
+}
+
+}  // namespace
+
+extern "C" int decode_attn_paged_static_ws(const da_params* p, const float* q,
+                                           const uint16_t* k_pool, const uint16_t* v_pool,
+                                           const int32_t* block_table, const int32_t* seq_lens,
+                                           const int32_t* q_pos, float* out, float* lse,
+                                           int32_t* dev_status, void* stream) {
+  if (!p) return DA_ERR_INVALID;
+  const size_t need = decode_attn_workspace_size(p);
+  if (need == 0) return DA_ERR_INVALID;
+  if (need > kStaticWsBytes) return DA_ERR_WORKSPACE;
+  void* ws = nullptr;
+  int st = static_ws_address(&ws);
+  if (st != DA_OK) return st;
+  const size_t clear = kTicketBytes < need ? kTicketBytes : need;
+  if (cudaMemsetAsync(ws, 0, clear, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return decode_attn_paged(p, q, k_pool, v_pool, block_table, seq_lens, q_pos, out, lse, ws, need,
+                           dev_status, stream);
+}

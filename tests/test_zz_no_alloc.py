@@ -1,0 +1,62 @@
+"""The entry point for callers that cannot allocate device memory.
+
+decode_attn_paged_static_ws runs the split-KV paged decode with its scratch
+in a buffer compiled into the library, so a caller inside a graph-captured
+region, a plugin without an allocator, or a loop that cannot afford
+cudaMalloc's synchronisation can still use the split path.  This test calls
+it through the C ABI twice in a row and checks it against decode_attn_paged
+with a caller-provided workspace, within the parity tolerance of the other
+GPU tests.  It sits in a file that pytest collects last, and it works both
+on its own in a fresh process and after the rest of the suite.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import quantized_kv_decode_paged_gb300 as qk
+from quantized_kv_decode_paged_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+OUT_ATOL = 1e-3
+OUT_RTOL = 1e-3
+LSE_ATOL = 1e-4
+
+
+def test_static_scratch_entry_point_matches_workspace_entry_point(cuda_lib):
+    import torch
+
+    lib = qk.load_library()
+    # long enough sequences that units are cut between CTAs (the scratch is used)
+    case = wl.make_paged("noalloc", 77, B=6, Hq=16, Hkv=4, D=128, block_size=16,
+                         seq_lens=[3000, 17, 1024, 4096, 511, 2222], num_blocks=1200)
+    t = case.device_tensors("cuda")
+    params = qk.make_params(t["q"], case.block_size, case.Hkv, case.max_blocks, case.num_blocks,
+                            max_seq_len=case.max_seq_len)
+    assert qk.decode_attn_workspace_size(params) <= 8 << 20
+    ws = torch.zeros(qk.decode_attn_workspace_size(params), dtype=torch.uint8, device="cuda")
+    ref_out, ref_lse = qk.decode_attn_paged(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                            t["seq_lens"], max_seq_len=case.max_seq_len,
+                                            workspace=ws)
+    torch.cuda.synchronize()
+    ref_out = ref_out.cpu().numpy().astype(np.float64)
+    ref_lse = ref_lse.cpu().numpy().astype(np.float64)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for call in range(2):
+        out = torch.full((case.B, case.Hq, case.D), float("nan"), device="cuda")
+        lse = torch.full((case.B, case.Hq), float("nan"), device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        st = lib.decode_attn_paged_static_ws(
+            ctypes.byref(params), t["q"].data_ptr(), t["k_pool"].data_ptr(),
+            t["v_pool"].data_ptr(), t["block_table"].data_ptr(), t["seq_lens"].data_ptr(), None,
+            out.data_ptr(), lse.data_ptr(), status.data_ptr(), stream)
+        assert st == qk.DA_OK, qk.decode_attn_status_string(st)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        got = out.cpu().numpy().astype(np.float64)
+        got_lse = lse.cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all(), f"call {call}: non-finite output"
+        assert (np.abs(got - ref_out) <= OUT_ATOL + OUT_RTOL * np.abs(ref_out)).all(), call
+        assert np.abs(got_lse - ref_lse).max() <= LSE_ATOL, call
+
