@@ -110,6 +110,16 @@ int kvb_override(int kind, int D, int Hkv, int kvb) {
   return kvb;
 }
 
+// Whether to launch the packed variant: at most four query heads per kv
+// head leave half of the MMA's eight columns free for the remainder parts.
+// DA_PACK=0 in the environment forces the unpacked variant (a tuning and
+// testing knob).
+bool use_packed(const KParams& k) {
+  if (k.NH > 4) return false;
+  const char* e = getenv("DA_PACK");
+  return !(e && e[0] == '0' && e[1] == '\0');
+}
+
 void fill_common(KParams& k, const da_params* p) {
   k.B = p->batch;
   k.Hq = p->num_q_heads;
@@ -296,7 +306,8 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
       if (grid < 1) grid = 1;
     }
     k.grid = grid;
-    cudaError_t e = da::launch_decode(lc.kind, k.D, k.KVB, k, dim3(grid), smem, stream);
+    cudaError_t e = da::launch_decode(lc.kind, k.D, k.KVB, use_packed(k), k, dim3(grid), smem,
+                                      stream);
     if (e != cudaSuccess) return DA_ERR_CUDA;
   }
   return DA_OK;
@@ -415,7 +426,8 @@ int decode_attn_split_partial(const da_params* p, int32_t split_tokens, int32_t 
     kk.o_part = o_part + (long long)b0 * Hq * max_splits * D;
     kk.lse_part = lse_part + (long long)b0 * Hq * max_splits;
     kk.grid = max_splits;
-    cudaError_t e = da::launch_decode(da::KIND_PAGED, kk.D, kk.KVB, kk, dim3(max_splits, nb * upb), smem,
+    cudaError_t e = da::launch_decode(da::KIND_PAGED, kk.D, kk.KVB, use_packed(kk), kk,
+                                      dim3(max_splits, nb * upb), smem,
                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return DA_ERR_CUDA;
   }

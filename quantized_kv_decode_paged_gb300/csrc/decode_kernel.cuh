@@ -539,6 +539,10 @@ struct Acc {
   float m[2], l[2];    // heads 2c, 2c+1 (base-2 units)
 };
 
+// Q^T B fragments.  Unpacked: hi and lo parts as two operands (one MMA
+// each).  Packed (at most four heads per kv head): hi holds columns 0-3 =
+// f16 part of heads 0-3 and columns 4-7 = remainder of the same heads, so
+// one MMA yields both parts of every score; lo is unused.
 template <int D>
 struct QFrag {
   uint32_t hi[D / 16][2], lo[D / 16][2];
@@ -560,10 +564,11 @@ __device__ __forceinline__ int o_row_d(int mt, int r, int hi8) {
 // Q rows of the head group, prescaled (scale*log2 e), as hi/lo f16 B
 // fragments.  Natural order: k-step ks covers d = 16ks + {2c, 2c+1} and
 // {2c+8, 2c+9}; permuted order (tiered): d = 16ks + 4c + {0, 1} and {2, 3}.
-template <int KIND, int D>
+template <int KIND, int D, bool PK>
 __device__ __forceinline__ void load_q(uint32_t qs, int NH, float qscale, int r, int c,
                                        QFrag<D>& q) {
-  const bool hv = r < NH;
+  const int hq = PK ? (r & 3) : r;  // head of B column r
+  const bool hv = hq < NH;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     int d0, d2;
@@ -576,7 +581,7 @@ __device__ __forceinline__ void load_q(uint32_t qs, int NH, float qscale, int r,
     }
     float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
     if (hv) {
-      const uint32_t row = qs + (uint32_t)(r * D) * 4u;
+      const uint32_t row = qs + (uint32_t)(hq * D) * 4u;
       const uint2 a = lds64(row + d0 * 4);
       const uint2 b = lds64(row + d2 * 4);
       x0 = __uint_as_float(a.x) * qscale;
@@ -586,6 +591,12 @@ __device__ __forceinline__ void load_q(uint32_t qs, int NH, float qscale, int r,
     }
     split_half2(x0, x1, q.hi[ks][0], q.lo[ks][0]);
     split_half2(x2, x3, q.hi[ks][1], q.lo[ks][1]);
+    if constexpr (PK) {
+      if (r >= 4) {
+        q.hi[ks][0] = q.lo[ks][0];
+        q.hi[ks][1] = q.lo[ks][1];
+      }
+    }
   }
 }
 
@@ -612,11 +623,25 @@ struct RowMap {
   }
 };
 
-// S^T[16 keys x 8 heads] of keys k0..k0+15.  Four accumulators (hi/lo Q
-// parts x even/odd k-steps) keep the dependency chains short.
-template <int TK, int D>
+// S^T[16 keys x 8 heads] of keys k0..k0+15 into NCH accumulators (summed
+// by the caller): unpacked, half take the hi Q part and half the lo part;
+// packed, k-step ks goes to accumulator ks mod NCH.  Several accumulators
+// keep the MMA dependency chains short.
+template <int TK, int D, bool PK, int NCH>
+__device__ __forceinline__ void qk_mma(float (&s4)[NCH][4], int ks, uint32_t a0, uint32_t a1,
+                                       uint32_t a2, uint32_t a3, const QFrag<D>& q) {
+  if constexpr (PK) {
+    mma_f16_16816(s4[ks % NCH], a0, a1, a2, a3, q.hi[ks][0], q.hi[ks][1]);
+  } else {
+    constexpr int H = NCH / 2;
+    mma_f16_16816(s4[ks % H], a0, a1, a2, a3, q.hi[ks][0], q.hi[ks][1]);
+    mma_f16_16816(s4[H + ks % H], a0, a1, a2, a3, q.lo[ks][0], q.lo[ks][1]);
+  }
+}
+
+template <int TK, int D, bool PK, int NCH>
 __device__ __forceinline__ void tile_qk(const RowMap& km, int k0, int lane, const QFrag<D>& q,
-                                        float (&s4)[4][4]) {
+                                        float (&s4)[NCH][4]) {
   const int r = lane >> 2, c = lane & 3;
   if constexpr (TK == TK_PAGED) {
     const int mat = lane >> 3;
@@ -629,8 +654,7 @@ __device__ __forceinline__ void tile_qk(const RowMap& km, int k0, int lane, cons
       const int ug = 2 * ks + dh;
       uint32_t a0, a1, a2, a3;
       ldsm_x4(rowaddr + (ug >> 3) * km.cstride + (((ug & 7) ^ x) << 4), a0, a1, a2, a3);
-      mma_f16_16816(s4[(ks & 1)], a0, a1, a2, a3, q.hi[ks][0], q.hi[ks][1]);
-      mma_f16_16816(s4[2 + (ks & 1)], a0, a1, a2, a3, q.lo[ks][0], q.lo[ks][1]);
+      qk_mma<TK, D, PK, NCH>(s4, ks, a0, a1, a2, a3, q);
     }
   } else if constexpr (TK == TK_COLD) {
     // int8 rows of D bytes: word c of 16-byte unit ks holds d = 16ks + 4c .. +3
@@ -643,8 +667,7 @@ __device__ __forceinline__ void tile_qk(const RowMap& km, int k0, int lane, cons
       const uint32_t w1 = lds32(rb1 + off) ^ 0x80808080u;
       const uint32_t a0 = biased_i8x2_to_h2(w0, 0x4140u), a2 = biased_i8x2_to_h2(w0, 0x4342u);
       const uint32_t a1 = biased_i8x2_to_h2(w1, 0x4140u), a3 = biased_i8x2_to_h2(w1, 0x4342u);
-      mma_f16_16816(s4[(ks & 1)], a0, a1, a2, a3, q.hi[ks][0], q.hi[ks][1]);
-      mma_f16_16816(s4[2 + (ks & 1)], a0, a1, a2, a3, q.lo[ks][0], q.lo[ks][1]);
+      qk_mma<TK, D, PK, NCH>(s4, ks, a0, a1, a2, a3, q);
     }
   } else {
     // f16 rows: 8 bytes at d = 16ks + 4c
@@ -656,14 +679,23 @@ __device__ __forceinline__ void tile_qk(const RowMap& km, int k0, int lane, cons
       const uint32_t off = (ks >> 2) * km.cstride + ((u ^ r) << 4);
       const uint2 v0 = lds64(rb0 + off);
       const uint2 v1 = lds64(rb1 + off);
-      mma_f16_16816(s4[(ks & 1)], v0.x, v1.x, v0.y, v1.y, q.hi[ks][0], q.hi[ks][1]);
-      mma_f16_16816(s4[2 + (ks & 1)], v0.x, v1.x, v0.y, v1.y, q.lo[ks][0], q.lo[ks][1]);
+      qk_mma<TK, D, PK, NCH>(s4, ks, v0.x, v1.x, v0.y, v1.y, q);
     }
   }
 }
 
+// One m-tile of O^T += V^T P^T: hi then lo P parts, or the packed operand
+// alone (columns 0-3 f16 part, 4-7 remainder).
+template <bool PK>
+__device__ __forceinline__ void pv_mma(float (&o)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                       uint32_t a3, uint32_t bh0, uint32_t bh1, uint32_t bl0,
+                                       uint32_t bl1) {
+  mma_f16_16816(o, a0, a1, a2, a3, bh0, bh1);
+  if constexpr (!PK) mma_f16_16816(o, a0, a1, a2, a3, bl0, bl1);
+}
+
 // O^T += V^T P^T for keys k0..k0+15; b* are the P^T fragments.
-template <int TK, int D>
+template <int TK, int D, bool PK>
 __device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, float (&o)[D / 16][4],
                                         uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
   const int r = lane >> 2, c = lane & 3;
@@ -678,8 +710,7 @@ __device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, floa
       const int ug = 2 * mt + dh;
       uint32_t a0, a1, a2, a3;
       ldsm_x4_trans(rowaddr + (ug >> 3) * vm.cstride + (((ug & 7) ^ x) << 4), a0, a1, a2, a3);
-      mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
-      mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+      pv_mma<PK>(o[mt], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
     }
   } else if constexpr (TK == TK_COLD) {
     // word q = 8pp + r (d = 4q .. 4q+3) of keys 2c, 2c+1, 2c+8, 2c+9
@@ -699,14 +730,12 @@ __device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, floa
       {
         const uint32_t a0 = biased_i8x2_to_h2(E, 0x4140u), a1 = biased_i8x2_to_h2(E, 0x4342u);
         const uint32_t a2 = biased_i8x2_to_h2(E2, 0x4140u), a3 = biased_i8x2_to_h2(E2, 0x4342u);
-        mma_f16_16816(o[2 * pp], a0, a1, a2, a3, bh0, bh1);
-        mma_f16_16816(o[2 * pp], a0, a1, a2, a3, bl0, bl1);
+        pv_mma<PK>(o[2 * pp], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
       }
       {
         const uint32_t a0 = biased_i8x2_to_h2(F, 0x4140u), a1 = biased_i8x2_to_h2(F, 0x4342u);
         const uint32_t a2 = biased_i8x2_to_h2(F2, 0x4140u), a3 = biased_i8x2_to_h2(F2, 0x4342u);
-        mma_f16_16816(o[2 * pp + 1], a0, a1, a2, a3, bh0, bh1);
-        mma_f16_16816(o[2 * pp + 1], a0, a1, a2, a3, bl0, bl1);
+        pv_mma<PK>(o[2 * pp + 1], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
       }
     }
   } else {
@@ -725,43 +754,62 @@ __device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, floa
       {
         const uint32_t a0 = __byte_perm(A.x, B.x, 0x5410u), a1 = __byte_perm(A.x, B.x, 0x7632u);
         const uint32_t a2 = __byte_perm(C.x, E.x, 0x5410u), a3 = __byte_perm(C.x, E.x, 0x7632u);
-        mma_f16_16816(o[2 * pp], a0, a1, a2, a3, bh0, bh1);
-        mma_f16_16816(o[2 * pp], a0, a1, a2, a3, bl0, bl1);
+        pv_mma<PK>(o[2 * pp], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
       }
       {
         const uint32_t a0 = __byte_perm(A.y, B.y, 0x5410u), a1 = __byte_perm(A.y, B.y, 0x7632u);
         const uint32_t a2 = __byte_perm(C.y, E.y, 0x5410u), a3 = __byte_perm(C.y, E.y, 0x7632u);
-        mma_f16_16816(o[2 * pp + 1], a0, a1, a2, a3, bh0, bh1);
-        mma_f16_16816(o[2 * pp + 1], a0, a1, a2, a3, bl0, bl1);
+        pv_mma<PK>(o[2 * pp + 1], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
       }
     }
   }
 }
 
-// One 16-key group of this warp: QK, mask, online softmax, PV.
-// vA / vB: validity of keys k0+r and k0+r+8.  ksA.. / vsA..: per-key K and
-// V scales of the int8 tier (rows r and r+8), 1 otherwise.
-template <int TK, int D>
-__device__ __forceinline__ void group_compute(const RowMap& km, const RowMap& vm, float softcap2,
-                                              int k0, int lane, const QFrag<D>& q, Acc<D>& a,
-                                              bool vA, bool vB, float ksA, float ksB, float vsA,
-                                              float vsB) {
-  float s4[4][4];
+// NG 16-key groups of this warp (keys k0[g] .. k0[g]+15) in one online-
+// softmax step: the QK products, one running-max update, then the PV
+// products.  v[2g], v[2g+1]: validity of keys k0[g]+r and k0[g]+r+8;
+// ks / vs: their K and V scales in the int8 tier (1 otherwise).  Taking two
+// groups at once halves the serial max/rescale work per key and gives the
+// warp two independent QK chains to interleave.
+template <int TK, int D, bool PK, int NG>
+__device__ __forceinline__ void groups_compute(const RowMap& km, const RowMap& vm,
+                                               float softcap2, const int (&k0)[NG], int lane,
+                                               const QFrag<D>& q, Acc<D>& a,
+                                               const bool (&v)[2 * NG],
+                                               const float (&ks)[2 * NG],
+                                               const float (&vs)[2 * NG]) {
+  constexpr int NCH = NG == 1 ? 4 : 2;
+  float s4[NG][NCH][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) s4[i][0] = s4[i][1] = s4[i][2] = s4[i][3] = 0.f;
-  tile_qk<TK, D>(km, k0, lane, q, s4);
-  float sc[4];
+  for (int g = 0; g < NG; ++g)
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float v = (s4[0][j] + s4[1][j]) + (s4[2][j] + s4[3][j]);
-    if constexpr (TK == TK_COLD) v *= (j < 2 ? ksA : ksB);
-    if (softcap2 > 0.f) v = softcap2 * tanhf(v / softcap2);
-    sc[j] = v;
+    for (int i = 0; i < NCH; ++i) s4[g][i][0] = s4[g][i][1] = s4[g][i][2] = s4[g][i][3] = 0.f;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) tile_qk<TK, D, PK, NCH>(km, k0[g], lane, q, s4[g]);
+  float sc[NG][4];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float x = s4[g][0][j];
+#pragma unroll
+      for (int i = 1; i < NCH; ++i) x += s4[g][i][j];
+      // packed: column h + 4 (lane c ^ 2) holds the remainder part of head h
+      if constexpr (PK) x += __shfl_xor_sync(0xffffffffu, x, 2);
+      if constexpr (TK == TK_COLD) x *= ks[2 * g + (j >> 1)];
+      if (softcap2 > 0.f) x = softcap2 * tanhf(x / softcap2);
+      sc[g][j] = x;
+    }
+    if (!v[2 * g]) sc[g][0] = sc[g][1] = kNegInf;
+    if (!v[2 * g + 1]) sc[g][2] = sc[g][3] = kNegInf;
   }
-  if (!vA) sc[0] = sc[1] = kNegInf;
-  if (!vB) sc[2] = sc[3] = kNegInf;
   // ---- online softmax (base 2)
-  float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+  float mx0 = fmaxf(sc[0][0], sc[0][2]), mx1 = fmaxf(sc[0][1], sc[0][3]);
+#pragma unroll
+  for (int g = 1; g < NG; ++g) {
+    mx0 = fmaxf(mx0, fmaxf(sc[g][0], sc[g][2]));
+    mx1 = fmaxf(mx1, fmaxf(sc[g][1], sc[g][3]));
+  }
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -772,10 +820,19 @@ __device__ __forceinline__ void group_compute(const RowMap& km, const RowMap& vm
   const float al1 = (mn1 == kNegInf) ? 1.f : exp2f(a.m[1] - mn1);
   const float mu0 = (mn0 == kNegInf) ? 0.f : mn0;
   const float mu1 = (mn1 == kNegInf) ? 0.f : mn1;
-  float p0 = exp2f(sc[0] - mu0), p1 = exp2f(sc[1] - mu1);
-  float p2 = exp2f(sc[2] - mu0), p3 = exp2f(sc[3] - mu1);
-  a.l[0] = a.l[0] * al0 + (p0 + p2);
-  a.l[1] = a.l[1] * al1 + (p1 + p3);
+  float pr[NG][4];
+  float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    pr[g][0] = exp2f(sc[g][0] - mu0);
+    pr[g][1] = exp2f(sc[g][1] - mu1);
+    pr[g][2] = exp2f(sc[g][2] - mu0);
+    pr[g][3] = exp2f(sc[g][3] - mu1);
+    ls0 += pr[g][0] + pr[g][2];
+    ls1 += pr[g][1] + pr[g][3];
+  }
+  a.l[0] = a.l[0] * al0 + ls0;
+  a.l[1] = a.l[1] * al1 + ls1;
   a.m[0] = mn0;
   a.m[1] = mn1;
   if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {
@@ -787,20 +844,43 @@ __device__ __forceinline__ void group_compute(const RowMap& km, const RowMap& vm
       a.o[mt][3] *= al1;
     }
   }
-  if constexpr (TK == TK_COLD) {
-    // the V scale of each key folds into its weight (masked keys: exactly 0)
-    p0 = vA ? p0 * vsA : 0.f;
-    p1 = vA ? p1 * vsA : 0.f;
-    p2 = vB ? p2 * vsB : 0.f;
-    p3 = vB ? p3 * vsB : 0.f;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    float p0 = pr[g][0], p1 = pr[g][1], p2 = pr[g][2], p3 = pr[g][3];
+    if constexpr (TK == TK_COLD) {
+      // the V scale of each key folds into its weight (masked keys: exactly 0)
+      p0 = v[2 * g] ? p0 * vs[2 * g] : 0.f;
+      p1 = v[2 * g] ? p1 * vs[2 * g] : 0.f;
+      p2 = v[2 * g + 1] ? p2 * vs[2 * g + 1] : 0.f;
+      p3 = v[2 * g + 1] ? p3 * vs[2 * g + 1] : 0.f;
+    }
+    // ---- P^T as the B operand (hi + lo), via an 8x8 transpose
+    uint32_t h01, l01, h23, l23;
+    split_half2(p0, p1, h01, l01);
+    split_half2(p2, p3, h23, l23);
+    if constexpr (PK) {
+      // lanes c < 2 give columns 0-3 (f16 parts), lanes c >= 2 columns 4-7
+      const bool lo_cols = (lane & 2) != 0;
+      const uint32_t b0 = movmatrix_trans(lo_cols ? l01 : h01);
+      const uint32_t b1 = movmatrix_trans(lo_cols ? l23 : h23);
+      tile_pv<TK, D, PK>(vm, k0[g], lane, a.o, b0, b1, 0u, 0u);
+    } else {
+      const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+      const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+      tile_pv<TK, D, PK>(vm, k0[g], lane, a.o, bh0, bh1, bl0, bl1);
+    }
   }
-  // ---- P^T as the B operand (hi + lo), via an 8x8 transpose
-  uint32_t h01, l01, h23, l23;
-  split_half2(p0, p1, h01, l01);
-  split_half2(p2, p3, h23, l23);
-  const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-  const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-  tile_pv<TK, D>(vm, k0, lane, a.o, bh0, bh1, bl0, bl1);
+}
+
+// One 16-key group (keys k0 .. k0+15) of an f16 tile.
+template <int TK, int D, bool PK>
+__device__ __forceinline__ void group_compute(const RowMap& km, const RowMap& vm, float softcap2,
+                                              int k0, int lane, const QFrag<D>& q, Acc<D>& a,
+                                              bool vA, bool vB) {
+  const int k0s[1] = {k0};
+  const bool v[2] = {vA, vB};
+  const float one[2] = {1.f, 1.f};
+  groups_compute<TK, D, PK, 1>(km, vm, softcap2, k0s, lane, q, a, v, one, one);
 }
 
 // Zeroes the f16 V rows of masked keys among k0..k0+15 of this warp's head,
@@ -872,7 +952,7 @@ __device__ __forceinline__ void store_state(const Acc<D>& a, float* red, int lan
 }
 
 // Merges the warps of each kv head of segment s and writes the result.
-template <int KIND, int D, int KVB>
+template <int KIND, int D, int KVB, bool PK>
 __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, Acc<D>& a,
                                                float* red, Misc* misc, const int* pre,
                                                const PlanStore<KIND>& plan) {
@@ -884,6 +964,14 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   const int r = lane >> 2, c = lane & 3;
   const int kvs = warp / TG, tg = warp % TG;
   const int NH = p.NH;
+  if constexpr (PK) {
+    // fold the remainder columns (lane c ^ 2) into the f16-part columns;
+    // both lanes of a pair then hold the same state
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) a.o[mt][k] += __shfl_xor_sync(0xffffffffu, a.o[mt][k], 2);
+  }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     float l = a.l[j];
@@ -902,7 +990,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   }
   const int kv = s.kvb * KVB + kvs;
   const long long row0 = (long long)s.b * p.Hq + (long long)kv * p.G + s.hg * kHeadTile;
-  if (tg == 0) {
+  if (tg == 0 && (!PK || c < 2)) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int h = 2 * c + j;
@@ -1013,7 +1101,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   named_bar_sync(kRedBarrier, NCW * 32);
 }
 
-template <int KIND, int D, int KVB>
+template <int KIND, int D, int KVB, bool PK>
 __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<KIND>& plan,
                                               const int* pre, uint8_t* stages, uint8_t* hdrs,
                                               uint8_t* qslot, const SmemLayout& L,
@@ -1074,7 +1162,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
         return;
       }
-      load_q<KIND, D>(smem_u32(qslot + kvs * NH * D * 4), NH, qscale, r, c, q);
+      load_q<KIND, D, PK>(smem_u32(qslot + kvs * NH * D * 4), NH, qscale, r, c, q);
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty);
       ++qn;
@@ -1119,24 +1207,31 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
           const int j = bs <= Gm::TOK ? (k >> bg.log2R) : 0;
           return ((bad_mask >> j) & 1u) == 0;
         };
-#pragma unroll
-        for (int gp = 0; gp < Gm::GPW; ++gp) {
-          const int k0 = 16 * (tg + gp * TG);
+        if constexpr (KIND == KIND_PAGED) {
+          static_assert(Gm::GPW == 1, "one key group per warp in an f16 tile");
+          const int k0 = 16 * tg;
           const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
-          if (!__any_sync(0xffffffffu, vA || vB)) continue;
-          if constexpr (KIND == KIND_PAGED) {
+          if (__any_sync(0xffffffffu, vA || vB)) {
             if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
-            group_compute<TK_PAGED, D>(km, vm, softcap2, k0, lane, q, a, vA, vB, 1.f, 1.f, 1.f,
-                                       1.f);
-          } else {
+            group_compute<TK_PAGED, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB);
+          }
+        } else {
+          // both key groups of the warp in one softmax step (int8 values are
+          // always finite, so masked keys need only a zero weight)
+          static_assert(Gm::GPW == 2, "two key groups per warp in a cold tile");
+          const int k0[2] = {16 * tg, 16 * (tg + TG)};
+          const bool v[4] = {ok(k0[0] + r), ok(k0[0] + r + 8), ok(k0[1] + r), ok(k0[1] + r + 8)};
+          if (__any_sync(0xffffffffu, v[0] || v[1] || v[2] || v[3])) {
             const uint32_t sck = smem_u32(st + L.off_sc);
             const uint32_t scv = sck + Gm::TOK * Hkv * 2;
-            const uint32_t iA = ((k0 + r) * Hkv + kv) * 2, iB = iA + 8 * Hkv * 2;
-            group_compute<TK_COLD, D>(km, vm, softcap2, k0, lane, q, a, vA, vB,
-                                      __half2float(__ushort_as_half(lds16(sck + iA))),
-                                      __half2float(__ushort_as_half(lds16(sck + iB))),
-                                      __half2float(__ushort_as_half(lds16(scv + iA))),
-                                      __half2float(__ushort_as_half(lds16(scv + iB))));
+            float ks[4], vs[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t off = ((k0[i >> 1] + r + 8 * (i & 1)) * Hkv + kv) * 2;
+              ks[i] = __half2float(__ushort_as_half(lds16(sck + off)));
+              vs[i] = __half2float(__ushort_as_half(lds16(scv + off)));
+            }
+            groups_compute<TK_COLD, D, PK, 2>(km, vm, softcap2, k0, lane, q, a, v, ks, vs);
           }
         }
       } else if constexpr (KIND == KIND_TIERED) {
@@ -1153,7 +1248,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
         if (__any_sync(0xffffffffu, vA || vB)) {
           if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
-          group_compute<TK_HOT, D>(km, vm, softcap2, k0, lane, q, a, vA, vB, 1.f, 1.f, 1.f, 1.f);
+          group_compute<TK_HOT, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB);
         }
       }
       __syncwarp();
@@ -1163,12 +1258,14 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         ++round;
       }
     }
-    finish_segment<KIND, D, KVB>(p, s, a, red, misc, pre, plan);
+    finish_segment<KIND, D, KVB, PK>(p, s, a, red, misc, pre, plan);
   }
 }
 
 // ================================================================ kernel
-template <int KIND, int D, int KVB>
+// PK: Q/P f16 and remainder parts packed into one MMA operand (requires at
+// most four query heads per kv head).
+template <int KIND, int D, int KVB, bool PK>
 __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
     decode_attn_kernel(const __grid_constant__ KParams p) {
   using Gm = Geo<KIND, D, KVB>;
@@ -1244,11 +1341,14 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
   if (p.sched != SCHED_SPLIT && warp == 0) plan_prefix<KIND>(plan, pre, p.B, units_per_seq(p), tid & 31);
   __syncthreads();
 
-  if (warp == NCW) {
-    producer_loop<KIND, D, KVB>(p, plan, pre, stages, hdrs, qslot, L, bg, full, empty, qfull,
-                                qempty, misc);
+  if (warp >= NCW) {
+    if constexpr (Gm::REG_SPLIT) setmaxnreg_dec<Gm::REG_PROD>();
+    if (warp == NCW)
+      producer_loop<KIND, D, KVB>(p, plan, pre, stages, hdrs, qslot, L, bg, full, empty, qfull,
+                                  qempty, misc);
   } else {
-    consumer_loop<KIND, D, KVB>(p, plan, pre, stages, hdrs, qslot, L, bg, full, empty, qfull,
+    if constexpr (Gm::REG_SPLIT) setmaxnreg_inc<Gm::REG_CONS>();
+    consumer_loop<KIND, D, KVB, PK>(p, plan, pre, stages, hdrs, qslot, L, bg, full, empty, qfull,
                                 qempty, red, misc);
   }
   __syncthreads();

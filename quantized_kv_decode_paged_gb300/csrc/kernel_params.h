@@ -53,7 +53,17 @@ struct Geo {
   static constexpr int TOK = 16 * TG * GPW;                   // keys per paged / cold tile
   static constexpr int TOKH = 16 * TG;                        // keys per hot-ring tile
   static constexpr int REGION = 32 * W * D;                   // K (or V) bytes of a stage
-  static constexpr int THREADS = (W + 1) * 32;
+  // Eight consumer warps share the SM with a producer warpgroup (the TMA
+  // warp and three idle warps) so that registers can move between
+  // warpgroups: the producer group gives up registers with setmaxnreg and
+  // the consumers take them (REG_PROD / REG_CONS per thread; the launch
+  // gives every warp REG_LAUNCH).  Four consumer warps need no such split.
+  static constexpr bool REG_SPLIT = (W == 8);
+  static constexpr int THREADS = REG_SPLIT ? (W + 4) * 32 : (W + 1) * 32;
+  static constexpr int REG_LAUNCH = 168, REG_PROD = 72, REG_CONS = 216;
+  static_assert(!REG_SPLIT || (W * REG_CONS + 4 * REG_PROD <= (W + 4) * REG_LAUNCH),
+                "register split must fit in the launch's registers");
+  static_assert(!REG_SPLIT || (W + 4) * 32 * REG_LAUNCH <= 65536, "launch registers");
   static_assert(W % KVB == 0, "warps per head");
   static_assert(TOK * KVB * ROWB == REGION && TOKH * KVB * D * 2 == REGION, "stage fill");
 };

@@ -22,10 +22,12 @@ struct GeoInfo {
 };
 GeoInfo decode_geo(int kind, int D, int KVB);
 
-// Launches the decode kernel of (kind, D, KVB).  Returns
-// cudaErrorInvalidValue for a combination that has no instantiation.
-cudaError_t launch_decode(int kind, int D, int KVB, const KParams& p, dim3 grid, int smem_bytes,
-                          cudaStream_t stream);
+// Launches the decode kernel of (kind, D, KVB); `packed` selects the variant
+// that packs the f16 and remainder parts of Q and P into one MMA operand
+// (valid when p.NH <= 4).  Returns cudaErrorInvalidValue for a combination
+// that has no instantiation.
+cudaError_t launch_decode(int kind, int D, int KVB, bool packed, const KParams& p, dim3 grid,
+                          int smem_bytes, cudaStream_t stream);
 
 // out/lse from max_splits partial states per (b, h).
 cudaError_t launch_split_merge(int rows, int max_splits, int D, const float* o_part,

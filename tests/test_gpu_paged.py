@@ -49,10 +49,23 @@ EDGE_LENS = [1, 7, 8, 9, 15, 16, 17, 63, 64, 65, 127, 128, 129, 200, 511, 777]
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 8, 16])
 def test_head_dims_and_group_sizes(D, G):
     Hkv = 2
     case = _case(100 + D + G, D, G * Hkv, Hkv, 16, EDGE_LENS[:: 2 if D == 256 else 1])
+    for mode in MODES:
+        _check_all_rows(case, mode)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("G", [1, 3, 4])
+def test_unpacked_variant_for_small_groups(D, G, monkeypatch):
+    """Groups of at most four heads normally pack the f16 and remainder parts
+    of Q and P into one MMA operand; DA_PACK=0 selects the two-operand
+    variant, which must agree with the oracle as well."""
+    monkeypatch.setenv("DA_PACK", "0")
+    Hkv = 2
+    case = _case(150 + D + G, D, G * Hkv, Hkv, 16, EDGE_LENS[:: 2 if D == 256 else 1])
     for mode in MODES:
         _check_all_rows(case, mode)
 

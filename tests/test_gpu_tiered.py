@@ -54,9 +54,19 @@ def test_tier_block_sizes(bs):
     _check(case)
 
 
-@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 8, 16])
 def test_tier_group_sizes(G):
     case = wl.make_tiered(f"g{G}", 40 + G, B=2, Hq=2 * G, Hkv=2, D=128, block_size=16,
+                          cold_len=200, hot_len=70, hot_window=96, hot_start=200)
+    _check(case)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("G", [1, 3, 4])
+def test_tier_unpacked_variant_for_small_groups(D, G, monkeypatch):
+    """DA_PACK=0: the two-operand variant for groups of at most four heads."""
+    monkeypatch.setenv("DA_PACK", "0")
+    case = wl.make_tiered(f"u{D}_{G}", 60 + G + D, B=2, Hq=2 * G, Hkv=2, D=D, block_size=16,
                           cold_len=200, hot_len=70, hot_window=96, hot_start=200)
     _check(case)
 
