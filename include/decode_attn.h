@@ -83,7 +83,9 @@ enum {
   DA_DEV_BAD_QPOS = 4,       /* q_pos[b] < 0: the row is written as empty (out 0, lse -inf)   */
   DA_DEV_SPLIT_OVERFLOW = 8, /* split_partial: keys past max_splits*split_tokens were dropped  */
   DA_DEV_BAD_TIER = 16,      /* tiered: hot_len > ring capacity or negative tier length        */
-  DA_DEV_TIMEOUT = 32        /* an internal pipeline wait gave up (never expected)             */
+  DA_DEV_TIMEOUT = 32        /* an internal pipeline wait ran past its time limit (never      */
+                             /* expected; 2 s, or DA_WAIT_LIMIT_MS): the kernel then ends     */
+                             /* without waiting further and its outputs are undefined          */
 };
 
 typedef struct {

@@ -120,6 +120,23 @@ bool use_packed(const KParams& k) {
   return !(e && e[0] == '0' && e[1] == '\0');
 }
 
+// Test knobs for the bounded waits.  DA_WAIT_LIMIT_MS sets the time limit
+// of every wait inside the kernels (default 2000 ms); DA_TEST_SKIP_ARM=1 makes
+// CTA 0 leave its first stage unarmed, so that its consumers' wait runs out
+// and the kernel ends in abort mode with DA_DEV_TIMEOUT (no copy is issued
+// for that stage and nothing faults).
+unsigned long long wait_limit_ns() {
+  const char* e = getenv("DA_WAIT_LIMIT_MS");
+  long long ms = e ? atoll(e) : 2000;
+  if (ms < 1) ms = 1;
+  if (ms > 10000) ms = 10000;
+  return (unsigned long long)ms * 1000000ull;
+}
+int test_skip_arm() {
+  const char* e = getenv("DA_TEST_SKIP_ARM");
+  return (e && e[0] == '1' && e[1] == '\0') ? 1 : 0;
+}
+
 void fill_common(KParams& k, const da_params* p) {
   k.B = p->batch;
   k.Hq = p->num_q_heads;
@@ -138,6 +155,8 @@ void fill_common(KParams& k, const da_params* p) {
   k.causal = p->causal;
   k.KVB = da::decode_kvb(da::KIND_PAGED, p->head_dim, p->num_kv_heads);
   k.KVB = kvb_override(da::KIND_PAGED, p->head_dim, p->num_kv_heads, k.KVB);
+  k.wait_ns = wait_limit_ns();
+  k.test_skip_arm = test_skip_arm();
 }
 
 int encode_pool_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,

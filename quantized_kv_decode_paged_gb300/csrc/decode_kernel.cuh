@@ -65,7 +65,21 @@ struct SegIter {
 struct Misc {
   int flags;
   int ticket;
+  int abort;  // set when a wait gave up: see note_abort
 };
+
+// A wait that gave up (its time limit passed, or another warp had already
+// given up) puts the CTA in abort mode: every later wait returns at once,
+// the producer issues no more copies, and every warp still runs its loops
+// to the end -- on whatever is in shared memory -- so that the barriers
+// stay matched and the kernel ends.  The host sees DEV_TIMEOUT.
+__device__ __forceinline__ void note_abort(Misc* misc) {
+  *reinterpret_cast<volatile int*>(&misc->abort) = 1;
+  atomicOr(&misc->flags, DEV_TIMEOUT);
+}
+__device__ __forceinline__ const volatile int* abort_flag(Misc* misc) {
+  return reinterpret_cast<const volatile int*>(&misc->abort);
+}
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
@@ -419,6 +433,10 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
   int stage = 0;
   uint32_t round = 0;
   int qn = 0;  // non-empty segments so far (Q slot phase)
+  // stages (bit j) holding an issued copy, and the phase parity it completes
+  uint32_t iss_mask = 0, iss_par = 0;
+  bool q_iss = false;
+  uint32_t q_par = 0;
   int bt_b = -1, bt_base = 0, bt_cur = -1, bt_nxt = -1;
   int flags = 0;
   while (seg_next<KIND, Gm::TOK>(p, plan, pre, it, s)) {
@@ -428,11 +446,13 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
     const int* bt_row = p.block_table + (long long)s.b * max_blocks;
     // ---- Q rows of the unit (KVB x NH heads) into the Q slot
     {
-      if (!mbar_wait(qempty, (qn & 1) ^ 1)) {
-        if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
-        return;
+      if (!mbar_wait(qempty, (qn & 1) ^ 1, abort_flag(misc), p.wait_ns) && lane == 0) note_abort(misc);
+      const bool live = !__any_sync(0xffffffffu, *abort_flag(misc) != 0);
+      if (live) {
+        q_iss = true;
+        q_par = qn & 1;
       }
-      if (lane == 0) {
+      if (lane == 0 && live) {
         const uint32_t per = (uint32_t)(p.NH * D * 4);
         mbar_arrive_expect_tx(qfull, per * KVB);
         const float* qb = p.q + (long long)s.b * p.Hq * D;
@@ -447,14 +467,15 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
       ++qn;
     }
     for (int i = s.i0; i < s.i1; ++i) {
-      if (!mbar_wait(&empty[stage], (round & 1) ^ 1)) {
-        if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
-        return;
-      }
+      if (!mbar_wait(&empty[stage], (round & 1) ^ 1, abort_flag(misc), p.wait_ns) && lane == 0)
+        note_abort(misc);
       uint8_t* st = stages + (size_t)stage * L.stage_bytes;
       bool is_hot;
       const int at = tile_of<KIND>(e, i, is_hot);
-      if (!is_hot) {
+      if (__any_sync(0xffffffffu, *abort_flag(misc) != 0) ||
+          (p.test_skip_arm && blockIdx.x == 0 && iss_mask == 0)) {
+        // abort mode (or the test knob): no copy, the stage stays unarmed
+      } else if (!is_hot) {
         // ----- pages through the block table
         const int tok0 = at * Gm::TOK;
         const int p_first = tok0 >> log2_bs;
@@ -491,6 +512,8 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
           mbar_arrive_expect_tx(&full[stage], (uint32_t)__popc(need_mask) * page_bytes);
         }
         __syncwarp();
+        iss_mask |= 1u << stage;
+        iss_par = (iss_par & ~(1u << stage)) | ((round & 1u) << stage);
         for (int base = 0; base < bg.npg * OPS; base += 32) {
           const int op = base + lane;
           const int j = op / OPS;
@@ -517,6 +540,8 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
           mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * Gm::REGION));
         }
         __syncwarp();
+        iss_mask |= 1u << stage;
+        iss_par = (iss_par & ~(1u << stage)) | ((round & 1u) << stage);
         if (lane < 2) {
           uint8_t* dst = st + (lane ? L.off_v : L.off_k);
           tma_load_5d(dst, lane ? &p.tm_vh : &p.tm_kh, &full[stage], 0, at * Gm::TOKH, 0, kv0,
@@ -529,6 +554,12 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
       }
     }
   }
+  // No copy may still be in flight when the CTA exits: wait (bounded, and
+  // also in abort mode) for the last one issued into each stage and the Q slot.
+  for (int j = 0; j < nstages; ++j)
+    if (((iss_mask >> j) & 1u) && !mbar_wait_lazy(&full[j], (iss_par >> j) & 1u, p.wait_ns))
+      flags |= DEV_TIMEOUT;
+  if (q_iss && !mbar_wait_lazy(qfull, q_par, p.wait_ns)) flags |= DEV_TIMEOUT;
   if (flags && lane == 0) atomicOr(&misc->flags, flags);
 }
 
@@ -1158,10 +1189,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
     const SeqPlan e = plan.get(s.pidx);
     const int kv = s.kvb * KVB + kvs;
     {
-      if (!mbar_wait(qfull, qn & 1)) {
-        if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
-        return;
-      }
+      if (!mbar_wait(qfull, qn & 1, abort_flag(misc), p.wait_ns) && lane == 0) note_abort(misc);
       load_q<KIND, D, PK>(smem_u32(qslot + kvs * NH * D * 4), NH, qscale, r, c, q);
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty);
@@ -1184,10 +1212,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
     const int vhc = (KIND == KIND_TIERED) ? min(s.vhi, e.cold_len) : s.vhi;
 
     for (int i = s.i0; i < s.i1; ++i) {
-      if (!mbar_wait(&full[stage], round & 1)) {
-        if (lane == 0) atomicOr(&misc->flags, DEV_TIMEOUT);
-        return;
-      }
+      if (!mbar_wait(&full[stage], round & 1, abort_flag(misc), p.wait_ns) && lane == 0) note_abort(misc);
       uint8_t* st = stages + (size_t)stage * L.stage_bytes;
       const uint32_t bad_mask = lds32(smem_u32(hdrs + stage * 16));
       bool is_hot;
@@ -1307,6 +1332,7 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
     fence_mbarrier_init();
     misc->flags = 0;
     misc->ticket = 0;
+    misc->abort = 0;
   }
   if (warp == NCW && (tid & 31) == 0) {
     prefetch_tensormap(&p.tm_k);

@@ -86,6 +86,8 @@ struct alignas(128) KParams {
   int stages;
   int sched;
   int grid;         // CTAs of the launch (STREAM / UNITS)
+  unsigned long long wait_ns;  // time limit of every wait (abort mode after it)
+  int test_skip_arm;  // test knob: CTA 0 never arms its first stage (a wait runs out)
 
   const float* q;
   const int* block_table;

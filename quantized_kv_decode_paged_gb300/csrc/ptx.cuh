@@ -55,15 +55,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
-// false if that did not happen within `limit_ns` nanoseconds.
+// false if that did not happen within `limit_ns` nanoseconds, or as soon as
+// `*abort` (when given) is found set.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
+                                          const volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    if ((++spins & 255u) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// As mbar_wait, for a warp off the critical path: it naps between polls
+// (up to 256 ns) so that it takes no issue slots from busy warps.
+__device__ __forceinline__ bool mbar_wait_lazy(uint64_t* bar, uint32_t parity,
+                                               uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t ns = 32;
+  while (true) {
+    __nanosleep(ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (ns < 256) ns <<= 1;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
