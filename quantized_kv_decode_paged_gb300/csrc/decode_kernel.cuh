@@ -58,7 +58,10 @@ struct Seg {
 };
 
 struct SegIter {
-  long long g, g_end;
+  long long g, g_end;  // next position and end of this CTA's range
+  long long s0;        // start of the range
+  long long fwd_end;   // end of the forward pass
+  long long last0;     // start of the range's last segment when it goes first, else -1
   int n;
 };
 
@@ -280,17 +283,45 @@ __device__ __forceinline__ int stream_grid(const KParams& p, long long T) {
 }
 __device__ __forceinline__ int units_per_seq(const KParams& p) { return (p.Hkv / p.KVB) * p.HG; }
 
-__device__ __forceinline__ void seg_init(const KParams& p, const int* pre, SegIter& it) {
+// Sequence whose tile positions contain g: the largest b with pre[b] <= g.
+__device__ __forceinline__ int seq_of(const KParams& p, const int* pre, long long g) {
+  int lo = 0, hi = p.B;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (pre[mid] <= g) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// STREAM order inside a CTA's range: when the range ends inside a unit that
+// continues in the next CTA, that last segment goes first, then the rest in
+// order.  Every unit cut between CTAs is then worked on at the start of its
+// participants' ranges, so the partial states, tickets and the merge happen
+// early, and a CTA's range ends with whole units (no cross-CTA work at the
+// end of the kernel).
+template <int KIND>
+__device__ __forceinline__ void seg_init(const KParams& p, const PlanStore<KIND>& plan,
+                                         const int* pre, SegIter& it) {
   it.n = 0;
+  it.last0 = -1;
   if (p.sched == SCHED_STREAM) {
     const long long T = pre[p.B];
     const int sg = stream_grid(p, T);
     if ((int)blockIdx.x >= sg) {
-      it.g = it.g_end = 0;
+      it.g = it.g_end = it.s0 = it.fwd_end = 0;
       return;
     }
-    it.g = stream_start(blockIdx.x, T, sg);
-    it.g_end = stream_start(blockIdx.x + 1, T, sg);
+    it.g = it.s0 = stream_start(blockIdx.x, T, sg);
+    it.g_end = it.fwd_end = stream_start(blockIdx.x + 1, T, sg);
+    if (it.g_end > it.g) {
+      const int b = seq_of(p, pre, it.g_end - 1);
+      const int nt = plan.ntiles(b);
+      const long long u0 = pre[b] + (it.g_end - 1 - pre[b]) / nt * nt;  // unit start
+      if (u0 > it.s0 && u0 + nt > it.g_end) {
+        it.last0 = u0;
+        it.fwd_end = u0;
+      }
+    }
   } else if (p.sched == SCHED_UNITS) {
     const long long U = (long long)p.B * units_per_seq(p);
     it.g = (long long)blockIdx.x * U / p.grid;
@@ -306,16 +337,15 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
                                          const int* pre, SegIter& it, Seg& s) {
   const int upb = units_per_seq(p);
   if (p.sched == SCHED_STREAM) {
-    if (it.g >= it.g_end) return false;
-    int lo = 0, hi = p.B;  // largest b with pre[b] <= g
-    while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
-      if (pre[mid] <= it.g) lo = mid; else hi = mid;
-    }
-    const int b = lo;
+    // the range's last segment first (see seg_init), then [s0, fwd_end)
+    const bool last_first = it.last0 >= 0;
+    const long long g = last_first ? it.last0 : it.g;
+    const long long end = last_first ? it.g_end : it.fwd_end;
+    if (g >= end) return false;
+    const int b = seq_of(p, pre, g);
     const SeqPlan e = plan.get(b);
     const int nt = e.ntiles;
-    const long long local = it.g - pre[b];
+    const long long local = g - pre[b];
     const int uib = (int)(local / nt);
     s.b = b;
     s.pidx = b;
@@ -323,13 +353,18 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
     s.hg = uib % p.HG;
     s.unit = b * upb + uib;
     s.i0 = (int)(local % nt);
-    long long rem = it.g_end - it.g;
+    const long long rem = end - g;
     s.i1 = (int)((long long)s.i0 + rem < nt ? s.i0 + rem : nt);
     s.vlo = e.lo;
     s.vhi = e.hi;
     s.dest = (s.i0 == 0 && s.i1 == nt) ? DEST_OUT : DEST_PARTIAL;
-    s.slot = it.n == 0 ? 0 : 1;
-    it.g += s.i1 - s.i0;
+    // partial slot: 0 for the segment at the start of the range, 1 for the
+    // one at its end (the only two that can be partial)
+    s.slot = g == it.s0 ? 0 : 1;
+    if (last_first)
+      it.last0 = -1;
+    else
+      it.g += s.i1 - s.i0;
     it.n++;
     return true;
   }
@@ -385,7 +420,8 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
 }
 
 // Flat index of the partial slot of participant c of a unit whose first
-// tile is g0 (STREAM): slot 1 when the unit is not c's first segment.
+// tile is g0 (STREAM): slot 1 when the unit starts after c's range does
+// (it is the segment at the end of c's range), else slot 0.
 __device__ __forceinline__ int stream_slot(int c, int c0, long long g0, long long T, int grid) {
   const int j = (c == c0 && stream_start(c, T, grid) < g0) ? 1 : 0;
   return c * 2 + j;
@@ -428,7 +464,7 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
   const uint32_t page_bytes =
       (uint32_t)(2 * bg.box_bytes + (KIND == KIND_TIERED ? 2 * bg.R * Hkv * 2 : 0));
   SegIter it;
-  seg_init(p, pre, it);
+  seg_init<KIND>(p, plan, pre, it);
   Seg s;
   int stage = 0;
   uint32_t round = 0;
@@ -1055,7 +1091,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     }
   }
   if (s.dest != DEST_PARTIAL) return;
-  __threadfence();
+  if (tg == 0) __threadfence();  // the warps that wrote the partial state
   named_bar_sync(kRedBarrier, NCW * 32);
   // ---- last-arriver merge of the unit's partial states
   const long long T = pre[p.B];
@@ -1066,8 +1102,8 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   const long long g1 = g0 + nt - 1;
   const int c0 = stream_cta_of(g0, T, sg);
   const int c1 = stream_cta_of(g1, T, sg);
-  // A unit cut between CTAs is the last segment of its first CTA c0, so c0
-  // names the unit's ticket counter.
+  // A unit cut between CTAs is the segment at the end of its first CTA c0's
+  // range, so c0 names the unit's ticket counter.
   if (tid == 0) misc->ticket = atomicAdd(&p.ws_cnt[c0], 1);
   named_bar_sync(kRedBarrier, NCW * 32);
   const int ticket = misc->ticket;
@@ -1164,7 +1200,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   }
 
   SegIter it;
-  seg_init(p, pre, it);
+  seg_init<KIND>(p, plan, pre, it);
   Seg s;
   int stage = 0;
   uint32_t round = 0;
