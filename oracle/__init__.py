@@ -79,6 +79,7 @@ class _TieredArgs(ctypes.Structure):
         ("block_table", ctypes.c_void_p), ("cold_lens", ctypes.c_void_p),
         ("hot_lens", ctypes.c_void_p), ("hot_starts", ctypes.c_void_p),
         ("q_pos", ctypes.c_void_p),
+        ("k_cold_f16", ctypes.c_void_p), ("v_cold_f16", ctypes.c_void_p),
     ]
 
 
@@ -249,7 +250,44 @@ def decode_tiered(q, k_hot, v_hot, k_cold, v_cold, k_scale, v_scale, block_table
                        int(sliding_window), int(bool(causal)), int(hot_window), cap,
                        _ptr(q), _ptr(k_hot), _ptr(v_hot), _ptr(k_cold), _ptr(v_cold),
                        _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(cold_lens),
-                       _ptr(hot_lens), _ptr(hot_starts), _ptr(q_pos))
+                       _ptr(hot_lens), _ptr(hot_starts), _ptr(q_pos), None, None)
+    rows_a = _rows_arg(rows)
+    n = B * Hq if rows_a is None else len(rows_a)
+    out = np.zeros((n, D), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    flags = _load().oracle_decode_tiered(ctypes.byref(args), _ptr(rows_a), n, _ptr(out), _ptr(lse))
+    return out, lse, int(flags)
+
+
+def decode_tiered_f16(q, k_hot, v_hot, k_cold, v_cold, block_table, cold_lens, hot_lens,
+                      hot_starts, *, hot_window, q_pos=None, scale=0.0, softcap=0.0,
+                      sliding_window=0, causal=True, rows=None):
+    """Tiered f16-cold / f16-hot decode attention (the f16 tiered layout of
+    doppler attention.js executeAttentionTiered).
+
+    k_hot/v_hot float16 [B, cap, Hkv, D]; k_cold/v_cold float16 [NB, bs, Hkv, D];
+    cold_lens/hot_lens/hot_starts int32 [B].  Returns (out [n, D], lse [n], flags)."""
+    keep = _Keep()
+    q = keep(q, np.float32)
+    k_hot = keep(k_hot, np.float16)
+    v_hot = keep(v_hot, np.float16)
+    k_cold = keep(k_cold, np.float16)
+    v_cold = keep(v_cold, np.float16)
+    block_table = keep(block_table, np.int32)
+    B, Hq, D = q.shape
+    cold_lens = keep(np.broadcast_to(np.asarray(cold_lens, dtype=np.int32), (B,)), np.int32)
+    hot_lens = keep(np.broadcast_to(np.asarray(hot_lens, dtype=np.int32), (B,)), np.int32)
+    hot_starts = keep(np.broadcast_to(np.asarray(hot_starts, dtype=np.int32), (B,)), np.int32)
+    q_pos = keep(q_pos, np.int32)
+    Bh, cap, Hkv, D2 = k_hot.shape
+    NB, bs, Hkv2, D3 = k_cold.shape
+    assert Bh == B and D2 == D and Hkv2 == Hkv and D3 == D and v_cold.shape == k_cold.shape
+    args = _TieredArgs(B, Hq, Hkv, D, bs, block_table.shape[1], NB,
+                       float(np.float32(scale)), float(np.float32(softcap)),
+                       int(sliding_window), int(bool(causal)), int(hot_window), cap,
+                       _ptr(q), _ptr(k_hot), _ptr(v_hot), None, None, None, None,
+                       _ptr(block_table), _ptr(cold_lens), _ptr(hot_lens), _ptr(hot_starts),
+                       _ptr(q_pos), _ptr(k_cold), _ptr(v_cold))
     rows_a = _rows_arg(rows)
     n = B * Hq if rows_a is None else len(rows_a)
     out = np.zeros((n, D), dtype=np.float64)

@@ -27,6 +27,10 @@
  *       times the f16 scale of (token, kv head)), get_hot_pos (slot =
  *       (hot_start + j) % hot_window, or j when hot_window = 0), absolute
  *       position of hot key j = hot_start + j.
+ *   [E] @simulatte/doppler 0.1.0 "attention.js", executeAttentionTiered:
+ *       the tiered cache with an f16 cold tier paged through "coldPageTable"
+ *       and an f16 hot ring (its kernel body is not on the pages: the cold
+ *       values are read as f16 and everything else is as in [T]).
  *   [S] com.microsoft.SparseAttention "sparse-attention.wgsl.jinja",
  *       combine_partials: m = max(m1, m2), d = d1 e^(m1-m) + d2 e^(m2-m),
  *       used here in its log-sum-exp form for the split merge.
@@ -297,7 +301,7 @@ void oracle_split_merge(int64_t nrows, int64_t max_splits, int64_t D, const doub
 }
 
 /* ================================================================== */
-/* Tiered decode: int8 cold pages + f16 hot ring                      */
+/* Tiered decode: int8 [T] or f16 [E] cold pages + f16 hot ring       */
 /* ================================================================== */
 typedef struct {
   int64_t B, Hq, Hkv, D, block_size, max_blocks, num_blocks;
@@ -316,6 +320,9 @@ typedef struct {
   const int32_t* hot_lens;    /* [B] */
   const int32_t* hot_starts;  /* [B] */
   const int32_t* q_pos;       /* [B] or NULL */
+  /* [E] f16 cold tier instead of the int8 words and scales (NULL for [T]) */
+  const uint16_t* k_cold_f16; /* [NB, bs, Hkv, D] f16 bits */
+  const uint16_t* v_cold_f16;
 } oracle_tiered_args;
 
 /* A visible key of the tiered cache: cold (page row) or hot (ring row). */
@@ -338,6 +345,9 @@ static void tiered_fetch_v(const void* ctx, int64_t i, double* v) {
   tiered_key k = c->keys[i];
   if (k.is_hot) {
     const uint16_t* row = a->v_hot + (k.row * a->Hkv + c->kv) * D;
+    for (int64_t d = 0; d < D; ++d) v[d] = oracle_half_to_double(row[d]);
+  } else if (a->v_cold_f16) {
+    const uint16_t* row = a->v_cold_f16 + (k.row * a->Hkv + c->kv) * D;
     for (int64_t d = 0; d < D; ++d) v[d] = oracle_half_to_double(row[d]);
   } else {
     const uint32_t* words = a->v_cold + (k.row * a->Hkv + c->kv) * (D / 4);
@@ -404,14 +414,19 @@ static void tiered_row(const oracle_tiered_args* a, int64_t b, int64_t h, double
       continue;
     }
     int64_t row = blk * a->block_size + t % a->block_size;
-    const uint32_t* words = a->k_cold + (row * a->Hkv + kv) * (D / 4);
-    double sc = oracle_half_to_double(a->k_scale[row * a->Hkv + kv]);
     double dot = 0.0;
-    for (int64_t w = 0; w < D / 4; ++w) {
-      int32_t vals[4];
-      oracle_unpack_int8_word(words[w], vals);
-      for (int lane = 0; lane < 4; ++lane)
-        dot += (double)qrow[4 * w + lane] * ((double)vals[lane] * sc);
+    if (a->k_cold_f16) {
+      const uint16_t* krow = a->k_cold_f16 + (row * a->Hkv + kv) * D;
+      for (int64_t d = 0; d < D; ++d) dot += (double)qrow[d] * oracle_half_to_double(krow[d]);
+    } else {
+      const uint32_t* words = a->k_cold + (row * a->Hkv + kv) * (D / 4);
+      double sc = oracle_half_to_double(a->k_scale[row * a->Hkv + kv]);
+      for (int64_t w = 0; w < D / 4; ++w) {
+        int32_t vals[4];
+        oracle_unpack_int8_word(words[w], vals);
+        for (int lane = 0; lane < 4; ++lane)
+          dot += (double)qrow[4 * w + lane] * ((double)vals[lane] * sc);
+      }
     }
     s[n] = apply_softcap(scale * dot, a->softcap);
     keys[n].is_hot = 0;

@@ -438,6 +438,78 @@ def test_tiered_equals_dense_attention_over_logical_order():
             assert abs(a_lse[b * Hq + h] - lse) < 1e-12
 
 
+def _tiered_f16_from_dense(kc, vc, kh, vh, bs, hot_window, hot_start, rng=None):
+    """f16 cold rows [B, C, H, D] into pages [NB, bs, H, D]; hot rows into the
+    ring as in _tiered_from_dense."""
+    B, C, H, D = kc.shape
+    zc = np.zeros((B, C, H, D), np.int64)
+    zs = np.zeros((B, C, H), np.float16)
+    hk, hv, _, _, _, _, table = _tiered_from_dense(zc, zc, zs, zs, kh, vh, bs, hot_window,
+                                                   hot_start, rng=rng)
+    NB = table.size
+    pk = np.zeros((NB, bs, H, D), np.float16)
+    pv = np.zeros_like(pk)
+    for b in range(B):
+        for t in range(C):
+            pk[table[b, t // bs], t % bs] = kc[b, t]
+            pv[table[b, t // bs], t % bs] = vc[b, t]
+    return hk, hv, pk, pv, table
+
+
+def test_f16_tier_equals_int8_tier_on_integer_data_bitwise():
+    """Cold values that are integers in [-127, 127] are exact in f16: the f16
+    cold tier must give bit-identical results to the int8 tier with unit
+    scales holding the same integers (hot ring shared)."""
+    rng = np.random.default_rng(18)
+    B, Hq, H, D, bs, C, Hl, W = 2, 8, 2, 16, 8, 19, 5, 8
+    kc = rng.integers(-127, 128, size=(B, C, H, D))
+    vc = rng.integers(-127, 128, size=(B, C, H, D))
+    kh, vh = rand_dense(rng, B, Hl, H, D)
+    ones = np.ones((B, C, H), np.float16)
+    hk, hv, wk, wv, sk, sv, table = _tiered_from_dense(kc, vc, ones, ones, kh, vh, bs, W, C,
+                                                       rng=np.random.default_rng(3))
+    hk2, hv2, pk, pv, table2 = _tiered_f16_from_dense(kc.astype(np.float16),
+                                                      vc.astype(np.float16), kh, vh, bs, W, C,
+                                                      rng=np.random.default_rng(3))
+    q = (rng.standard_normal((B, Hq, D)) * 0.05).astype(np.float32)
+    a = oracle.decode_tiered(q, hk, hv, wk, wv, sk, sv, table, C, Hl, C, hot_window=W,
+                             softcap=30.0)
+    b_ = oracle.decode_tiered_f16(q, hk2, hv2, pk, pv, table2, C, Hl, C, hot_window=W,
+                                  softcap=30.0)
+    assert a[2] == 0 and b_[2] == 0
+    assert np.array_equal(a[0], b_[0]) and np.array_equal(a[1], b_[1])
+
+
+def test_f16_tier_equals_dense_attention_over_logical_order():
+    """f16 cold + hot keys against a dense f16 cache holding the cold rows
+    followed by the hot rows (positions contiguous), with window and softcap."""
+    rng = np.random.default_rng(19)
+    B, Hq, H, D, bs, C, Hl, W = 2, 4, 2, 16, 4, 13, 6, 8
+    kc, vc = rand_dense(rng, B, C, H, D)
+    kh, vh = rand_dense(rng, B, Hl, H, D)
+    hk, hv, pk, pv, table = _tiered_f16_from_dense(kc, vc, kh, vh, bs, W, C, rng=rng)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    a_out, a_lse, flags = oracle.decode_tiered_f16(q, hk, hv, pk, pv, table, C, Hl, C,
+                                                   hot_window=W, softcap=20.0, sliding_window=15)
+    assert flags == 0
+    from scipy.special import logsumexp
+    G = Hq // H
+    kd = np.concatenate([kc, kh], axis=1).astype(np.float64)
+    vd = np.concatenate([vc, vh], axis=1).astype(np.float64)
+    L = C + Hl
+    vis = np.arange(L) >= L - 15
+    scale = float(np.float32(1 / math.sqrt(D)))
+    for b in range(B):
+        for h in range(Hq):
+            s = kd[b, :, h // G] @ q[b, h].astype(np.float64) * scale
+            s = 20.0 * np.tanh(s / 20.0)
+            s = np.where(vis, s, -np.inf)
+            lse = logsumexp(s)
+            w = np.exp(s - lse)
+            np.testing.assert_allclose(a_out[b * Hq + h], w @ vd[b, :, h // G], atol=1e-12)
+            assert abs(a_lse[b * Hq + h] - lse) < 1e-12
+
+
 def test_hot_ring_rotation_invariance():
     """The same hot keys stored at a different ring phase (hot_start not a
     multiple of the window) give bit-identical results."""
