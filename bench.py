@@ -157,7 +157,8 @@ def describe(case):
                 "num_blocks": case.num_blocks, "seq_len_min": int(lens.min()),
                 "seq_len_max": int(lens.max()), "seq_len_mean": float(lens.mean()),
                 "sliding_window": case.sliding_window, "softcap": case.softcap}
-    return {"workload": case.name, "kind": "tiered int8 cold + f16 hot ring", "B": case.B,
+    kind = "tiered f16 cold + f16 hot ring" if case.cold_f16 else "tiered int8 cold + f16 hot ring"
+    return {"workload": case.name, "kind": kind, "B": case.B,
             "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D, "block_size": case.block_size,
             "cold_len": int(case.cold_lens[0]), "hot_len": int(case.hot_lens[0]),
             "hot_window": case.hot_window, "hot_start": int(case.hot_starts[0])}
@@ -194,16 +195,21 @@ def make_step(case, t):
         nbytes = qk.decode_attn_workspace_size(params)
         ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
 
+        tier = dict(hot_window=case.hot_window, cold_len=int(case.cold_lens[0]),
+                    hot_len=int(case.hot_lens[0]), hot_start=int(case.hot_starts[0]),
+                    q_pos=t["q_pos"], scale=case.scale, softcap=case.softcap,
+                    sliding_window=case.sliding_window, causal=case.causal,
+                    max_seq_len=case.max_seq_len, out=out, lse=lse, workspace=ws)
+
         def step(q=None, block_table=None, seq_lens=None):
-            return qk.decode_attn_tiered_int8(
-                t["q"] if q is None else q, t["k_hot"], t["v_hot"], t["k_cold"], t["v_cold"],
-                t["k_scale"], t["v_scale"],
-                t["block_table"] if block_table is None else block_table,
-                hot_window=case.hot_window, cold_len=int(case.cold_lens[0]),
-                hot_len=int(case.hot_lens[0]), hot_start=int(case.hot_starts[0]),
-                q_pos=t["q_pos"], scale=case.scale, softcap=case.softcap,
-                sliding_window=case.sliding_window, causal=case.causal,
-                max_seq_len=case.max_seq_len, out=out, lse=lse, workspace=ws)
+            q = t["q"] if q is None else q
+            block_table = t["block_table"] if block_table is None else block_table
+            if case.cold_f16:
+                return qk.decode_attn_tiered_f16(q, t["k_hot"], t["v_hot"], t["k_cold"],
+                                                 t["v_cold"], block_table, **tier)
+            return qk.decode_attn_tiered_int8(q, t["k_hot"], t["v_hot"], t["k_cold"],
+                                              t["v_cold"], t["k_scale"], t["v_scale"],
+                                              block_table, **tier)
     return step, out, lse
 
 
@@ -230,7 +236,8 @@ def oracle_sample(case, target_s, max_units=None):
             lo, hi = visible_range(L, L - 1, case.causal, case.sliding_window)
             return max(0, hi - lo) * case.D * 2 * 2 + G * case.D * 8
         cl, hl = int(case.cold_lens[b]), int(case.hot_lens[b])
-        return cl * (case.D * 2 + 4) + hl * case.D * 4 + G * case.D * 8
+        cold_row = case.D * 4 if case.cold_f16 else case.D * 2 + 4
+        return cl * cold_row + hl * case.D * 4 + G * case.D * 8
 
     def run(sel):
         rows = np.array([b * case.Hq + kv * G + g for (b, kv) in sel for g in range(G)])
@@ -241,6 +248,15 @@ def oracle_sample(case, target_s, max_units=None):
             oracle.decode_paged(case.q, kp, vp, case.block_table, case.seq_lens, case.q_pos,
                                 scale=case.scale, softcap=case.softcap,
                                 sliding_window=case.sliding_window, causal=case.causal, rows=rows)
+        elif case.cold_f16:
+            h = case.host_arrays(seqs)
+            t0 = time.perf_counter()
+            oracle.decode_tiered_f16(case.q, h["k_hot"], h["v_hot"], h["k_cold"], h["v_cold"],
+                                     case.block_table, case.cold_lens, case.hot_lens,
+                                     case.hot_starts, hot_window=case.hot_window,
+                                     q_pos=case.q_pos, scale=case.scale, softcap=case.softcap,
+                                     sliding_window=case.sliding_window, causal=case.causal,
+                                     rows=rows)
         else:
             h = case.host_arrays(seqs)
             t0 = time.perf_counter()
@@ -474,7 +490,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=["tiny", "paged", "tiered", "window", "longctx", "paged_compact"])
+                    choices=["tiny", "paged", "tiered", "window", "longctx", "paged_compact",
+                             "tiered_f16"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0,

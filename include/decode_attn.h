@@ -129,7 +129,7 @@ int decode_attn_paged(const da_params* p, const float* q, const uint16_t* k_pool
                       int32_t* dev_status, void* stream);
 
 /*
- * Tier geometry for decode_attn_tiered_int8.
+ * Tier geometry for decode_attn_tiered_int8 and decode_attn_tiered_f16.
  * Cold keys have absolute positions 0 .. cold_len-1 and are paged through
  * block_table (the f16 "coldPageTable" layout of doppler attention.js
  * executeAttentionTiered, applied to the int8 tier).  Hot key j
@@ -174,6 +174,25 @@ int decode_attn_tiered_int8(const da_params* p, const da_tier_params* t, const f
                             const int32_t* block_table, const int32_t* q_pos, float* out,
                             float* lse, void* workspace, size_t workspace_bytes,
                             int32_t* dev_status, void* stream);
+
+/*
+ * decode_attn_tiered_f16 — decode attention over an f16 cold tier and an f16
+ * hot ring: the f16 tiered layout of doppler attention.js
+ * executeAttentionTiered (cold tier paged through "coldPageTable", hot tier a
+ * ring), whose kernel body is not on the pages; it computes exactly what
+ * decode_attn_tiered_int8 computes with the cold values read as f16.
+ *   k_hot, v_hot   f16 [B, hot_capacity, Hkv, D]
+ *   k_cold, v_cold f16 [num_blocks, block_size, Hkv, D] (cold pages)
+ *   block_table    i32 [B, max_blocks_per_seq] (cold pages)
+ * Tier geometry, q_pos, masks, output, workspace and errors as for
+ * decode_attn_tiered_int8; p->head_dim may be 64, 128 or 256.
+ */
+int decode_attn_tiered_f16(const da_params* p, const da_tier_params* t, const float* q,
+                           const uint16_t* k_hot, const uint16_t* v_hot,
+                           const uint16_t* k_cold, const uint16_t* v_cold,
+                           const int32_t* block_table, const int32_t* q_pos, float* out,
+                           float* lse, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream);
 
 /*
  * decode_attn_split_partial — first half of flash-decoding: split s covers

@@ -1,4 +1,4 @@
-"""GB300 decode attention over a paged / int8-tiered KV cache.
+"""GB300 decode attention over a paged / tiered (int8 or f16 cold tier) KV cache.
 
 Thin Python binding of ``libdecode_attn.so`` (C ABI in ``include/decode_attn.h``).
 The functions below only marshal torch tensors into the C calls: every step
@@ -22,7 +22,8 @@ from . import _build
 
 __all__ = [
     "load_library", "library_path", "build",
-    "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_split_partial",
+    "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
+    "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_status_string",
     "decode_attn_paged_static_ws", "DecodeAttnError", "DEV_BAD_BLOCK", "DEV_BAD_SEQ_LEN",
     "DEV_BAD_QPOS", "DEV_SPLIT_OVERFLOW", "DEV_BAD_TIER", "DEV_TIMEOUT",
@@ -42,7 +43,8 @@ DA_ERR_WORKSPACE = -3
 DA_ERR_CUDA = -4
 
 _EXPORTS = (
-    "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_split_partial",
+    "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
+    "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_workspace_init",
     "decode_attn_status_string", "decode_attn_paged_static_ws",
 )
@@ -109,6 +111,10 @@ def load_library():
         lib.decode_attn_tiered_int8.argtypes = [ctypes.POINTER(DaParams),
                                                 ctypes.POINTER(DaTierParams), P, P, P, P, P, P,
                                                 P, P, P, P, P, P, ctypes.c_size_t, P, P]
+        lib.decode_attn_tiered_f16.restype = ctypes.c_int
+        lib.decode_attn_tiered_f16.argtypes = [ctypes.POINTER(DaParams),
+                                               ctypes.POINTER(DaTierParams), P, P, P, P, P, P,
+                                               P, P, P, P, ctypes.c_size_t, P, P]
         lib.decode_attn_split_partial.restype = ctypes.c_int
         lib.decode_attn_split_partial.argtypes = [ctypes.POINTER(DaParams), i32, i32, P, P, P,
                                                   P, P, P, P, P, P, P]
@@ -331,6 +337,51 @@ def decode_attn_tiered_int8(q, k_hot, v_hot, k_cold, v_cold, k_scale, v_scale, b
                                      _ptr(out), _ptr(lse), ws_ptr, ws_bytes, _ptr(dev_status),
                                      _stream(dev, stream))
     _check("decode_attn_tiered_int8", st)
+    return out, lse
+
+
+def decode_attn_tiered_f16(q, k_hot, v_hot, k_cold, v_cold, block_table, *, hot_window,
+                           cold_len=0, hot_len=0, hot_start=0, cold_lens=None, hot_lens=None,
+                           hot_starts=None, q_pos=None, scale=0.0, softcap=0.0,
+                           sliding_window=0, causal=True, max_seq_len=0, out=None, lse=None,
+                           workspace="auto", dev_status=None, stream=None):
+    """Decode attention over an f16 cold tier (paged) and an f16 hot ring.
+
+    k_hot/v_hot f16 [B, hot_capacity, Hkv, D]; k_cold/v_cold f16 [NB, bs, Hkv, D].
+    Tier arguments as for decode_attn_tiered_int8.  Returns (out, lse)."""
+    torch = _torch()
+    lib = load_library()
+    dev = q.device
+    _req(q, "q", torch.float32, dev, 3)
+    _req(k_hot, "k_hot", torch.float16, dev, 4)
+    _req(v_hot, "v_hot", torch.float16, dev, 4)
+    _req(k_cold, "k_cold", torch.float16, dev, 4)
+    _req(v_cold, "v_cold", torch.float16, dev, 4)
+    _req(block_table, "block_table", torch.int32, dev, 2)
+    for name, t in (("cold_lens", cold_lens), ("hot_lens", hot_lens), ("hot_starts", hot_starts),
+                    ("q_pos", q_pos)):
+        if t is not None:
+            _req(t, name, torch.int32, dev, 1)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cold.shape
+    cap = k_hot.shape[1]
+    if (D2 != D or v_cold.shape != k_cold.shape or k_hot.shape != (B, cap, Hkv, D)
+            or v_hot.shape != k_hot.shape):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    params = make_params(q, bs, Hkv, block_table.shape[1], NB, scale=scale, softcap=softcap,
+                         sliding_window=sliding_window, causal=causal, max_seq_len=max_seq_len)
+    tier = DaTierParams(int(hot_window), int(cap), int(cold_len), int(hot_len), int(hot_start),
+                        _ptr(cold_lens), _ptr(hot_lens), _ptr(hot_starts))
+    ws_ptr, ws_bytes = _workspace_args(workspace, params, dev)
+    st = lib.decode_attn_tiered_f16(ctypes.byref(params), ctypes.byref(tier), _ptr(q),
+                                    _ptr(k_hot), _ptr(v_hot), _ptr(k_cold), _ptr(v_cold),
+                                    _ptr(block_table), _ptr(q_pos), _ptr(out), _ptr(lse), ws_ptr,
+                                    ws_bytes, _ptr(dev_status), _stream(dev, stream))
+    _check("decode_attn_tiered_f16", st)
     return out, lse
 
 

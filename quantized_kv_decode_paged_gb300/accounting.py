@@ -1,7 +1,7 @@
 """Algorithmic byte counts of one decode step (the roofline numerator).
 
 Counts what the method must move: the visible K/V rows (int8 words plus
-their scales for the cold tier), the block-table entries of the pages those
+their scales, or f16 rows, for the cold tier), the block-table entries of the pages those
 rows sit in, Q, out, lse and the length arrays.  Masked pages, unused pool
 pages and split-KV partials are not counted.
 """
@@ -43,7 +43,8 @@ def algorithmic_bytes(case) -> dict:
         qp = int(case.q_pos[b]) if case.q_pos is not None else (hs + hl - 1 if hl > 0 else cl - 1)
         lo, hi = visible_range(cl, qp, case.causal, case.sliding_window)
         nc = max(0, hi - lo)
-        kv += nc * case.Hkv * (case.D * 2 + 2 * 2)
+        # int8 cold: D bytes of K and of V plus two f16 scales; f16 cold: 2D + 2D
+        kv += nc * case.Hkv * (case.D * 2 * 2 if case.cold_f16 else case.D * 2 + 2 * 2)
         if nc:
             bt += ((hi - 1) // case.block_size - lo // case.block_size + 1) * 4
         for j in range(hl):

@@ -162,15 +162,15 @@ void fill_common(KParams& k, const da_params* p) {
 int encode_pool_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
                     long long D, long long heads, long long rows, int box_rows, int kvb);
 
-// K/V pool maps of a paged (f16) or cold (int8) cache for the chosen KVB.
+// K/V pool maps of a paged / cold cache (f16, or int8 words) for the chosen KVB.
 int encode_paged_maps(KParams& k, int kind, const void* kp, const void* vp, const da_params* p) {
   const da::GeoInfo g = da::decode_geo(kind, p->head_dim, k.KVB);
   if (g.W == 0) return DA_ERR_UNSUPPORTED;
   const int box_rows = p->block_size < g.TOK ? p->block_size : g.TOK;
   const long long rows = (long long)p->num_blocks * p->block_size;
   const CUtensorMapDataType dt =
-      kind == da::KIND_PAGED ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  const int esize = kind == da::KIND_PAGED ? 2 : 1;
+      da::cold_int8(kind) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const int esize = da::cold_int8(kind) ? 1 : 2;
   int st = encode_pool_map(&k.tm_k, kp, dt, esize, p->head_dim, p->num_kv_heads, rows, box_rows,
                            k.KVB);
   if (st != DA_OK) return st;
@@ -264,9 +264,12 @@ WsLayout ws_layout(int grid, int D, int kvb) {
 // kv heads per unit the workspace must serve (either cache kind).
 int ws_kvb(const da_params* p) {
   const int D = p->head_dim, H = p->num_kv_heads;
-  const int a = kvb_override(da::KIND_PAGED, D, H, da::decode_kvb(da::KIND_PAGED, D, H));
-  const int b = kvb_override(da::KIND_TIERED, D, H, da::decode_kvb(da::KIND_TIERED, D, H));
-  return a > b ? a : b;
+  int m = 0;
+  for (int kind : {da::KIND_PAGED, da::KIND_TIERED, da::KIND_TIERED_F16}) {
+    const int v = kvb_override(kind, D, H, da::decode_kvb(kind, D, H));
+    m = v > m ? v : m;
+  }
+  return m;
 }
 
 struct Launch {
@@ -330,6 +333,81 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
     if (e != cudaSuccess) return DA_ERR_CUDA;
   }
   return DA_OK;
+}
+
+// Both tiered caches: int8 cold words with scales (KIND_TIERED) or f16 cold
+// rows (KIND_TIERED_F16, k_scale = v_scale = NULL).
+int tiered_impl(int kind, const da_params* p, const da_tier_params* t, const float* q,
+                const uint16_t* k_hot, const uint16_t* v_hot, const void* k_cold,
+                const void* v_cold, const uint16_t* k_scale, const uint16_t* v_scale,
+                const int32_t* block_table, const int32_t* q_pos, float* out, float* lse,
+                void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  const bool i8 = da::cold_int8(kind);
+  int st = check_params(p, i8);
+  if (st != DA_OK) return st;
+  if (!t || !q || !k_hot || !v_hot || !k_cold || !v_cold || (i8 && (!k_scale || !v_scale)) ||
+      !block_table || !out)
+    return DA_ERR_INVALID;
+  if (!workspace && workspace_bytes) return DA_ERR_INVALID;
+  if (t->hot_window < 0 || t->hot_capacity < 1 || t->hot_capacity < t->hot_window)
+    return DA_ERR_INVALID;
+  if (!t->cold_lens && t->cold_len < 0) return DA_ERR_INVALID;
+  if (!t->hot_starts && t->hot_start < 0) return DA_ERR_INVALID;
+  if (!t->hot_lens) {
+    const int limit = t->hot_window > 0 ? t->hot_window : t->hot_capacity;
+    if (t->hot_len < 0 || t->hot_len > limit) return DA_ERR_INVALID;
+  }
+  if (!t->cold_lens && (long long)t->cold_len > (long long)p->max_blocks_per_seq * p->block_size)
+    return DA_ERR_INVALID;
+  if (((long long)p->block_size * p->num_kv_heads * 2) % 16 != 0) return DA_ERR_UNSUPPORTED;
+  if ((long long)t->hot_capacity * p->batch > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_hot, 16) || !aligned(v_hot, 16) || !aligned(k_cold, 16) ||
+      !aligned(v_cold, 16) || (i8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))) ||
+      !aligned(out, 16) || !aligned(block_table, 4) || (q_pos && !aligned(q_pos, 4)) ||
+      (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
+    return DA_ERR_INVALID;
+  if (p->batch == 0) return DA_OK;
+  KParams k;
+  memset(&k, 0, sizeof(k));
+  fill_common(k, p);
+  k.KVB = kvb_override(kind, p->head_dim, p->num_kv_heads,
+                       da::decode_kvb(kind, p->head_dim, p->num_kv_heads));
+  st = encode_paged_maps(k, kind, k_cold, v_cold, p);
+  if (st != DA_OK) return st;
+  {
+    const da::GeoInfo g = da::decode_geo(kind, k.D, k.KVB);
+    if (g.W == 0) return DA_ERR_UNSUPPORTED;
+    st = encode_ring_map(&k.tm_kh, k_hot, p->head_dim, p->num_kv_heads, t->hot_capacity,
+                         p->batch, g.TOKH, k.KVB);
+    if (st != DA_OK) return st;
+    st = encode_ring_map(&k.tm_vh, v_hot, p->head_dim, p->num_kv_heads, t->hot_capacity,
+                         p->batch, g.TOKH, k.KVB);
+    if (st != DA_OK) return st;
+  }
+  k.dev_status = dev_status;
+  k.k_scale = k_scale;
+  k.v_scale = v_scale;
+  k.hot_window = t->hot_window;
+  k.hot_cap = t->hot_capacity;
+  k.cold_len = t->cold_len;
+  k.hot_len = t->hot_len;
+  k.hot_start = t->hot_start;
+  Launch lc{kind, p, workspace, workspace_bytes};
+  const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
+  // The hot-ring tensor map spans the whole batch; a chunk keeps the global
+  // sequence index through `hot_b0`, so the ring map is not re-encoded.
+  auto off = [&](KParams& kk, int b0) {
+    kk.q = q + (long long)b0 * Hq * D;
+    kk.block_table = block_table + (long long)b0 * mb;
+    kk.q_pos = q_pos ? q_pos + b0 : nullptr;
+    kk.out = out + (long long)b0 * Hq * D;
+    kk.lse = lse ? lse + (long long)b0 * Hq : nullptr;
+    kk.cold_lens = t->cold_lens ? t->cold_lens + b0 : nullptr;
+    kk.hot_lens = t->hot_lens ? t->hot_lens + b0 : nullptr;
+    kk.hot_starts = t->hot_starts ? t->hot_starts + b0 : nullptr;
+    kk.hot_b0 = b0;
+  };
+  return run_batched(k, lc, off, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -472,71 +550,19 @@ int decode_attn_tiered_int8(const da_params* p, const da_tier_params* t, const f
                             const int32_t* block_table, const int32_t* q_pos, float* out,
                             float* lse, void* workspace, size_t workspace_bytes,
                             int32_t* dev_status, void* stream) {
-  int st = check_params(p, true);
-  if (st != DA_OK) return st;
-  if (!t || !q || !k_hot || !v_hot || !k_cold || !v_cold || !k_scale || !v_scale ||
-      !block_table || !out)
-    return DA_ERR_INVALID;
-  if (!workspace && workspace_bytes) return DA_ERR_INVALID;
-  if (t->hot_window < 0 || t->hot_capacity < 1 || t->hot_capacity < t->hot_window)
-    return DA_ERR_INVALID;
-  if (!t->cold_lens && t->cold_len < 0) return DA_ERR_INVALID;
-  if (!t->hot_starts && t->hot_start < 0) return DA_ERR_INVALID;
-  if (!t->hot_lens) {
-    const int limit = t->hot_window > 0 ? t->hot_window : t->hot_capacity;
-    if (t->hot_len < 0 || t->hot_len > limit) return DA_ERR_INVALID;
-  }
-  if (!t->cold_lens && (long long)t->cold_len > (long long)p->max_blocks_per_seq * p->block_size)
-    return DA_ERR_INVALID;
-  if (((long long)p->block_size * p->num_kv_heads * 2) % 16 != 0) return DA_ERR_UNSUPPORTED;
-  if ((long long)t->hot_capacity * p->batch > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
-  if (!aligned(q, 16) || !aligned(k_hot, 16) || !aligned(v_hot, 16) || !aligned(k_cold, 16) ||
-      !aligned(v_cold, 16) || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
-      !aligned(out, 16) || !aligned(block_table, 4) || (q_pos && !aligned(q_pos, 4)) ||
-      (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
-    return DA_ERR_INVALID;
-  if (p->batch == 0) return DA_OK;
-  KParams k;
-  memset(&k, 0, sizeof(k));
-  fill_common(k, p);
-  k.KVB = kvb_override(da::KIND_TIERED, p->head_dim, p->num_kv_heads,
-                       da::decode_kvb(da::KIND_TIERED, p->head_dim, p->num_kv_heads));
-  st = encode_paged_maps(k, da::KIND_TIERED, k_cold, v_cold, p);
-  if (st != DA_OK) return st;
-  {
-    const da::GeoInfo g = da::decode_geo(da::KIND_TIERED, k.D, k.KVB);
-    if (g.W == 0) return DA_ERR_UNSUPPORTED;
-    st = encode_ring_map(&k.tm_kh, k_hot, p->head_dim, p->num_kv_heads, t->hot_capacity,
-                         p->batch, g.TOKH, k.KVB);
-    if (st != DA_OK) return st;
-    st = encode_ring_map(&k.tm_vh, v_hot, p->head_dim, p->num_kv_heads, t->hot_capacity,
-                         p->batch, g.TOKH, k.KVB);
-    if (st != DA_OK) return st;
-  }
-  k.dev_status = dev_status;
-  k.k_scale = k_scale;
-  k.v_scale = v_scale;
-  k.hot_window = t->hot_window;
-  k.hot_cap = t->hot_capacity;
-  k.cold_len = t->cold_len;
-  k.hot_len = t->hot_len;
-  k.hot_start = t->hot_start;
-  Launch lc{da::KIND_TIERED, p, workspace, workspace_bytes};
-  const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
-  // The hot-ring tensor map spans the whole batch; a chunk keeps the global
-  // sequence index through `hot_b0`, so the ring map is not re-encoded.
-  auto off = [&](KParams& kk, int b0) {
-    kk.q = q + (long long)b0 * Hq * D;
-    kk.block_table = block_table + (long long)b0 * mb;
-    kk.q_pos = q_pos ? q_pos + b0 : nullptr;
-    kk.out = out + (long long)b0 * Hq * D;
-    kk.lse = lse ? lse + (long long)b0 * Hq : nullptr;
-    kk.cold_lens = t->cold_lens ? t->cold_lens + b0 : nullptr;
-    kk.hot_lens = t->hot_lens ? t->hot_lens + b0 : nullptr;
-    kk.hot_starts = t->hot_starts ? t->hot_starts + b0 : nullptr;
-    kk.hot_b0 = b0;
-  };
-  return run_batched(k, lc, off, static_cast<cudaStream_t>(stream));
+  return tiered_impl(da::KIND_TIERED, p, t, q, k_hot, v_hot, k_cold, v_cold, k_scale, v_scale,
+                     block_table, q_pos, out, lse, workspace, workspace_bytes, dev_status, stream);
+}
+
+int decode_attn_tiered_f16(const da_params* p, const da_tier_params* t, const float* q,
+                           const uint16_t* k_hot, const uint16_t* v_hot,
+                           const uint16_t* k_cold, const uint16_t* v_cold,
+                           const int32_t* block_table, const int32_t* q_pos, float* out,
+                           float* lse, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream) {
+  return tiered_impl(da::KIND_TIERED_F16, p, t, q, k_hot, v_hot, k_cold, v_cold, nullptr,
+                     nullptr, block_table, q_pos, out, lse, workspace, workspace_bytes,
+                     dev_status, stream);
 }
 
 }  // extern "C"

@@ -430,7 +430,7 @@ __device__ __forceinline__ int stream_slot(int c, int c0, long long g0, long lon
 // Absolute tile of unit-local tile i (tiered: hot tiles follow cold ones).
 template <int KIND>
 __device__ __forceinline__ int tile_of(const SeqPlan& e, int i, bool& is_hot) {
-  if (KIND == KIND_TIERED && i >= e.ncold) {
+  if (is_tiered(KIND) && i >= e.ncold) {
     is_hot = true;
     const int hi_ = i - e.ncold;
     const int na = e.ha1 - e.ha0;
@@ -456,13 +456,13 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
                                               const BoxGeo& bg, uint64_t* full, uint64_t* empty,
                                               uint64_t* qfull, uint64_t* qempty, Misc* misc) {
   using Gm = Geo<KIND, D, KVB>;
-  constexpr int OPS = (KIND == KIND_PAGED) ? 2 : 4;  // copies per page: K, V (+ 2 scale slabs)
+  constexpr int OPS = cold_int8(KIND) ? 4 : 2;  // copies per page: K, V (+ 2 scale slabs)
   const int lane = threadIdx.x & 31;
   const int nstages = p.stages;
   const int bs = p.bs, log2_bs = p.log2_bs, max_blocks = p.max_blocks, nblocks = p.num_blocks;
   const int Hkv = p.Hkv;
   const uint32_t page_bytes =
-      (uint32_t)(2 * bg.box_bytes + (KIND == KIND_TIERED ? 2 * bg.R * Hkv * 2 : 0));
+      (uint32_t)(2 * bg.box_bytes + (cold_int8(KIND) ? 2 * bg.R * Hkv * 2 : 0));
   SegIter it;
   seg_init<KIND>(p, plan, pre, it);
   Seg s;
@@ -536,7 +536,7 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
         const int vn = __shfl_sync(0xffffffffu, bt_nxt, idx & 31);
         const int pg = p_first + lane;
         const int blk = (lane < bg.npg && pg < max_blocks) ? (idx < 32 ? vc : vn) : -1;
-        const int vhi_keys = (KIND == KIND_TIERED) ? min(s.vhi, e.cold_len) : s.vhi;
+        const int vhi_keys = is_tiered(KIND) ? min(s.vhi, e.cold_len) : s.vhi;
         const int r0 = tok0 + lane * bg.R;
         const bool needed = lane < bg.npg && (r0 < vhi_keys) && (r0 + bg.R > s.vlo);
         const bool ok = needed && blk >= 0 && blk < nblocks;
@@ -560,7 +560,7 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
             if (r < 2) {
               uint8_t* dst = st + (r ? L.off_v : L.off_k) + j * bg.box_bytes;
               tma_load_4d(dst, r ? &p.tm_v : &p.tm_k, &full[stage], 0, row, 0, kv0);
-            } else if constexpr (KIND == KIND_TIERED) {
+            } else if constexpr (cold_int8(KIND)) {
               // the box's rows of the page's [rows, Hkv] f16 scale slab
               const int isv = r - 2;
               const uint16_t* src = (isv ? p.v_scale : p.k_scale) + (long long)row * Hkv;
@@ -569,7 +569,7 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
             }
           }
         }
-      } else if constexpr (KIND == KIND_TIERED) {
+      } else if constexpr (is_tiered(KIND)) {
         // ----- hot ring tile: slots [at*TOKH, at*TOKH + TOKH) of sequence b
         if (lane == 0) {
           *reinterpret_cast<volatile uint32_t*>(hdrs + stage * 16) = 0u;
@@ -1236,7 +1236,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
     a.m[0] = a.m[1] = kNegInf;
     a.l[0] = a.l[1] = 0.f;
     HotView hv;
-    if constexpr (KIND == KIND_TIERED) {
+    if constexpr (is_tiered(KIND)) {
       hv.W = p.hot_window;
       hv.cap_eff = p.hot_window > 0 ? p.hot_window : p.hot_cap;
       hv.hs_mod = p.hot_window > 0 ? e.hot_start % p.hot_window : 0;
@@ -1245,7 +1245,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
       hv.j0 = j0 > 0 ? j0 : 0;
       hv.j1 = j1 < e.hot_len ? j1 : e.hot_len;
     }
-    const int vhc = (KIND == KIND_TIERED) ? min(s.vhi, e.cold_len) : s.vhi;
+    const int vhc = is_tiered(KIND) ? min(s.vhi, e.cold_len) : s.vhi;
 
     for (int i = s.i0; i < s.i1; ++i) {
       if (!mbar_wait(&full[stage], round & 1, abort_flag(misc), p.wait_ns) && lane == 0) note_abort(misc);
@@ -1276,6 +1276,15 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
             if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
             group_compute<TK_PAGED, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB);
           }
+        } else if constexpr (KIND == KIND_TIERED_F16) {
+          // f16 cold rows, read like hot-ring rows (the tiered d order)
+          static_assert(Gm::GPW == 1, "one key group per warp in an f16 tile");
+          const int k0 = 16 * tg;
+          const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
+          if (__any_sync(0xffffffffu, vA || vB)) {
+            if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
+            group_compute<TK_HOT, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB);
+          }
         } else {
           // both key groups of the warp in one softmax step (int8 values are
           // always finite, so masked keys need only a zero weight)
@@ -1295,7 +1304,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
             groups_compute<TK_COLD, D, PK, 2>(km, vm, softcap2, k0, lane, q, a, v, ks, vs);
           }
         }
-      } else if constexpr (KIND == KIND_TIERED) {
+      } else if constexpr (is_tiered(KIND)) {
         RowMap km, vm;
         km.log2R = 31 - __clz(Gm::TOKH);
         km.box_bytes = 0;
@@ -1373,7 +1382,7 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
   if (warp == NCW && (tid & 31) == 0) {
     prefetch_tensormap(&p.tm_k);
     prefetch_tensormap(&p.tm_v);
-    if (KIND == KIND_TIERED) {
+    if (is_tiered(KIND)) {
       prefetch_tensormap(&p.tm_kh);
       prefetch_tensormap(&p.tm_vh);
     }

@@ -14,7 +14,11 @@ constexpr int kMaxBatchPerLaunch = 256;  // per-sequence plan lives in shared me
 constexpr int kSmemLimit = 232448;       // 227 KB opt-in per block on sm_100-class parts
 constexpr uint32_t kRedBarrier = 1;      // named barrier id for the consumer warps
 
-enum Kind : int { KIND_PAGED = 0, KIND_TIERED = 1 };
+// PAGED: f16 pages.  TIERED: int8 cold pages (+ f16 scales) and an f16 hot
+// ring.  TIERED_F16: f16 cold pages and an f16 hot ring.
+enum Kind : int { KIND_PAGED = 0, KIND_TIERED = 1, KIND_TIERED_F16 = 2 };
+__host__ __device__ constexpr bool is_tiered(int kind) { return kind != KIND_PAGED; }
+__host__ __device__ constexpr bool cold_int8(int kind) { return kind == KIND_TIERED; }
 // STREAM: every CTA takes an equal share of the concatenated key tiles of all
 //         units; units cut between CTAs are merged by the last CTA to finish.
 // UNITS:  every CTA takes whole units (no workspace needed).
@@ -45,11 +49,11 @@ template <int KIND, int D, int KVB>
 struct Geo {
   static constexpr int W = (D >= 256) ? 4 : 8;
   static constexpr int TG = W / KVB;
-  static constexpr int ESZ = (KIND == KIND_PAGED) ? 2 : 1;  // bytes of a paged / cold element
+  static constexpr int ESZ = cold_int8(KIND) ? 1 : 2;  // bytes of a paged / cold element
   static constexpr int ROWB = D * ESZ;                        // bytes of one (token, head) row
   static constexpr int CHN = ROWB / 128;                      // 128-byte slices of such a row
   static constexpr int CHH = D * 2 / 128;                     // slices of an f16 hot row
-  static constexpr int GPW = (KIND == KIND_PAGED) ? 1 : 2;    // key groups per warp, cold tile
+  static constexpr int GPW = cold_int8(KIND) ? 2 : 1;    // key groups per warp, paged/cold tile
   static constexpr int TOK = 16 * TG * GPW;                   // keys per paged / cold tile
   static constexpr int TOKH = 16 * TG;                        // keys per hot-ring tile
   static constexpr int REGION = 32 * W * D;                   // K (or V) bytes of a stage
@@ -158,7 +162,7 @@ __host__ __device__ inline SmemLayout make_layout(int kind, int D, int KVB, int 
   L.off_k = 0;
   L.off_v = region;
   L.off_sc = 2 * region;
-  const int sc_bytes = (kind == KIND_TIERED) ? align_up(2 * tok * Hkv * 2, 128) : 0;
+  const int sc_bytes = cold_int8(kind) ? align_up(2 * tok * Hkv * 2, 128) : 0;
   L.stage_bytes = align_up(L.off_sc + sc_bytes, 1024);
   L.off_stages = 0;
   int off = stages * L.stage_bytes;
@@ -170,7 +174,7 @@ __host__ __device__ inline SmemLayout make_layout(int kind, int D, int KVB, int 
   L.off_red = off;
   off += (W / 2) * red_floats(D) * 4;
   L.off_plan = off;
-  off += B * (kind == KIND_TIERED ? (int)sizeof(SeqPlan) : (int)sizeof(SeqPlanPaged));
+  off += B * (is_tiered(kind) ? (int)sizeof(SeqPlan) : (int)sizeof(SeqPlanPaged));
   L.off_pre = off;
   off += (B + 1) * 4;
   off = align_up(off, 8);

@@ -11,7 +11,7 @@ namespace da {
 // Hkv kv heads: enough that one token row of the block is >= 512
 // contiguous bytes, and a divisor of Hkv.
 inline int decode_kvb(int kind, int D, int Hkv) {
-  int pref = (kind == KIND_PAGED) ? (D == 64 ? 4 : D == 128 ? 2 : 1) : (D == 128 ? 4 : 2);
+  int pref = cold_int8(kind) ? (D == 128 ? 4 : 2) : (D == 64 ? 4 : D == 128 ? 2 : 1);
   while (pref > 1 && Hkv % pref != 0) pref /= 2;
   return pref;
 }

@@ -19,6 +19,7 @@ Workloads (the shapes of the pages' serving cases):
                 1% of keys scaled by 8
 * ``longctx``   B=128, Hq=64, Hkv=8, D=128, L ~ lognormal(median 8192, sigma 0.8)
                 clamped to [128, 32768], bs=16, pool exactly filled and shuffled
+* ``tiered_f16`` the ``tiered`` shape with the 7168 cold keys kept as f16 rows
 """
 from __future__ import annotations
 
@@ -34,7 +35,7 @@ import numpy as np
 _S_K, _S_V, _S_OUTLIER, _S_Q, _S_META = 0, 1, 2, 3, 4
 _GLOBAL = 1 << 30  # "sequence" index used for batch-wide draws
 
-WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx")
+WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx", "tiered_f16")
 # Same keys and values as "paged", in a pool holding exactly the used pages
 # (about 310 MB instead of 4 GiB of device memory): for profiler captures.
 VARIANTS = ("paged_compact",)
@@ -213,6 +214,10 @@ def workload(name: str):
     if name == "tiered":
         return make_tiered("tiered", 2, B=16, Hq=32, Hkv=8, D=128, block_size=16,
                            cold_len=7168, hot_len=1024, hot_window=1024, hot_start=7168)
+    if name == "tiered_f16":
+        return make_tiered("tiered_f16", 2, B=16, Hq=32, Hkv=8, D=128, block_size=16,
+                           cold_len=7168, hot_len=1024, hot_window=1024, hot_start=7168,
+                           cold_f16=True)
     if name == "window":
         return make_paged("window", 3, B=64, Hq=16, Hkv=8, D=256, block_size=32,
                           seq_lens=[8192] * 64, num_blocks=64 * 256, max_blocks=256,
@@ -279,6 +284,7 @@ class TieredCase:
     q_pos: Optional[np.ndarray] = None
     pages_per_seq: Optional[np.ndarray] = None
     uniform: bool = True     # every sequence has the same tier lengths
+    cold_f16: bool = False   # cold tier as f16 rows instead of int8 words + scales
 
     @property
     def max_blocks(self) -> int:
@@ -300,9 +306,12 @@ class TieredCase:
 
     def seq_encoded(self, b: int):
         kc, vc, kh, vh = self.seq_source(b)
+        n = int(self.pages_per_seq[b])
+        if self.cold_f16:
+            shp = (n, self.block_size, self.Hkv, self.D)
+            return kc.reshape(shp), vc.reshape(shp), None, None, kh, vh
         kq, ks = quantize_int8_rows(kc)
         vq, vs = quantize_int8_rows(vc)
-        n = int(self.pages_per_seq[b])
         shp = (n, self.block_size, self.Hkv)
         return (pack_int8_words(kq).reshape(shp + (self.D // 4,)),
                 pack_int8_words(vq).reshape(shp + (self.D // 4,)),
@@ -314,12 +323,15 @@ class TieredCase:
         return (hs + j) % self.hot_window if self.hot_window > 0 else j
 
     def host_arrays(self, seqs=None):
-        """Host buffers: k_hot, v_hot, k_cold, v_cold, k_scale, v_scale (zeros
-        except the data of ``seqs``; default all)."""
+        """Host buffers: k_hot, v_hot, k_cold, v_cold and (int8 cold tier)
+        k_scale, v_scale; zeros except the data of ``seqs`` (default all)."""
         cap, H, D = self.hot_capacity, self.Hkv, self.D
         k_hot = np.zeros((self.B, cap, H, D), dtype=np.float16)
         v_hot = np.zeros_like(k_hot)
-        k_cold = np.zeros((self.num_blocks, self.block_size, H, D // 4), dtype=np.uint32)
+        if self.cold_f16:
+            k_cold = np.zeros((self.num_blocks, self.block_size, H, D), dtype=np.float16)
+        else:
+            k_cold = np.zeros((self.num_blocks, self.block_size, H, D // 4), dtype=np.uint32)
         v_cold = np.zeros_like(k_cold)
         k_scale = np.zeros((self.num_blocks, self.block_size, H), dtype=np.float16)
         v_scale = np.zeros_like(k_scale)
@@ -330,19 +342,23 @@ class TieredCase:
                 pages = self.block_table[b, :int(self.pages_per_seq[b])].astype(np.int64)
                 ok = (pages >= 0) & (pages < self.num_blocks)  # a corrupted entry holds no data
                 k_cold[pages[ok]], v_cold[pages[ok]] = kw[ok], vw[ok]
-                k_scale[pages[ok]], v_scale[pages[ok]] = ks[ok], vs[ok]
+                if not self.cold_f16:
+                    k_scale[pages[ok]], v_scale[pages[ok]] = ks[ok], vs[ok]
                 slots = self._hot_slots(b)
                 k_hot[b, slots] = kh
                 v_hot[b, slots] = vh
-        return dict(k_hot=k_hot, v_hot=v_hot, k_cold=k_cold, v_cold=v_cold,
-                    k_scale=k_scale, v_scale=v_scale)
+        out = dict(k_hot=k_hot, v_hot=v_hot, k_cold=k_cold, v_cold=v_cold)
+        if not self.cold_f16:
+            out.update(k_scale=k_scale, v_scale=v_scale)
+        return out
 
     def device_tensors(self, device="cuda"):
         import torch
 
         h = self.host_arrays()
-        for k in ("k_cold", "v_cold"):
-            h[k] = h[k].view(np.int32)  # the same 32-bit words, as a torch-friendly dtype
+        if not self.cold_f16:
+            for k in ("k_cold", "v_cold"):
+                h[k] = h[k].view(np.int32)  # the same 32-bit words, as a torch-friendly dtype
         t = {k: torch.from_numpy(v).to(device) for k, v in h.items()}
         t["q"] = torch.from_numpy(self.q).to(device)
         t["block_table"] = torch.from_numpy(self.block_table).to(device)
@@ -354,7 +370,8 @@ class TieredCase:
 
 def make_tiered(name, seed, B, Hq, Hkv, D, block_size, cold_len, hot_len, hot_window,
                 hot_start, hot_capacity=None, scale=0.0, softcap=0.0, sliding_window=0,
-                causal=True, q_pos=None, num_blocks=None, max_blocks=None) -> TieredCase:
+                causal=True, q_pos=None, num_blocks=None, max_blocks=None,
+                cold_f16=False) -> TieredCase:
     cold_lens = np.broadcast_to(np.asarray(cold_len, dtype=np.int32), (B,)).copy()
     hot_lens = np.broadcast_to(np.asarray(hot_len, dtype=np.int32), (B,)).copy()
     hot_starts = np.broadcast_to(np.asarray(hot_start, dtype=np.int32), (B,)).copy()
@@ -377,4 +394,4 @@ def make_tiered(name, seed, B, Hq, Hkv, D, block_size, cold_len, hot_len, hot_wi
                       scale=scale, softcap=softcap, sliding_window=sliding_window,
                       causal=causal, q_pos=None if q_pos is None else
                       np.asarray(q_pos, dtype=np.int32).reshape(B),
-                      pages_per_seq=pages, uniform=uniform)
+                      pages_per_seq=pages, uniform=uniform, cold_f16=bool(cold_f16))

@@ -61,6 +61,13 @@ def run_paged(case, t, mode, split_tokens=256, dev_status=None):
 def oracle_tiered(case, rows=None):
     seqs = None if rows is None else sorted({int(r) // case.Hq for r in rows})
     h = case.host_arrays(seqs)
+    if case.cold_f16:
+        return oracle.decode_tiered_f16(case.q, h["k_hot"], h["v_hot"], h["k_cold"], h["v_cold"],
+                                        case.block_table, case.cold_lens, case.hot_lens,
+                                        case.hot_starts, hot_window=case.hot_window,
+                                        q_pos=case.q_pos, scale=case.scale, softcap=case.softcap,
+                                        sliding_window=case.sliding_window, causal=case.causal,
+                                        rows=rows)
     return oracle.decode_tiered(case.q, h["k_hot"], h["v_hot"], h["k_cold"], h["v_cold"],
                                 h["k_scale"], h["v_scale"], case.block_table, case.cold_lens,
                                 case.hot_lens, case.hot_starts, hot_window=case.hot_window,
@@ -81,9 +88,15 @@ def run_tiered(case, t, mode, per_seq=None, dev_status=None):
     else:
         kw.update(cold_len=int(case.cold_lens[0]), hot_len=int(case.hot_lens[0]),
                   hot_start=int(case.hot_starts[0]))
-    out, lse = qk.decode_attn_tiered_int8(
-        t["q"], t["k_hot"], t["v_hot"], t["k_cold"], t["v_cold"], t["k_scale"], t["v_scale"],
-        t["block_table"], q_pos=t["q_pos"], workspace="auto" if mode == "stream" else None,
-        dev_status=dev_status, **kw)
+    if case.cold_f16:
+        out, lse = qk.decode_attn_tiered_f16(
+            t["q"], t["k_hot"], t["v_hot"], t["k_cold"], t["v_cold"], t["block_table"],
+            q_pos=t["q_pos"], workspace="auto" if mode == "stream" else None,
+            dev_status=dev_status, **kw)
+    else:
+        out, lse = qk.decode_attn_tiered_int8(
+            t["q"], t["k_hot"], t["v_hot"], t["k_cold"], t["v_cold"], t["k_scale"], t["v_scale"],
+            t["block_table"], q_pos=t["q_pos"], workspace="auto" if mode == "stream" else None,
+            dev_status=dev_status, **kw)
     torch.cuda.synchronize()
     return out.cpu().numpy(), lse.cpu().numpy()

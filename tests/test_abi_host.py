@@ -115,6 +115,22 @@ def test_tiered_rejects_bad_tier(lib):
     assert call(qk.DaTierParams(**good), _params(head_dim=64)) == qk.DA_ERR_UNSUPPORTED
 
 
+def test_tiered_f16_rejects_bad_tier(lib):
+    p = _params(head_dim=128)
+    def call(t, pp=p, k_cold=FAKE):
+        return lib.decode_attn_tiered_f16(ctypes.byref(pp), ctypes.byref(t), FAKE, FAKE, FAKE,
+                                          k_cold, FAKE, FAKE, None, FAKE, None, None, 0, None,
+                                          None)
+    good = dict(hot_window=16, hot_capacity=16, cold_len=32, hot_len=8, hot_start=32,
+                cold_lens=None, hot_lens=None, hot_starts=None)
+    for bad in (dict(hot_len=17), dict(hot_capacity=8), dict(hot_window=-1), dict(cold_len=-1),
+                dict(cold_len=65), dict(hot_start=-3)):
+        t = qk.DaTierParams(**{**good, **bad})
+        assert call(t) == qk.DA_ERR_INVALID, bad
+    assert call(qk.DaTierParams(**good), k_cold=None) == qk.DA_ERR_INVALID
+    assert call(qk.DaTierParams(**good), _params(head_dim=96)) == qk.DA_ERR_UNSUPPORTED
+
+
 def test_batch_zero_is_a_no_op(lib):
     p = _params(batch=0)
     st = lib.decode_attn_paged(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None,
