@@ -83,6 +83,14 @@ class _TieredArgs(ctypes.Structure):
     ]
 
 
+class _AppendArgs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("B", "Hkv", "D", "block_size", "max_blocks",
+                                              "num_blocks", "hot_window", "hot_capacity")] + [
+        (n, ctypes.c_void_p) for n in ("k_new", "v_new", "k_hot", "v_hot", "k_cold", "v_cold",
+                                       "k_scale", "v_scale", "k_cold_f16", "v_cold_f16",
+                                       "block_table", "cold_lens", "hot_lens", "hot_starts")]
+
+
 def _load():
     global _lib
     with _lock:
@@ -106,6 +114,16 @@ def _load():
             lib.oracle_decode_tiered.restype = ctypes.c_int32
             lib.oracle_decode_tiered.argtypes = [ctypes.POINTER(_TieredArgs), ctypes.c_void_p,
                                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_float_to_half_array.restype = None
+            lib.oracle_float_to_half_array.argtypes = [ctypes.c_void_p, ctypes.c_int64,
+                                                       ctypes.c_void_p]
+            lib.oracle_quantize_row_int8.restype = None
+            lib.oracle_quantize_row_int8.argtypes = [ctypes.c_void_p, ctypes.c_int64,
+                                                     ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_append_tiered.restype = ctypes.c_int32
+            lib.oracle_append_tiered.argtypes = [ctypes.POINTER(_AppendArgs)]
+            lib.oracle_append_paged.restype = ctypes.c_int32
+            lib.oracle_append_paged.argtypes = [ctypes.c_int64] * 6 + [ctypes.c_void_p] * 6
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -294,3 +312,73 @@ def decode_tiered_f16(q, k_hot, v_hot, k_cold, v_cold, block_table, cold_lens, h
     lse = np.zeros(n, dtype=np.float64)
     flags = _load().oracle_decode_tiered(ctypes.byref(args), _ptr(rows_a), n, _ptr(out), _ptr(lse))
     return out, lse, int(flags)
+
+
+# ---------------------------------------------------------------------------
+# KV append and int8 demotion
+# ---------------------------------------------------------------------------
+
+def float_to_half(x) -> np.ndarray:
+    """binary16 bit patterns (uint16) of float32 values, round to nearest even,
+    with the oracle's own encoder."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.zeros(x.shape, dtype=np.uint16)
+    _load().oracle_float_to_half_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def quantize_row_int8(x):
+    """Demotion quantizer of one row of f16 values: (int8 codes, f16 scale bits)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float16))
+    assert x.ndim == 1 and x.size <= 1024
+    code = np.zeros(x.size, dtype=np.int8)
+    scale = np.zeros(1, dtype=np.uint16)
+    _load().oracle_quantize_row_int8(_ptr(x.view(np.uint16)), x.size, _ptr(code), _ptr(scale))
+    return code, int(scale[0])
+
+
+def append_tiered(k_new, v_new, k_hot, v_hot, k_cold, v_cold, k_scale, v_scale, block_table,
+                  cold_lens, hot_lens, hot_starts, *, hot_window):
+    """One append step of a tiered cache, on copies.  int8 tier: k_cold/v_cold
+    uint32 words [NB, bs, Hkv, D/4] with k_scale/v_scale f16 [NB, bs, Hkv];
+    f16 tier: k_cold/v_cold float16 [NB, bs, Hkv, D] and k_scale = v_scale =
+    None.  Returns (dict of the updated arrays, flags)."""
+    k_new = np.ascontiguousarray(k_new, dtype=np.float16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.float16)
+    st = {n: np.array(a, copy=True) for n, a in (("k_hot", k_hot), ("v_hot", v_hot),
+                                                  ("k_cold", k_cold), ("v_cold", v_cold))}
+    f16 = st["k_cold"].dtype == np.float16
+    if not f16:
+        st["k_scale"] = np.array(k_scale, dtype=np.float16, copy=True)
+        st["v_scale"] = np.array(v_scale, dtype=np.float16, copy=True)
+    for n, a in (("cold_lens", cold_lens), ("hot_lens", hot_lens), ("hot_starts", hot_starts)):
+        st[n] = np.array(a, dtype=np.int32, copy=True)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    B, cap, Hkv, D = st["k_hot"].shape
+    NB, bs = st["k_cold"].shape[:2]
+    assert D <= 1024 and k_new.shape == (B, Hkv, D)
+    args = _AppendArgs(B, Hkv, D, bs, bt.shape[1], NB, int(hot_window), cap,
+                       _ptr(k_new), _ptr(v_new), _ptr(st["k_hot"]), _ptr(st["v_hot"]),
+                       None if f16 else _ptr(st["k_cold"]), None if f16 else _ptr(st["v_cold"]),
+                       None if f16 else _ptr(st["k_scale"]), None if f16 else _ptr(st["v_scale"]),
+                       _ptr(st["k_cold"]) if f16 else None, _ptr(st["v_cold"]) if f16 else None,
+                       _ptr(bt), _ptr(st["cold_lens"]), _ptr(st["hot_lens"]),
+                       _ptr(st["hot_starts"]))
+    flags = _load().oracle_append_tiered(ctypes.byref(args))
+    return st, int(flags)
+
+
+def append_paged(k_new, v_new, positions, block_table, k_pool, v_pool):
+    """Writes each sequence's new K/V row [B, Hkv, D] at its position, on
+    copies of the pools.  Returns (k_pool, v_pool, flags)."""
+    k_new = np.ascontiguousarray(k_new, dtype=np.float16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.float16)
+    kp = np.array(k_pool, dtype=np.float16, copy=True)
+    vp = np.array(v_pool, dtype=np.float16, copy=True)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    NB, bs, Hkv, D = kp.shape
+    B = k_new.shape[0]
+    flags = _load().oracle_append_paged(B, Hkv, D, bs, bt.shape[1], NB, _ptr(k_new), _ptr(v_new),
+                                        _ptr(pos), _ptr(bt), _ptr(kp), _ptr(vp))
+    return kp, vp, int(flags)

@@ -469,6 +469,196 @@ int32_t oracle_decode_tiered(const oracle_tiered_args* a, const int64_t* rows, i
   return flags;
 }
 
+/* ================================================================== */
+/* KV append and int8 demotion (the steps either side of decode: the  */
+/* layouts of [T] and [E]; the demotion quantizer is the one the      */
+/* tiered workload's inputs are made with, scale = max|x|/127)         */
+/* ================================================================== */
+
+/* binary16 encoding of an f32 value, round to nearest even, written out
+ * from the format definition.  Values are handled exactly in double. */
+uint16_t oracle_float_to_half(float f) {
+  uint32_t bits;
+  memcpy(&bits, &f, sizeof bits);
+  const uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+  if ((bits & 0x7f800000u) == 0x7f800000u)
+    return (uint16_t)(sign | ((bits & 0x007fffffu) ? 0x7e00u : 0x7c00u));
+  const double a = fabs((double)f);
+  if (a >= 65520.0) return (uint16_t)(sign | 0x7c00u); /* past max + half an ulp */
+  if (a < ldexp(1.0, -14)) {
+    /* subnormal range: multiples of 2^-24; 1024 of them is the smallest normal */
+    const double r = rint(a / ldexp(1.0, -24));
+    return (uint16_t)(sign | (uint16_t)r);
+  }
+  int e2;
+  frexp(a, &e2);
+  int e = e2 - 1; /* 2^e <= a < 2^(e+1) */
+  double r = rint(a / ldexp(1.0, e - 10)); /* 1024 .. 2048 */
+  if (r == 2048.0) {
+    r = 1024.0;
+    e += 1;
+  }
+  return (uint16_t)(sign | (uint16_t)(((e + 15) << 10) | ((int)r - 1024)));
+}
+
+/* Element-wise oracle_float_to_half over an array. */
+void oracle_float_to_half_array(const float* x, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_float_to_half(x[i]);
+}
+
+/* Quantizer of one (token, kv head) row of n f16 values: s16 = f16(m / 127)
+ * with m = max|x| and the division in f32; code = rint(x / f32(s16)) (ties
+ * to even, f32 division) clamped to [-127, 127]; code 0 when s16 is 0 or the
+ * ratio is not a number.  Codes are written as int8. */
+void oracle_quantize_row_int8(const uint16_t* x, int64_t n, int8_t* code, uint16_t* scale) {
+  float m = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    const float v = (float)oracle_half_to_double(x[i]);
+    const float av = fabsf(v);
+    if (av > m) m = av;
+  }
+  const float sf = m / 127.0f;
+  const uint16_t s16 = oracle_float_to_half(sf);
+  const float s = (float)oracle_half_to_double(s16);
+  for (int64_t i = 0; i < n; ++i) {
+    int c = 0;
+    if (s != 0.0f) {
+      const float r = (float)oracle_half_to_double(x[i]) / s;
+      if (r == r) {
+        float t = rintf(r);
+        if (t > 127.0f) t = 127.0f;
+        if (t < -127.0f) t = -127.0f;
+        c = (int)t;
+      }
+    }
+    code[i] = (int8_t)c;
+  }
+  *scale = s16;
+}
+
+typedef struct {
+  int64_t B, Hkv, D, block_size, max_blocks, num_blocks, hot_window, hot_capacity;
+  const uint16_t* k_new;      /* [B, Hkv, D] f16 bits */
+  const uint16_t* v_new;
+  uint16_t* k_hot;            /* [B, cap, Hkv, D] */
+  uint16_t* v_hot;
+  uint32_t* k_cold;           /* int8 tier: [NB, bs, Hkv, D/4] words, or NULL */
+  uint32_t* v_cold;
+  uint16_t* k_scale;          /* int8 tier: [NB, bs, Hkv] */
+  uint16_t* v_scale;
+  uint16_t* k_cold_f16;       /* f16 tier: [NB, bs, Hkv, D], or NULL */
+  uint16_t* v_cold_f16;
+  const int32_t* block_table; /* [B, max_blocks] (cold pages) */
+  int32_t* cold_lens;         /* [B], updated */
+  int32_t* hot_lens;
+  int32_t* hot_starts;
+} oracle_append_args;
+
+static void demote_row(const oracle_append_args* a, const uint16_t* hot, uint32_t* words,
+                       uint16_t* scales, uint16_t* f16rows, int64_t hot_row, int64_t cold_row) {
+  const int64_t D = a->D;
+  for (int64_t kv = 0; kv < a->Hkv; ++kv) {
+    const uint16_t* x = hot + (hot_row * a->Hkv + kv) * D;
+    if (f16rows) {
+      memcpy(f16rows + (cold_row * a->Hkv + kv) * D, x, sizeof(uint16_t) * (size_t)D);
+      continue;
+    }
+    int8_t code[1024]; /* D <= 1024 (checked by the caller) */
+    uint16_t s16;
+    oracle_quantize_row_int8(x, D, code, &s16);
+    for (int64_t w = 0; w < D / 4; ++w) {
+      uint32_t word = 0;
+      for (int lane = 0; lane < 4; ++lane)
+        word |= (uint32_t)(uint8_t)code[4 * w + lane] << (8 * lane);
+      words[(cold_row * a->Hkv + kv) * (D / 4) + w] = word;
+    }
+    scales[cold_row * a->Hkv + kv] = s16;
+  }
+}
+
+/* One append step of every sequence of a tiered cache (ring of W slots):
+ *  - when the ring holds W tokens, the oldest (position hot_start, slot
+ *    hot_start % W) moves to the cold tier at position cold_len, which must
+ *    equal hot_start (contiguous tiers): page block_table[b][cold_len/bs],
+ *    row cold_len % bs; int8 tier: quantized as above; f16 tier: copied;
+ *    cold_len += 1, hot_start += 1, hot_len -= 1;
+ *  - the new token goes to slot (hot_start + hot_len) % W; hot_len += 1.
+ * A sequence whose state is inconsistent (flag 16), whose cold position is
+ * past the block table (flag 2) or whose page id is out of range (flag 1)
+ * is left unchanged.  Returns the flags. */
+int32_t oracle_append_tiered(const oracle_append_args* a) {
+  int32_t flags = 0;
+  const int64_t W = a->hot_window;
+  for (int64_t b = 0; b < a->B; ++b) {
+    int64_t cl = a->cold_lens[b], hl = a->hot_lens[b], hs = a->hot_starts[b];
+    if (W <= 0 || hl < 0 || hl > W || cl < 0 || hs < 0) {
+      flags |= ORACLE_FLAG_BAD_TIER;
+      continue;
+    }
+    if (hl == W) {
+      if (cl != hs) {
+        flags |= ORACLE_FLAG_BAD_TIER;
+        continue;
+      }
+      if (cl >= a->max_blocks * a->block_size) {
+        flags |= ORACLE_FLAG_BAD_SEQ_LEN;
+        continue;
+      }
+      const int64_t blk = a->block_table[b * a->max_blocks + cl / a->block_size];
+      if (blk < 0 || blk >= a->num_blocks) {
+        flags |= ORACLE_FLAG_BAD_BLOCK;
+        continue;
+      }
+      const int64_t cold_row = blk * a->block_size + cl % a->block_size;
+      const int64_t hot_row = b * a->hot_capacity + hs % W;
+      demote_row(a, a->k_hot, a->k_cold, a->k_scale, a->k_cold_f16, hot_row, cold_row);
+      demote_row(a, a->v_hot, a->v_cold, a->v_scale, a->v_cold_f16, hot_row, cold_row);
+      cl += 1;
+      hs += 1;
+      hl -= 1;
+    }
+    const int64_t slot = (hs + hl) % W;
+    const size_t row_bytes = sizeof(uint16_t) * (size_t)(a->Hkv * a->D);
+    memcpy(a->k_hot + (b * a->hot_capacity + slot) * a->Hkv * a->D, a->k_new + b * a->Hkv * a->D,
+           row_bytes);
+    memcpy(a->v_hot + (b * a->hot_capacity + slot) * a->Hkv * a->D, a->v_new + b * a->Hkv * a->D,
+           row_bytes);
+    hl += 1;
+    a->cold_lens[b] = (int32_t)cl;
+    a->hot_lens[b] = (int32_t)hl;
+    a->hot_starts[b] = (int32_t)hs;
+  }
+  return flags;
+}
+
+/* Append to a paged f16 cache (the paged address of [B]): the new
+ * token of sequence b at position positions[b] goes to page
+ * block_table[b][pos/bs], row pos % bs.  A position past the table (flag 2) or
+ * a page id out of range (flag 1) writes nothing. */
+int32_t oracle_append_paged(int64_t B, int64_t Hkv, int64_t D, int64_t block_size,
+                            int64_t max_blocks, int64_t num_blocks, const uint16_t* k_new,
+                            const uint16_t* v_new, const int32_t* positions,
+                            const int32_t* block_table, uint16_t* k_pool, uint16_t* v_pool) {
+  int32_t flags = 0;
+  const size_t row_bytes = sizeof(uint16_t) * (size_t)(Hkv * D);
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t pos = positions[b];
+    if (pos < 0 || pos >= max_blocks * block_size) {
+      flags |= ORACLE_FLAG_BAD_SEQ_LEN;
+      continue;
+    }
+    const int64_t blk = block_table[b * max_blocks + pos / block_size];
+    if (blk < 0 || blk >= num_blocks) {
+      flags |= ORACLE_FLAG_BAD_BLOCK;
+      continue;
+    }
+    const int64_t row = blk * block_size + pos % block_size;
+    memcpy(k_pool + row * Hkv * D, k_new + b * Hkv * D, row_bytes);
+    memcpy(v_pool + row * Hkv * D, v_new + b * Hkv * D, row_bytes);
+  }
+  return flags;
+}
+
 /* Threads the OpenMP runtime will use (reported beside timings). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

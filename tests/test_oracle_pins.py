@@ -573,3 +573,211 @@ def test_negative_qpos_gives_empty_row():
                                           np.array([-3], np.int32))
     assert flags & oracle.FLAG_BAD_QPOS
     assert not out.any() and lse[0] == -np.inf
+
+
+# ---------------------------------------------------------------------------
+# KV append and int8 demotion
+# ---------------------------------------------------------------------------
+
+def test_float_to_half_matches_numpy_round_to_nearest_even():
+    """The oracle's binary16 encoder against numpy's f32 -> f16 cast (IEEE
+    round to nearest even) on every exact tie between neighbouring f16
+    values, the f32 values either side of each tie, and random patterns."""
+    h = np.arange(0, 0x7c00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = (h[:-1] + h[1:]) / 2  # exact in f32 (12 significant bits)
+    m32 = mids.astype(np.float32)
+    cand = np.concatenate([m32, np.nextafter(m32, np.float32(0)), np.nextafter(m32, np.float32(1e9)),
+                           np.float32([0.0, 65504.0, 65519.996, 65520.0, 1e9, 2.0 ** -25,
+                                       2.0 ** -24, 3 * 2.0 ** -26])])
+    rng = np.random.default_rng(20)
+    rnd = rng.integers(0, 2 ** 32, size=200_000, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    cand = np.concatenate([cand, -cand, rnd])
+    cand = cand[np.isfinite(cand)]
+    with np.errstate(over="ignore"):
+        want = cand.astype(np.float16).view(np.uint16)
+    got = oracle.float_to_half(cand)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (cand[bad[:5]], got[bad[:5]], want[bad[:5]])
+    assert oracle.float_to_half(np.float32([np.inf, -np.inf]))[0] == 0x7c00
+    assert oracle.float_to_half(np.float32([np.nan]))[0] & 0x7fff > 0x7c00
+
+
+def test_demotion_quantizer_golden_and_ties():
+    code, s = oracle.quantize_row_int8(np.array([127, -127, 63.5, 62.5, 0.5, -1.5, 1.5, 0],
+                                                np.float16))
+    assert s == 0x3c00  # f16(127 / 127) = 1.0
+    assert code.tolist() == [127, -127, 64, 62, 0, -2, 2, 0]  # ties to even
+    code, s = oracle.quantize_row_int8(np.zeros(8, np.float16))
+    assert s == 0 and not code.any()
+    # scale = f16(max|x| / 127) with the division in f32
+    x = np.array([3.0, -0.1, 2.9], np.float16)
+    code, s = oracle.quantize_row_int8(x)
+    assert s == int(np.array(np.float32(3.0) / np.float32(127.0), np.float32)
+                    .astype(np.float16).view(np.uint16))
+
+
+def test_demotion_quantizer_error_bound_and_agreement_with_input_quantizer():
+    """Every code reconstructs its value within half a scale step (no value
+    exceeds 127 steps), and the oracle's quantizer agrees bit for bit with
+    the independent numpy quantizer that makes the int8 workload inputs."""
+    from quantized_kv_decode_paged_gb300.workloads import quantize_int8_rows
+    rng = np.random.default_rng(21)
+    for D in (8, 64, 128, 256):
+        for sc in (1e-4, 0.01, 1.0, 300.0):
+            x = (rng.standard_normal(D) * sc).astype(np.float16)
+            code, s = oracle.quantize_row_int8(x)
+            s_val = float(np.uint16(s).view(np.float16))
+            q_ref, s_ref = quantize_int8_rows(x[None])
+            assert int(s_ref.view(np.uint16)[0]) == s
+            assert np.array_equal(q_ref[0], code)
+            err = np.abs(code.astype(np.float64) * s_val - x.astype(np.float64))
+            lim = np.abs(x.astype(np.float64)) <= 127 * s_val
+            assert (err[lim] <= s_val / 2 * (1 + 1e-6)).all()
+            assert np.abs(code).max() <= 127
+            if s_val >= 2.0 ** -14:  # a normal f16 scale is within 2^-11 of max|x|/127
+                assert np.abs(code).max() >= 126
+
+
+def _empty_tier(B, H, D, bs, W, npages, rng, f16=False):
+    NB = B * npages
+    table = rng.permutation(NB).reshape(B, npages).astype(np.int32)
+    kh = np.zeros((B, W, H, D), np.float16)
+    if f16:
+        kc = np.zeros((NB, bs, H, D), np.float16)
+        ks = None
+    else:
+        kc = np.zeros((NB, bs, H, D // 4), np.uint32)
+        ks = np.zeros((NB, bs, H), np.float16)
+    return kh, kc, ks, table
+
+
+def _words_to_int8(words):
+    return words.view(np.uint8).view(np.int8)
+
+
+@pytest.mark.parametrize("f16", [False, True])
+def test_append_tiered_state_machine(f16):
+    """W = 4: the first four appends fill the ring; each later append first
+    moves the oldest hot token (position hot_start) to cold position
+    cold_len (quantized, or copied for the f16 tier) and then writes the new
+    token into the freed slot."""
+    rng = np.random.default_rng(22)
+    B, H, D, bs, W = 2, 2, 16, 4, 4
+    kh, kc, ks, table = _empty_tier(B, H, D, bs, W, 3, rng, f16)
+    st = dict(k_hot=kh, v_hot=kh.copy(), k_cold=kc, v_cold=kc.copy(), k_scale=ks,
+              v_scale=None if ks is None else ks.copy(), cold_lens=np.full(B, 5, np.int32),
+              hot_lens=np.zeros(B, np.int32), hot_starts=np.full(B, 5, np.int32))
+    toks_k = rng.standard_normal((7, B, H, D)).astype(np.float16)
+    toks_v = rng.standard_normal((7, B, H, D)).astype(np.float16)
+    for i in range(7):
+        st, flags = oracle.append_tiered(toks_k[i], toks_v[i], st["k_hot"], st["v_hot"],
+                                         st["k_cold"], st["v_cold"], st.get("k_scale"),
+                                         st.get("v_scale"), table, st["cold_lens"],
+                                         st["hot_lens"], st["hot_starts"], hot_window=W)
+        assert flags == 0
+        n_demoted = max(0, i + 1 - W)
+        assert (st["hot_lens"] == min(i + 1, W)).all()
+        assert (st["cold_lens"] == 5 + n_demoted).all() and (st["hot_starts"] == 5 + n_demoted).all()
+    for b in range(B):
+        # hot token j (position 5 + 3 + j) sits in slot (8 + j) % 4 and is token 3 + j
+        for j in range(W):
+            slot = (8 + j) % W
+            assert np.array_equal(st["k_hot"][b, slot], toks_k[3 + j, b])
+            assert np.array_equal(st["v_hot"][b, slot], toks_v[3 + j, b])
+        # cold positions 5, 6, 7 hold tokens 0, 1, 2
+        for j in range(3):
+            pos = 5 + j
+            page, row = table[b, pos // bs], pos % bs
+            for h in range(H):
+                if f16:
+                    assert np.array_equal(st["k_cold"][page, row, h], toks_k[j, b, h])
+                    assert np.array_equal(st["v_cold"][page, row, h], toks_v[j, b, h])
+                else:
+                    code, s = oracle.quantize_row_int8(toks_k[j, b, h])
+                    assert np.array_equal(_words_to_int8(st["k_cold"][page, row, h]), code)
+                    assert int(st["k_scale"][page, row, h].view(np.uint16)) == s
+                    code, s = oracle.quantize_row_int8(toks_v[j, b, h])
+                    assert np.array_equal(_words_to_int8(st["v_cold"][page, row, h]), code)
+                    assert int(st["v_scale"][page, row, h].view(np.uint16)) == s
+
+
+def test_append_then_decode_equals_dense_attention():
+    """After appends that demote tokens, the tiered decode of the updated
+    cache equals dense attention over (dequantized demoted tokens, hot
+    tokens) in logical order."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(23)
+    B, Hq, H, D, bs, W = 2, 4, 2, 16, 4, 6
+    kh, kc, ks, table = _empty_tier(B, H, D, bs, W, 4, rng)
+    st = dict(k_hot=kh, v_hot=kh.copy(), k_cold=kc, v_cold=kc.copy(), k_scale=ks,
+              v_scale=ks.copy(), cold_lens=np.zeros(B, np.int32),
+              hot_lens=np.zeros(B, np.int32), hot_starts=np.zeros(B, np.int32))
+    n = 11
+    tk = rng.standard_normal((n, B, H, D)).astype(np.float16)
+    tv = rng.standard_normal((n, B, H, D)).astype(np.float16)
+    for i in range(n):
+        st, flags = oracle.append_tiered(tk[i], tv[i], st["k_hot"], st["v_hot"], st["k_cold"],
+                                         st["v_cold"], st["k_scale"], st["v_scale"], table,
+                                         st["cold_lens"], st["hot_lens"], st["hot_starts"],
+                                         hot_window=W)
+        assert flags == 0
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    out, lse, flags = oracle.decode_tiered(q, st["k_hot"], st["v_hot"], st["k_cold"],
+                                           st["v_cold"], st["k_scale"], st["v_scale"], table,
+                                           st["cold_lens"], st["hot_lens"], st["hot_starts"],
+                                           hot_window=W)
+    assert flags == 0
+    nd = n - W
+    G = Hq // H
+    scale = float(np.float32(1 / math.sqrt(D)))
+    for b in range(B):
+        kd, vd = [], []
+        for i in range(n):
+            if i < nd:
+                rk, rv = [], []
+                for h in range(H):
+                    c, s = oracle.quantize_row_int8(tk[i, b, h])
+                    rk.append(c * float(np.uint16(s).view(np.float16)))
+                    c, s = oracle.quantize_row_int8(tv[i, b, h])
+                    rv.append(c * float(np.uint16(s).view(np.float16)))
+                kd.append(np.array(rk)); vd.append(np.array(rv))
+            else:
+                kd.append(tk[i, b].astype(np.float64)); vd.append(tv[i, b].astype(np.float64))
+        kd, vd = np.array(kd), np.array(vd)
+        for h in range(Hq):
+            s_ = kd[:, h // G] @ q[b, h].astype(np.float64) * scale
+            l_ = logsumexp(s_)
+            np.testing.assert_allclose(out[b * Hq + h], np.exp(s_ - l_) @ vd[:, h // G], atol=1e-12)
+            assert abs(lse[b * Hq + h] - l_) < 1e-12
+
+
+def test_append_tiered_inconsistent_state_is_flagged_and_left_unchanged():
+    rng = np.random.default_rng(24)
+    B, H, D, bs, W = 3, 1, 8, 4, 2
+    kh, kc, ks, table = _empty_tier(B, H, D, bs, W, 2, rng)
+    table[2, 1] = 999  # out-of-range page for cold position 4..7
+    cl = np.array([3, 2, 4], np.int32)
+    hl = np.array([2, 2, 2], np.int32)
+    hs = np.array([4, 2, 4], np.int32)  # sequence 0: cold_len != hot_start with a full ring
+    new = rng.standard_normal((B, H, D)).astype(np.float16)
+    st, flags = oracle.append_tiered(new, new, kh, kh, kc, kc, ks, ks, table, cl, hl, hs,
+                                     hot_window=W)
+    assert flags == oracle.FLAG_BAD_TIER | oracle.FLAG_BAD_BLOCK
+    assert (st["cold_lens"] == [3, 3, 4]).all() and (st["hot_starts"] == [4, 3, 4]).all()
+    assert (st["hot_lens"] == [2, 2, 2]).all()
+    assert not st["k_hot"][0].any() and not st["k_hot"][2].any()  # untouched
+
+
+def test_append_paged_writes_the_row_and_flags_bad_positions():
+    rng = np.random.default_rng(25)
+    B, H, D, bs, npg = 3, 2, 8, 4, 2
+    NB = B * npg
+    table = rng.permutation(NB).reshape(B, npg).astype(np.int32)
+    table[1, 1] = -1
+    kp = np.zeros((NB, bs, H, D), np.float16)
+    new = rng.standard_normal((B, H, D)).astype(np.float16)
+    pos = np.array([5, 6, 8], np.int32)  # seq 1: page -1; seq 2: past the table
+    k2, v2, flags = oracle.append_paged(new, -new, pos, table, kp, kp)
+    assert flags == oracle.FLAG_BAD_BLOCK | oracle.FLAG_BAD_SEQ_LEN
+    assert np.array_equal(k2[table[0, 1], 1], new[0]) and np.array_equal(v2[table[0, 1], 1], -new[0])
+    assert np.count_nonzero(k2) == np.count_nonzero(new[0])
