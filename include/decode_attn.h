@@ -195,6 +195,66 @@ int decode_attn_tiered_f16(const da_params* p, const da_tier_params* t, const fl
                            int32_t* dev_status, void* stream);
 
 /*
+ * KV append: the step before a decode step (none of the pages prints it; the
+ * layouts are the ones the decode entry points read).
+ *
+ * decode_attn_append_paged — writes the new token of every sequence into the
+ * paged pool: k_new / v_new f16 [B, Hkv, D] go to page
+ * block_table[b][pos / block_size], row pos % block_size, pos = positions[b]
+ * (i32 [B], device; typically the new seq_len - 1).  A position outside
+ * [0, max_blocks_per_seq * block_size) sets DA_DEV_BAD_SEQ_LEN, a page id
+ * outside [0, num_blocks) DA_DEV_BAD_BLOCK; that sequence writes nothing.
+ * Uses batch, num_kv_heads, head_dim, block_size, max_blocks_per_seq and
+ * num_blocks of p.  Pointers to rows must be 16-byte aligned.
+ */
+int decode_attn_append_paged(const da_params* p, const uint16_t* k_new, const uint16_t* v_new,
+                             const int32_t* positions, const int32_t* block_table,
+                             uint16_t* k_pool, uint16_t* v_pool, int32_t* dev_status,
+                             void* stream);
+
+/*
+ * decode_attn_append_tiered_int8 — one append step of every sequence of an
+ * int8-cold / f16-hot tiered cache whose tier lengths live on the device
+ * (cold_lens, hot_lens, hot_starts: i32 [B], read and updated in place).
+ * With W = hot_window (> 0):
+ *   - when hot_len == W, the oldest hot token (position hot_start, ring
+ *     slot hot_start % W) moves to cold position cold_len, which must equal
+ *     hot_start: page block_table[b][cold_len / block_size], row
+ *     cold_len % block_size.  Each (token, kv head) row is quantized with
+ *     scale s = f16(max|x| / 127) (f32 division) and value
+ *     clamp(rint(x / s), -127, 127) (ties to even; 0 when s is 0), the
+ *     symmetric int8 format the tiered decode reads.  Then cold_len += 1,
+ *     hot_start += 1, hot_len -= 1;
+ *   - the new token (k_new / v_new f16 [B, Hkv, D]) goes to slot
+ *     (hot_start + hot_len) % W and hot_len += 1.
+ * A sequence with an inconsistent state (hot_len outside [0, W], negative
+ * lengths, or cold_len != hot_start with a full ring) sets DA_DEV_BAD_TIER,
+ * a cold position past the table DA_DEV_BAD_SEQ_LEN, a bad page id
+ * DA_DEV_BAD_BLOCK; such a sequence is left unchanged.  hot_capacity >= W
+ * is the row count per sequence of k_hot / v_hot.  Buffers as for
+ * decode_attn_tiered_int8.  Two calls that share the cache must be ordered.
+ */
+int decode_attn_append_tiered_int8(const da_params* p, int32_t hot_window, int32_t hot_capacity,
+                                   const uint16_t* k_new, const uint16_t* v_new,
+                                   uint16_t* k_hot, uint16_t* v_hot, uint32_t* k_cold,
+                                   uint32_t* v_cold, uint16_t* k_scale, uint16_t* v_scale,
+                                   const int32_t* block_table, int32_t* cold_lens,
+                                   int32_t* hot_lens, int32_t* hot_starts, int32_t* dev_status,
+                                   void* stream);
+
+/*
+ * decode_attn_append_tiered_f16 — as decode_attn_append_tiered_int8 for the
+ * f16 cold tier (decode_attn_tiered_f16's layout): the token leaving the
+ * ring is copied as f16 into its cold row.
+ */
+int decode_attn_append_tiered_f16(const da_params* p, int32_t hot_window, int32_t hot_capacity,
+                                  const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_hot,
+                                  uint16_t* v_hot, uint16_t* k_cold, uint16_t* v_cold,
+                                  const int32_t* block_table, int32_t* cold_lens,
+                                  int32_t* hot_lens, int32_t* hot_starts, int32_t* dev_status,
+                                  void* stream);
+
+/*
  * decode_attn_split_partial — first half of flash-decoding: split s covers
  * the visible keys of [s*split_tokens, (s+1)*split_tokens) and writes the
  * normalised partial output and its LSE:

@@ -25,7 +25,8 @@ __all__ = [
     "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
     "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_status_string",
-    "decode_attn_paged_static_ws", "DecodeAttnError", "DEV_BAD_BLOCK", "DEV_BAD_SEQ_LEN",
+    "decode_attn_paged_static_ws", "decode_attn_append_paged", "decode_attn_append_tiered_int8",
+    "decode_attn_append_tiered_f16", "DecodeAttnError", "DEV_BAD_BLOCK", "DEV_BAD_SEQ_LEN",
     "DEV_BAD_QPOS", "DEV_SPLIT_OVERFLOW", "DEV_BAD_TIER", "DEV_TIMEOUT",
 ]
 
@@ -46,7 +47,8 @@ _EXPORTS = (
     "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
     "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_workspace_init",
-    "decode_attn_status_string", "decode_attn_paged_static_ws",
+    "decode_attn_status_string", "decode_attn_paged_static_ws", "decode_attn_append_paged",
+    "decode_attn_append_tiered_int8", "decode_attn_append_tiered_f16",
 )
 
 
@@ -127,6 +129,14 @@ def load_library():
         lib.decode_attn_paged_static_ws.restype = ctypes.c_int
         lib.decode_attn_paged_static_ws.argtypes = [ctypes.POINTER(DaParams), P, P, P, P, P,
                                                     P, P, P, P, P]
+        lib.decode_attn_append_paged.restype = ctypes.c_int
+        lib.decode_attn_append_paged.argtypes = [ctypes.POINTER(DaParams)] + [P] * 8
+        lib.decode_attn_append_tiered_int8.restype = ctypes.c_int
+        lib.decode_attn_append_tiered_int8.argtypes = ([ctypes.POINTER(DaParams), i32, i32]
+                                                       + [P] * 14)
+        lib.decode_attn_append_tiered_f16.restype = ctypes.c_int
+        lib.decode_attn_append_tiered_f16.argtypes = ([ctypes.POINTER(DaParams), i32, i32]
+                                                      + [P] * 12)
         lib.decode_attn_status_string.restype = ctypes.c_char_p
         lib.decode_attn_status_string.argtypes = [ctypes.c_int]
         _lib = lib
@@ -438,3 +448,100 @@ def default_scale(head_dim: int) -> float:
     """1/sqrt(D) rounded to f32 (what scale=0 selects)."""
     import numpy as np
     return float(np.float32(1.0 / math.sqrt(head_dim)))
+
+
+# ---------------------------------------------------------------------------
+# KV append
+# ---------------------------------------------------------------------------
+
+def _append_params(k_new, block_table, pool_shape):
+    B, Hkv, D = k_new.shape
+    NB, bs = pool_shape[0], pool_shape[1]
+    return DaParams(B, Hkv, Hkv, D, bs, block_table.shape[1], NB, 0, 0.0, 0.0, 0, 1)
+
+
+def decode_attn_append_paged(k_new, v_new, positions, block_table, k_pool, v_pool, *,
+                             dev_status=None, stream=None):
+    """Writes k_new/v_new f16 [B, Hkv, D] into the paged pools [NB, bs, Hkv, D]
+    at positions i32 [B] (in place)."""
+    torch = _torch()
+    lib = load_library()
+    dev = k_new.device
+    _req(k_new, "k_new", torch.float16, dev, 3)
+    _req(v_new, "v_new", torch.float16, dev, 3)
+    _req(positions, "positions", torch.int32, dev, 1)
+    _req(block_table, "block_table", torch.int32, dev, 2)
+    _req(k_pool, "k_pool", torch.float16, dev, 4)
+    _req(v_pool, "v_pool", torch.float16, dev, 4)
+    if (v_new.shape != k_new.shape or v_pool.shape != k_pool.shape
+            or k_pool.shape[2:] != k_new.shape[1:] or positions.shape[0] != k_new.shape[0]):
+        raise ValueError("inconsistent shapes")
+    params = _append_params(k_new, block_table, k_pool.shape)
+    st = lib.decode_attn_append_paged(ctypes.byref(params), _ptr(k_new), _ptr(v_new),
+                                      _ptr(positions), _ptr(block_table), _ptr(k_pool),
+                                      _ptr(v_pool), _ptr(dev_status), _stream(dev, stream))
+    _check("decode_attn_append_paged", st)
+
+
+def _tier_state_checks(torch, dev, k_new, v_new, k_hot, v_hot, block_table, cold_lens, hot_lens,
+                       hot_starts):
+    _req(k_new, "k_new", torch.float16, dev, 3)
+    _req(v_new, "v_new", torch.float16, dev, 3)
+    _req(k_hot, "k_hot", torch.float16, dev, 4)
+    _req(v_hot, "v_hot", torch.float16, dev, 4)
+    _req(block_table, "block_table", torch.int32, dev, 2)
+    for name, t in (("cold_lens", cold_lens), ("hot_lens", hot_lens), ("hot_starts", hot_starts)):
+        _req(t, name, torch.int32, dev, 1)
+    B, Hkv, D = k_new.shape
+    if (v_new.shape != k_new.shape or k_hot.shape[0] != B or k_hot.shape[2:] != (Hkv, D)
+            or v_hot.shape != k_hot.shape):
+        raise ValueError("inconsistent shapes")
+
+
+def decode_attn_append_tiered_int8(k_new, v_new, k_hot, v_hot, k_cold, v_cold, k_scale, v_scale,
+                                   block_table, cold_lens, hot_lens, hot_starts, *, hot_window,
+                                   dev_status=None, stream=None):
+    """One append step of an int8-cold / f16-hot tiered cache (in place): the
+    oldest hot token of a full ring is quantized into the cold tier, then the
+    new token enters the ring; cold_lens/hot_lens/hot_starts are updated."""
+    torch = _torch()
+    lib = load_library()
+    dev = k_new.device
+    _tier_state_checks(torch, dev, k_new, v_new, k_hot, v_hot, block_table, cold_lens, hot_lens,
+                       hot_starts)
+    for name, t in (("k_cold", k_cold), ("v_cold", v_cold)):
+        if t.dtype not in (torch.int32, torch.uint32):
+            raise TypeError(f"{name} must hold 32-bit words")
+        _req(t, name, t.dtype, dev, 4)
+    _req(k_scale, "k_scale", torch.float16, dev, 3)
+    _req(v_scale, "v_scale", torch.float16, dev, 3)
+    if k_cold.shape[3] * 4 != k_new.shape[2] or v_cold.shape != k_cold.shape:
+        raise ValueError("inconsistent shapes")
+    params = _append_params(k_new, block_table, k_cold.shape)
+    st = lib.decode_attn_append_tiered_int8(
+        ctypes.byref(params), int(hot_window), int(k_hot.shape[1]), _ptr(k_new), _ptr(v_new),
+        _ptr(k_hot), _ptr(v_hot), _ptr(k_cold), _ptr(v_cold), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_table), _ptr(cold_lens), _ptr(hot_lens), _ptr(hot_starts), _ptr(dev_status),
+        _stream(dev, stream))
+    _check("decode_attn_append_tiered_int8", st)
+
+
+def decode_attn_append_tiered_f16(k_new, v_new, k_hot, v_hot, k_cold, v_cold, block_table,
+                                  cold_lens, hot_lens, hot_starts, *, hot_window,
+                                  dev_status=None, stream=None):
+    """As decode_attn_append_tiered_int8 for an f16 cold tier [NB, bs, Hkv, D]."""
+    torch = _torch()
+    lib = load_library()
+    dev = k_new.device
+    _tier_state_checks(torch, dev, k_new, v_new, k_hot, v_hot, block_table, cold_lens, hot_lens,
+                       hot_starts)
+    _req(k_cold, "k_cold", torch.float16, dev, 4)
+    _req(v_cold, "v_cold", torch.float16, dev, 4)
+    if k_cold.shape[2:] != k_new.shape[1:] or v_cold.shape != k_cold.shape:
+        raise ValueError("inconsistent shapes")
+    params = _append_params(k_new, block_table, k_cold.shape)
+    st = lib.decode_attn_append_tiered_f16(
+        ctypes.byref(params), int(hot_window), int(k_hot.shape[1]), _ptr(k_new), _ptr(v_new),
+        _ptr(k_hot), _ptr(v_hot), _ptr(k_cold), _ptr(v_cold), _ptr(block_table),
+        _ptr(cold_lens), _ptr(hot_lens), _ptr(hot_starts), _ptr(dev_status), _stream(dev, stream))
+    _check("decode_attn_append_tiered_f16", st)

@@ -36,6 +36,26 @@ def test_library_exports_every_declared_function(lib):
         assert hasattr(lib, name), name
 
 
+def _header_arity():
+    src = open(os.path.join(ROOT, "include", "decode_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(decode_attn_\w+)\s*\(([^)]*)\)\s*;", src):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_the_header(lib):
+    """Every ctypes prototype the binding sets has as many arguments as the
+    header declares (a mismatch would misplace every later argument)."""
+    arity = _header_arity()
+    assert set(arity) == set(_header_functions())
+    for name, n in arity.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None and len(fn.argtypes) == n, (name, n, fn.argtypes)
+
+
 def test_status_strings(lib):
     assert qk.decode_attn_status_string(0) == "ok"
     assert "invalid" in qk.decode_attn_status_string(-1)
