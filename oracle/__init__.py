@@ -61,7 +61,7 @@ class _PagedArgs(ctypes.Structure):
         ("window", ctypes.c_int64), ("causal", ctypes.c_int64),
         ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
         ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
-        ("q_pos", ctypes.c_void_p),
+        ("q_pos", ctypes.c_void_p), ("q_len", ctypes.c_int64),
     ]
 
 
@@ -181,7 +181,9 @@ def _paged_struct(keep, q, k_pool, v_pool, block_table, seq_lens, q_pos, scale, 
     block_table = keep(block_table, np.int32)
     seq_lens = keep(seq_lens, np.int32)
     q_pos = keep(q_pos, np.int32)
-    B, Hq, D = q.shape
+    # q is [B, Hq, D], or [B, T, Hq, D] for T query tokens per sequence
+    T = q.shape[1] if q.ndim == 4 else 1
+    B, Hq, D = q.shape[0], q.shape[-2], q.shape[-1]
     NB, bs, Hkv, D2 = k_pool.shape
     assert D2 == D and v_pool.shape == k_pool.shape
     assert block_table.shape[0] == B and seq_lens.shape == (B,)
@@ -189,20 +191,22 @@ def _paged_struct(keep, q, k_pool, v_pool, block_table, seq_lens, q_pos, scale, 
                       float(np.float32(scale)), float(np.float32(softcap)),
                       int(sliding_window), int(bool(causal)),
                       _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
-                      _ptr(seq_lens), _ptr(q_pos))
-    return args, B, Hq, D
+                      _ptr(seq_lens), _ptr(q_pos), T)
+    return args, B, Hq, D, T
 
 
 def decode_paged(q, k_pool, v_pool, block_table, seq_lens, q_pos=None, *, scale=0.0,
                  softcap=0.0, sliding_window=0, causal=True, rows=None):
     """Paged f16 decode attention.  Returns (out [n, D], lse [n], flags).
 
-    ``rows`` selects flat rows b*Hq + h (default: every row, in order)."""
+    ``q`` is [B, Hq, D] (one query token per sequence) or [B, T, Hq, D] (T
+    tokens at positions q_pos[b] + t, by default seq_len - T + t).  ``rows``
+    selects flat rows (b*T + t)*Hq + h (default: every row, in order)."""
     keep = _Keep()
-    args, B, Hq, D = _paged_struct(keep, q, k_pool, v_pool, block_table, seq_lens, q_pos,
-                                   scale, softcap, sliding_window, causal)
+    args, B, Hq, D, T = _paged_struct(keep, q, k_pool, v_pool, block_table, seq_lens, q_pos,
+                                      scale, softcap, sliding_window, causal)
     rows_a = _rows_arg(rows)
-    n = B * Hq if rows_a is None else len(rows_a)
+    n = B * T * Hq if rows_a is None else len(rows_a)
     out = np.zeros((n, D), dtype=np.float64)
     lse = np.zeros(n, dtype=np.float64)
     flags = _load().oracle_decode_paged(ctypes.byref(args), _ptr(rows_a), n, _ptr(out), _ptr(lse))
@@ -212,10 +216,11 @@ def decode_paged(q, k_pool, v_pool, block_table, seq_lens, q_pos=None, *, scale=
 def decode_paged_split(q, k_pool, v_pool, block_table, seq_lens, q_pos=None, *, split_tokens,
                        max_splits, scale=0.0, softcap=0.0, sliding_window=0, causal=True,
                        rows=None):
-    """Split partials.  Returns (o_part [n, S, D], lse_part [n, S], flags)."""
+    """Split partials (one query token).  Returns (o_part [n, S, D], lse_part [n, S], flags)."""
     keep = _Keep()
-    args, B, Hq, D = _paged_struct(keep, q, k_pool, v_pool, block_table, seq_lens, q_pos,
-                                   scale, softcap, sliding_window, causal)
+    args, B, Hq, D, T = _paged_struct(keep, q, k_pool, v_pool, block_table, seq_lens, q_pos,
+                                      scale, softcap, sliding_window, causal)
+    assert T == 1
     rows_a = _rows_arg(rows)
     n = B * Hq if rows_a is None else len(rows_a)
     o_part = np.zeros((n, max_splits, D), dtype=np.float64)

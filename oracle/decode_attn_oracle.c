@@ -141,7 +141,8 @@ typedef struct {
   const uint16_t* v_pool;    /* [NB, bs, Hkv, D] f16 bits */
   const int32_t* block_table;/* [B, max_blocks] */
   const int32_t* seq_lens;   /* [B] */
-  const int32_t* q_pos;      /* [B] or NULL */
+  const int32_t* q_pos;      /* [B] or NULL: position of query token 0 */
+  int64_t q_len;             /* query tokens per sequence (q is [B, q_len, Hq, D]); 0 => 1 */
 } oracle_paged_args;
 
 typedef struct {
@@ -171,23 +172,29 @@ static int64_t paged_len(const oracle_paged_args* a, int64_t b, int32_t* flags) 
 }
 
 /*
- * One row (b, h) restricted to keys in [t_begin, t_end) (the whole sequence
- * for a plain call, one split's range for a split call).
+ * One row (b, query token tq, head h) restricted to keys in [t_begin, t_end)
+ * (the whole sequence for a plain call, one split's range for a split call).
+ * With T query tokens per sequence, token tq has position base + tq, where
+ * base is q_pos[b] or, by default, L - T (the T new tokens are the last T
+ * cached keys); each token applies the causal and window rules at its own
+ * position.
  */
-static void paged_row(const oracle_paged_args* a, int64_t b, int64_t h, int64_t t_begin,
-                      int64_t t_end, double* out, double* lse, int32_t* flags) {
+static void paged_row(const oracle_paged_args* a, int64_t b, int64_t tq, int64_t h,
+                      int64_t t_begin, int64_t t_end, double* out, double* lse, int32_t* flags) {
   const int64_t D = a->D;
   const int64_t G = a->Hq / a->Hkv;
   const int64_t kv = h / G;
+  const int64_t T = a->q_len > 1 ? a->q_len : 1;
   const double scale = effective_scale(a->scale, D);
   int64_t L = paged_len(a, b, flags);
-  int64_t qpos = L - 1;
+  int64_t qpos = L - T + tq;
   if (a->q_pos) {
     qpos = a->q_pos[b];
     if (qpos < 0) {
       *flags |= ORACLE_FLAG_BAD_QPOS;
       L = 0;
     }
+    qpos += tq;
   }
   if (t_end > L) t_end = L;
   if (t_begin < 0) t_begin = 0;
@@ -195,7 +202,7 @@ static void paged_row(const oracle_paged_args* a, int64_t b, int64_t h, int64_t 
   double* s = (double*)malloc(sizeof(double) * (size_t)(n_max + 1));
   int64_t* rowaddr = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_max + 1));
   double* vbuf = (double*)malloc(sizeof(double) * (size_t)D);
-  const float* qrow = a->q + (b * a->Hq + h) * D;
+  const float* qrow = a->q + ((b * T + tq) * a->Hq + h) * D;
   int64_t n = 0;
   for (int64_t t = t_begin; t < t_end; ++t) {
     if (!key_visible(t, qpos, a->causal, a->window)) continue;
@@ -220,19 +227,20 @@ static void paged_row(const oracle_paged_args* a, int64_t b, int64_t h, int64_t 
 }
 
 /*
- * rows: flat row ids r = b*Hq + h (NULL => all B*Hq rows in order).
+ * rows: flat row ids r = (b*T + tq)*Hq + h (NULL => all B*T*Hq rows in order).
  * out: [nrows, D]; lse: [nrows].  Returns the OR of the flags.
  */
 int32_t oracle_decode_paged(const oracle_paged_args* a, const int64_t* rows, int64_t nrows,
                             double* out, double* lse) {
   int32_t flags = 0;
-  if (!rows) nrows = a->B * a->Hq;
+  const int64_t T = a->q_len > 1 ? a->q_len : 1;
+  if (!rows) nrows = a->B * T * a->Hq;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : flags)
   for (int64_t i = 0; i < nrows; ++i) {
     int64_t r = rows ? rows[i] : i;
-    int64_t b = r / a->Hq, h = r % a->Hq;
+    int64_t bt = r / a->Hq, h = r % a->Hq;
     int32_t f = 0;
-    paged_row(a, b, h, 0, INT64_MAX, out + i * a->D, lse + i, &f);
+    paged_row(a, bt / T, bt % T, h, 0, INT64_MAX, out + i * a->D, lse + i, &f);
     flags |= f;
   }
   return flags;
@@ -256,14 +264,14 @@ int32_t oracle_decode_paged_split(const oracle_paged_args* a, int64_t split_toke
     int32_t f = 0;
     for (int64_t sp = 0; sp < max_splits; ++sp) {
       int64_t t0 = sp * split_tokens, t1 = t0 + split_tokens;
-      paged_row(a, b, h, t0, t1, o_part + (i * max_splits + sp) * a->D,
+      paged_row(a, b, 0, h, t0, t1, o_part + (i * max_splits + sp) * a->D,
                 lse_part + i * max_splits + sp, &f);
     }
     /* keys beyond the last split: any visible one raises the flag */
     double tail_lse;
     double* tail = (double*)malloc(sizeof(double) * (size_t)a->D);
     int32_t ftail = 0;
-    paged_row(a, b, h, max_splits * split_tokens, INT64_MAX, tail, &tail_lse, &ftail);
+    paged_row(a, b, 0, h, max_splits * split_tokens, INT64_MAX, tail, &tail_lse, &ftail);
     if (tail_lse > -INFINITY) f |= ORACLE_FLAG_SPLIT_OVERFLOW;
     free(tail);
     flags |= f;

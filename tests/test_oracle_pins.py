@@ -781,3 +781,58 @@ def test_append_paged_writes_the_row_and_flags_bad_positions():
     assert flags == oracle.FLAG_BAD_BLOCK | oracle.FLAG_BAD_SEQ_LEN
     assert np.array_equal(k2[table[0, 1], 1], new[0]) and np.array_equal(v2[table[0, 1], 1], -new[0])
     assert np.count_nonzero(k2) == np.count_nonzero(new[0])
+
+
+# ---------------------------------------------------------------------------
+# multi-token query decode
+# ---------------------------------------------------------------------------
+
+def test_multi_token_rows_equal_single_token_calls_at_their_positions():
+    """A T-token call is T single-token decodes: token t of sequence b is
+    the one-token decode at position q_pos[b] + t (window and softcap on)."""
+    rng = np.random.default_rng(30)
+    B, T, Hq, H, D, bs = 3, 5, 8, 2, 16, 4
+    lens = np.array([40, 23, 9], np.int32)
+    k, v = rand_dense(rng, B, int(lens.max()), H, D)
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng)
+    q = rng.standard_normal((B, T, Hq, D)).astype(np.float32)
+    base = np.array([30, 18, 2], np.int32)
+    multi = oracle.decode_paged(q, kp, vp, table, lens, base, softcap=15.0, sliding_window=11)
+    assert multi[2] == 0
+    for t in range(T):
+        single = oracle.decode_paged(np.ascontiguousarray(q[:, t]), kp, vp, table, lens,
+                                     base + t, softcap=15.0, sliding_window=11)
+        for b in range(B):
+            rows = slice((b * T + t) * Hq, (b * T + t + 1) * Hq)
+            assert np.array_equal(multi[0][rows], single[0][b * Hq:(b + 1) * Hq])
+            assert np.array_equal(multi[1][rows], single[1][b * Hq:(b + 1) * Hq])
+
+
+def test_multi_token_default_positions_are_the_last_cached_keys():
+    """Without q_pos, token t sits at seq_len - T + t: the last token sees
+    every key (the one-token default), token t sees keys 0 .. L-T+t (dense
+    causal reference)."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(31)
+    B, T, Hq, H, D, bs = 2, 4, 4, 2, 8, 8
+    lens = np.array([21, 13], np.int32)
+    k, v = rand_dense(rng, B, int(lens.max()), H, D)
+    kp, vp, table = paged_from_dense(k, v, bs, rng=rng)
+    q = rng.standard_normal((B, T, Hq, D)).astype(np.float32)
+    out, lse, flags = oracle.decode_paged(q, kp, vp, table, lens)
+    assert flags == 0
+    last = oracle.decode_paged(np.ascontiguousarray(q[:, T - 1]), kp, vp, table, lens)
+    G = Hq // H
+    scale = float(np.float32(1 / math.sqrt(D)))
+    for b in range(B):
+        rows = slice((b * T + T - 1) * Hq, (b * T + T) * Hq)
+        assert np.array_equal(out[rows], last[0][b * Hq:(b + 1) * Hq])
+        for t in range(T):
+            n = int(lens[b]) - T + t + 1
+            for h in range(Hq):
+                s = k[b, :n, h // G].astype(np.float64) @ q[b, t, h].astype(np.float64) * scale
+                l_ = logsumexp(s)
+                r = (b * T + t) * Hq + h
+                np.testing.assert_allclose(out[r], np.exp(s - l_) @ v[b, :n, h // G].astype(np.float64),
+                                           atol=1e-12)
+                assert abs(lse[r] - l_) < 1e-12
