@@ -54,9 +54,9 @@
  *       lse          f32  [B, Hq] or NULL (not written)
  *   - A sequence with no visible key (seq_len 0) gets out = 0, lse = -inf.
  *   - Supported sizes: head_dim in {64, 128, 256}; num_q_heads a multiple of
- *     num_kv_heads with G = Hq/Hkv <= 8 or a multiple of 8; block_size a
- *     power of two in [8, 256]; tensor pointers 16-byte aligned (index
- *     arrays 4-byte aligned).  Other sizes return DA_ERR_UNSUPPORTED.
+ *     num_kv_heads; block_size a power of two in [8, 256]; tensor pointers
+ *     16-byte aligned (index arrays 4-byte aligned).  Other sizes return
+ *     DA_ERR_UNSUPPORTED.
  */
 #ifndef DECODE_ATTN_H
 #define DECODE_ATTN_H
@@ -127,6 +127,24 @@ int decode_attn_paged(const da_params* p, const float* q, const uint16_t* k_pool
                       const int32_t* seq_lens, const int32_t* q_pos, float* out,
                       float* lse, void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
+
+/*
+ * decode_attn_paged_multi — decode attention of q_len query tokens per
+ * sequence (speculative or chunked decode) over the paged cache.  Token t of
+ * sequence b has position q_pos[b] + t (q_pos NULL: seq_len - q_len + t, the
+ * q_len new tokens being the last q_len cached keys) and applies the causal
+ * and sliding-window rules at its own position (doppler
+ * "attention_f16kv.wgsl" is_masked for a query tile with start_pos).
+ *   q   f32 [B, q_len, Hq, D]
+ *   out f32 [B, q_len, Hq, D];  lse f32 [B, q_len, Hq] or NULL
+ * Everything else as for decode_attn_paged, which is the q_len = 1 case.
+ * The q_len*G query rows of a kv head share every K/V byte read from HBM.
+ */
+int decode_attn_paged_multi(const da_params* p, int32_t q_len, const float* q,
+                            const uint16_t* k_pool, const uint16_t* v_pool,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            const int32_t* q_pos, float* out, float* lse, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
  * Tier geometry for decode_attn_tiered_int8 and decode_attn_tiered_f16.

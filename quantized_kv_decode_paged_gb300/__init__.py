@@ -22,7 +22,7 @@ from . import _build
 
 __all__ = [
     "load_library", "library_path", "build",
-    "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
+    "decode_attn_paged", "decode_attn_paged_multi", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
     "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_status_string",
     "decode_attn_paged_static_ws", "decode_attn_append_paged", "decode_attn_append_tiered_int8",
@@ -44,7 +44,7 @@ DA_ERR_WORKSPACE = -3
 DA_ERR_CUDA = -4
 
 _EXPORTS = (
-    "decode_attn_paged", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
+    "decode_attn_paged", "decode_attn_paged_multi", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
     "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_workspace_init",
     "decode_attn_status_string", "decode_attn_paged_static_ws", "decode_attn_append_paged",
@@ -109,6 +109,9 @@ def load_library():
         lib.decode_attn_paged.restype = ctypes.c_int
         lib.decode_attn_paged.argtypes = [ctypes.POINTER(DaParams), P, P, P, P, P, P, P, P, P,
                                           ctypes.c_size_t, P, P]
+        lib.decode_attn_paged_multi.restype = ctypes.c_int
+        lib.decode_attn_paged_multi.argtypes = [ctypes.POINTER(DaParams), i32, P, P, P, P, P, P,
+                                                P, P, P, ctypes.c_size_t, P, P]
         lib.decode_attn_tiered_int8.restype = ctypes.c_int
         lib.decode_attn_tiered_int8.argtypes = [ctypes.POINTER(DaParams),
                                                 ctypes.POINTER(DaTierParams), P, P, P, P, P, P,
@@ -265,6 +268,48 @@ def decode_attn_paged(q, k_pool, v_pool, block_table, seq_lens, q_pos=None, *, s
                                _ptr(lse), ws_ptr, ws_bytes, _ptr(dev_status),
                                _stream(dev, stream))
     _check("decode_attn_paged", st)
+    return out, lse
+
+
+def decode_attn_paged_multi(q, k_pool, v_pool, block_table, seq_lens, q_pos=None, *, scale=0.0,
+                            softcap=0.0, sliding_window=0, causal=True, max_seq_len=0, out=None,
+                            lse=None, workspace="auto", dev_status=None, stream=None):
+    """Decode of T query tokens per sequence: q f32 [B, T, Hq, D]; token t sits
+    at q_pos[b] + t (default seq_len - T + t).  Returns (out [B, T, Hq, D],
+    lse [B, T, Hq])."""
+    torch = _torch()
+    lib = load_library()
+    dev = q.device
+    _req(q, "q", torch.float32, dev, 4)
+    _req(k_pool, "k_pool", torch.float16, dev, 4)
+    _req(v_pool, "v_pool", torch.float16, dev, 4)
+    _req(block_table, "block_table", torch.int32, dev, 2)
+    _req(seq_lens, "seq_lens", torch.int32, dev, 1)
+    if q_pos is not None:
+        _req(q_pos, "q_pos", torch.int32, dev, 1)
+    if k_pool.shape != v_pool.shape:
+        raise ValueError("k_pool and v_pool shapes differ")
+    B, T, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_pool.shape
+    if D2 != D or block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((B, T, Hq, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=dev)
+    _req(out, "out", torch.float32, dev, 4)
+    _req(lse, "lse", torch.float32, dev, 3)
+    if dev_status is not None:
+        _req(dev_status, "dev_status", torch.int32, dev)
+    params = make_params(q[:, 0], bs, Hkv, block_table.shape[1], NB, scale=scale,
+                         softcap=softcap, sliding_window=sliding_window, causal=causal,
+                         max_seq_len=max_seq_len)
+    ws_ptr, ws_bytes = _workspace_args(workspace, params, dev)
+    st = lib.decode_attn_paged_multi(ctypes.byref(params), int(T), _ptr(q), _ptr(k_pool),
+                                     _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
+                                     _ptr(q_pos), _ptr(out), _ptr(lse), ws_ptr, ws_bytes,
+                                     _ptr(dev_status), _stream(dev, stream))
+    _check("decode_attn_paged_multi", st)
     return out, lse
 
 

@@ -69,11 +69,6 @@ int check_params(const da_params* p, bool tiered) {
   if (!p) return DA_ERR_INVALID;
   if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0) return DA_ERR_INVALID;
   if (p->num_q_heads % p->num_kv_heads != 0) return DA_ERR_INVALID;
-  {
-    // head groups of 8: a group size above 8 must split into whole groups
-    const int G = p->num_q_heads / p->num_kv_heads;
-    if (G > da::kHeadTile && G % da::kHeadTile != 0) return DA_ERR_UNSUPPORTED;
-  }
   if (p->head_dim <= 0) return DA_ERR_INVALID;
   if (tiered) {
     if (p->head_dim != 128 && p->head_dim != 256) return DA_ERR_UNSUPPORTED;
@@ -137,14 +132,22 @@ int test_skip_arm() {
   return (e && e[0] == '1' && e[1] == '\0') ? 1 : 0;
 }
 
+// T query tokens per sequence: T*G query rows per kv head, in head groups of
+// kHeadTile (the last one may be partial).
+void set_query_tokens(KParams& k, int T) {
+  k.q_len = T;
+  k.Gv = T * k.G;
+  k.NH = k.Gv < da::kHeadTile ? k.Gv : da::kHeadTile;
+  k.HG = (k.Gv + da::kHeadTile - 1) / da::kHeadTile;
+}
+
 void fill_common(KParams& k, const da_params* p) {
   k.B = p->batch;
   k.Hq = p->num_q_heads;
   k.Hkv = p->num_kv_heads;
   k.D = p->head_dim;
   k.G = p->num_q_heads / p->num_kv_heads;
-  k.NH = k.G < da::kHeadTile ? k.G : da::kHeadTile;
-  k.HG = (k.G + da::kHeadTile - 1) / da::kHeadTile;
+  set_query_tokens(k, 1);
   k.bs = p->block_size;
   k.log2_bs = ilog2(p->block_size);
   k.max_blocks = p->max_blocks_per_seq;
@@ -265,7 +268,7 @@ WsLayout ws_layout(int grid, int D, int kvb) {
 int ws_kvb(const da_params* p) {
   const int D = p->head_dim, H = p->num_kv_heads;
   int m = 0;
-  for (int kind : {da::KIND_PAGED, da::KIND_TIERED, da::KIND_TIERED_F16}) {
+  for (int kind : {da::KIND_PAGED, da::KIND_TIERED, da::KIND_TIERED_F16, da::KIND_PAGED_MULTI}) {
     const int v = kvb_override(kind, D, H, da::decode_kvb(kind, D, H));
     m = v > m ? v : m;
   }
@@ -410,6 +413,45 @@ int tiered_impl(int kind, const da_params* p, const da_tier_params* t, const flo
   return run_batched(k, lc, off, static_cast<cudaStream_t>(stream));
 }
 
+// Paged decode of T query tokens per sequence (T = 1: one-token decode).
+int paged_impl(const da_params* p, int T, const float* q, const uint16_t* k_pool,
+               const uint16_t* v_pool, const int32_t* block_table, const int32_t* seq_lens,
+               const int32_t* q_pos, float* out, float* lse, void* workspace,
+               size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  int st = check_params(p, false);
+  if (st != DA_OK) return st;
+  if (T < 1) return DA_ERR_INVALID;
+  if ((long long)T * p->num_q_heads > 0x7fffffffLL / 64) return DA_ERR_UNSUPPORTED;
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out) return DA_ERR_INVALID;
+  if (!workspace && workspace_bytes) return DA_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || (q_pos && !aligned(q_pos, 4)) ||
+      (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
+    return DA_ERR_INVALID;
+  if (p->batch == 0) return DA_OK;
+  KParams k;
+  memset(&k, 0, sizeof(k));
+  fill_common(k, p);
+  set_query_tokens(k, T);
+  const int kind = T > 1 ? da::KIND_PAGED_MULTI : da::KIND_PAGED;
+  k.KVB = kvb_override(kind, p->head_dim, p->num_kv_heads,
+                       da::decode_kvb(kind, p->head_dim, p->num_kv_heads));
+  st = encode_paged_maps(k, kind, k_pool, v_pool, p);
+  if (st != DA_OK) return st;
+  k.dev_status = dev_status;
+  Launch lc{kind, p, workspace, workspace_bytes};
+  const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
+  auto off = [&](KParams& kk, int b0) {
+    kk.q = q + (long long)b0 * T * Hq * D;
+    kk.block_table = block_table + (long long)b0 * mb;
+    kk.seq_lens = seq_lens + b0;
+    kk.q_pos = q_pos ? q_pos + b0 : nullptr;
+    kk.out = out + (long long)b0 * T * Hq * D;
+    kk.lse = lse ? lse + (long long)b0 * T * Hq : nullptr;
+  };
+  return run_batched(k, lc, off, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -445,32 +487,17 @@ int decode_attn_paged(const da_params* p, const float* q, const uint16_t* k_pool
                       const int32_t* seq_lens, const int32_t* q_pos, float* out, float* lse,
                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
                       void* stream) {
-  int st = check_params(p, false);
-  if (st != DA_OK) return st;
-  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out) return DA_ERR_INVALID;
-  if (!workspace && workspace_bytes) return DA_ERR_INVALID;
-  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
-      !aligned(block_table, 4) || !aligned(seq_lens, 4) || (q_pos && !aligned(q_pos, 4)) ||
-      (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
-    return DA_ERR_INVALID;
-  if (p->batch == 0) return DA_OK;
-  KParams k;
-  memset(&k, 0, sizeof(k));
-  fill_common(k, p);
-  st = encode_paged_maps(k, da::KIND_PAGED, k_pool, v_pool, p);
-  if (st != DA_OK) return st;
-  k.dev_status = dev_status;
-  Launch lc{da::KIND_PAGED, p, workspace, workspace_bytes};
-  const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
-  auto off = [&](KParams& kk, int b0) {
-    kk.q = q + (long long)b0 * Hq * D;
-    kk.block_table = block_table + (long long)b0 * mb;
-    kk.seq_lens = seq_lens + b0;
-    kk.q_pos = q_pos ? q_pos + b0 : nullptr;
-    kk.out = out + (long long)b0 * Hq * D;
-    kk.lse = lse ? lse + (long long)b0 * Hq : nullptr;
-  };
-  return run_batched(k, lc, off, static_cast<cudaStream_t>(stream));
+  return paged_impl(p, 1, q, k_pool, v_pool, block_table, seq_lens, q_pos, out, lse, workspace,
+                    workspace_bytes, dev_status, stream);
+}
+
+int decode_attn_paged_multi(const da_params* p, int32_t q_len, const float* q,
+                            const uint16_t* k_pool, const uint16_t* v_pool,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            const int32_t* q_pos, float* out, float* lse, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return paged_impl(p, q_len, q, k_pool, v_pool, block_table, seq_lens, q_pos, out, lse,
+                    workspace, workspace_bytes, dev_status, stream);
 }
 
 int decode_attn_split_partial(const da_params* p, int32_t split_tokens, int32_t max_splits,

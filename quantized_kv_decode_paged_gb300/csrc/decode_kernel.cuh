@@ -126,11 +126,11 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
   bool empty = false;
   long long L = 0;  // paged: keys 0..L-1
   long long cl = 0, hl = 0, hs = 0;
-  if (KIND == KIND_PAGED) {
+  if (is_paged(KIND)) {
     L = p.seq_lens[b];
     if (L < 0) { flags |= DEV_BAD_SEQ_LEN; L = 0; }
     if (L > cap) { flags |= DEV_BAD_SEQ_LEN; L = cap; }
-    qp = L - 1;
+    qp = L - p.q_len;  // query token 0; the T new tokens are the last T keys
   } else {
     cl = p.cold_lens ? p.cold_lens[b] : p.cold_len;
     hl = p.hot_lens ? p.hot_lens[b] : p.hot_len;
@@ -147,16 +147,18 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
     qp = p.q_pos[b];
     if (qp < 0) { flags |= DEV_BAD_QPOS; empty = true; }
   }
-  // is_masked: causal hides keys after qp; a window W hides keys below
-  // qp - W + 1 once qp >= W.
+  e.qp0 = (int)qp;
+  // is_masked: causal hides keys after a token's position qp + t; a window W
+  // hides keys below qp + t - W + 1 once qp + t >= W.  [lo, hi) is the union
+  // over the T tokens (token 0's lower bound, token T-1's upper bound).
   long long lo = (p.window > 0 && qp >= p.window) ? qp - p.window + 1 : 0;
-  long long hi = p.causal ? qp + 1 : (long long)0x7fffffff;
+  long long hi = p.causal ? qp + p.q_len : (long long)0x7fffffff;
   if (lo < 0) lo = 0;
   if (hi > 0x7fffffff) hi = 0x7fffffff;
   e.lo = (int)lo;
   e.hi = (int)hi;
   if (empty) return flags;
-  if (KIND == KIND_PAGED) {
+  if (is_paged(KIND)) {
     long long vh = hi < L ? hi : L;
     e.hi = (int)vh;
     if (vh > lo) {
@@ -209,8 +211,8 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
   return flags;
 }
 
-// Shared-memory plan storage: 4 ints per sequence for paged kernels, the
-// whole SeqPlan for tiered ones.
+// Shared-memory plan storage: 4 ints per sequence for the one-token paged
+// kernel, the whole SeqPlan for the others.
 template <int KIND>
 struct PlanStore {
   uint8_t* base;
@@ -229,6 +231,7 @@ struct PlanStore {
       e.hi = s.hi;
       e.t0 = s.t0;
       e.ntiles = s.ntiles;
+      e.qp0 = s.hi - 1;  // (not used: one query token)
       e.ncold = s.ntiles;
       e.hot_start = e.hot_len = e.ha0 = e.ha1 = e.hb0 = e.hb1 = e.cold_len = 0;
     } else {
@@ -282,6 +285,32 @@ __device__ __forceinline__ int stream_grid(const KParams& p, long long T) {
   return (int)(T < p.grid ? T : p.grid);
 }
 __device__ __forceinline__ int units_per_seq(const KParams& p) { return (p.Hkv / p.KVB) * p.HG; }
+
+// Query rows (virtual heads) of head group hg of a kv head: kHeadTile, or
+// fewer in the last group.  Virtual head j = t*G + g is head g of the kv
+// head's group for query token t.
+__device__ __forceinline__ int unit_nh(const KParams& p, int hg) {
+  const int n = p.Gv - hg * kHeadTile;
+  return n < kHeadTile ? n : kHeadTile;
+}
+
+// Row of out / lse ([B, T, Hq]) of virtual head h of head group hg of kv head kv.
+template <int KIND>
+__device__ __forceinline__ long long out_row(const KParams& p, int b, int kv, int hg, int h) {
+  const int j = hg * kHeadTile + h;
+  if constexpr (KIND != KIND_PAGED_MULTI) {
+    return (long long)b * p.Hq + (long long)kv * p.G + j;  // one token
+  } else {
+    const int t = j / p.G, g = j - t * p.G;
+    return ((long long)b * p.q_len + t) * p.Hq + (long long)kv * p.G + g;
+  }
+}
+
+// Query row of q ([B, T, Hq, D]) for the same virtual head (the same index).
+template <int KIND>
+__device__ __forceinline__ long long q_row(const KParams& p, int b, int kv, int hg, int h) {
+  return out_row<KIND>(p, b, kv, hg, h);
+}
 
 // Sequence whose tile positions contain g: the largest b with pre[b] <= g.
 __device__ __forceinline__ int seq_of(const KParams& p, const int* pre, long long g) {
@@ -489,15 +518,24 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
         q_par = qn & 1;
       }
       if (lane == 0 && live) {
-        const uint32_t per = (uint32_t)(p.NH * D * 4);
-        mbar_arrive_expect_tx(qfull, per * KVB);
-        const float* qb = p.q + (long long)s.b * p.Hq * D;
-        if (p.HG == 1) {
-          bulk_load(qslot, qb + (long long)kv0 * p.G * D, per * KVB, qfull);
-        } else {
+        // slot layout [KVB][NH][D]; this unit fills nh rows per kv head
+        const int nh = unit_nh(p, s.hg);
+        const uint32_t row = (uint32_t)(D * 4);
+        const uint32_t per = (uint32_t)p.NH * row;
+        mbar_arrive_expect_tx(qfull, (uint32_t)(nh * KVB) * row);
+        if (KIND != KIND_PAGED_MULTI && p.HG == 1) {
+          // one token, one group: the unit's KVB x G rows are contiguous
+          bulk_load(qslot, p.q + q_row<KIND>(p, s.b, kv0, 0, 0) * D, (uint32_t)(nh * KVB) * row, qfull);
+        } else if (KIND != KIND_PAGED_MULTI) {
           for (int j = 0; j < KVB; ++j)
-            bulk_load(qslot + j * per, qb + ((long long)(kv0 + j) * p.G + s.hg * kHeadTile) * D, per,
-                      qfull);
+            bulk_load(qslot + j * per, p.q + q_row<KIND>(p, s.b, kv0 + j, s.hg, 0) * D,
+                      (uint32_t)nh * row, qfull);
+        } else {
+          // several tokens: rows of different tokens are Hq rows apart
+          for (int j = 0; j < KVB; ++j)
+            for (int h = 0; h < nh; ++h)
+              bulk_load(qslot + j * per + h * row, p.q + q_row<KIND>(p, s.b, kv0 + j, s.hg, h) * D, row,
+                        qfull);
         }
       }
       ++qn;
@@ -621,7 +659,7 @@ struct QFrag {
 // (2p, 2p+1) covers d = 4*(8p + r) + {0, 1, 2, 3}.
 template <int KIND>
 __device__ __forceinline__ int o_row_d(int mt, int r, int hi8) {
-  if constexpr (KIND == KIND_PAGED) {
+  if constexpr (is_paged(KIND)) {
     return 16 * mt + r + 8 * hi8;
   } else {
     return 4 * (8 * (mt >> 1) + r) + 2 * (mt & 1) + hi8;
@@ -639,7 +677,7 @@ __device__ __forceinline__ void load_q(uint32_t qs, int NH, float qscale, int r,
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     int d0, d2;
-    if constexpr (KIND == KIND_PAGED) {
+    if constexpr (is_paged(KIND)) {
       d0 = 16 * ks + 2 * c;
       d2 = d0 + 8;
     } else {
@@ -832,6 +870,15 @@ __device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, floa
   }
 }
 
+// Per-column masks of a multi-token query: the lane's two score columns
+// belong to query tokens whose own causal / window bounds [lo, hi) cut the
+// keys (absolute position kbase + tile key index).
+struct ColMask {
+  bool on;
+  int kbase;
+  int lo[2], hi[2];
+};
+
 // NG 16-key groups of this warp (keys k0[g] .. k0[g]+15) in one online-
 // softmax step: the QK products, one running-max update, then the PV
 // products.  v[2g], v[2g+1]: validity of keys k0[g]+r and k0[g]+r+8;
@@ -844,7 +891,8 @@ __device__ __forceinline__ void groups_compute(const RowMap& km, const RowMap& v
                                                const QFrag<D>& q, Acc<D>& a,
                                                const bool (&v)[2 * NG],
                                                const float (&ks)[2 * NG],
-                                               const float (&vs)[2 * NG]) {
+                                               const float (&vs)[2 * NG],
+                                               const ColMask& cm) {
   constexpr int NCH = NG == 1 ? 4 : 2;
   float s4[NG][NCH][4];
 #pragma unroll
@@ -869,6 +917,13 @@ __device__ __forceinline__ void groups_compute(const RowMap& km, const RowMap& v
     }
     if (!v[2 * g]) sc[g][0] = sc[g][1] = kNegInf;
     if (!v[2 * g + 1]) sc[g][2] = sc[g][3] = kNegInf;
+    if (cm.on) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int key = cm.kbase + k0[g] + (lane >> 2) + 8 * (j >> 1);
+        if (key < cm.lo[j & 1] || key >= cm.hi[j & 1]) sc[g][j] = kNegInf;
+      }
+    }
   }
   // ---- online softmax (base 2)
   float mx0 = fmaxf(sc[0][0], sc[0][2]), mx1 = fmaxf(sc[0][1], sc[0][3]);
@@ -943,11 +998,11 @@ __device__ __forceinline__ void groups_compute(const RowMap& km, const RowMap& v
 template <int TK, int D, bool PK>
 __device__ __forceinline__ void group_compute(const RowMap& km, const RowMap& vm, float softcap2,
                                               int k0, int lane, const QFrag<D>& q, Acc<D>& a,
-                                              bool vA, bool vB) {
+                                              bool vA, bool vB, const ColMask& cm) {
   const int k0s[1] = {k0};
   const bool v[2] = {vA, vB};
   const float one[2] = {1.f, 1.f};
-  groups_compute<TK, D, PK, 1>(km, vm, softcap2, k0s, lane, q, a, v, one, one);
+  groups_compute<TK, D, PK, 1>(km, vm, softcap2, k0s, lane, q, a, v, one, one, cm);
 }
 
 // Zeroes the f16 V rows of masked keys among k0..k0+15 of this warp's head,
@@ -1030,7 +1085,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   const int warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
   const int kvs = warp / TG, tg = warp % TG;
-  const int NH = p.NH;
+  const int nh = unit_nh(p, s.hg);  // query rows of this unit per kv head
   if constexpr (PK) {
     // fold the remainder columns (lane c ^ 2) into the f16-part columns;
     // both lanes of a pair then hold the same state
@@ -1056,12 +1111,12 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     named_bar_sync(kRedBarrier, NCW * 32);
   }
   const int kv = s.kvb * KVB + kvs;
-  const long long row0 = (long long)s.b * p.Hq + (long long)kv * p.G + s.hg * kHeadTile;
   if (tg == 0 && (!PK || c < 2)) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int h = 2 * c + j;
-      if (h >= NH) continue;
+      if (h >= nh) continue;
+      const long long orow = out_row<KIND>(p, s.b, kv, s.hg, h);
       const float L = a.l[j];
       const float inv = L > 0.f ? 1.f / L : 0.f;
       const float lse = (a.m[j] == kNegInf) ? kNegInf : (a.m[j] + log2f(L)) * kLn2;
@@ -1069,10 +1124,10 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
       float* ldst;
       long long ostride = 1;
       if (s.dest == DEST_OUT) {
-        dst = p.out + (row0 + h) * D;
-        ldst = p.lse ? p.lse + row0 + h : nullptr;
+        dst = p.out + orow * D;
+        ldst = p.lse ? p.lse + orow : nullptr;
       } else if (s.dest == DEST_SPLIT) {
-        const long long pr = (row0 + h) * p.max_splits + s.slot;
+        const long long pr = orow * p.max_splits + s.slot;
         dst = p.o_part + pr * D;
         ldst = p.lse_part + pr;
       } else {
@@ -1112,13 +1167,12 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     // One float4 of one head row per thread; the participants' states are
     // read in batches of eight (all loads in flight together) and folded
     // with a running log-sum-exp.
-    const long long urow0 = (long long)s.b * p.Hq + s.hg * kHeadTile;
     constexpr int D4 = D / 4;
     const int nk = c1 - c0 + 1;
-    for (int idx = tid; idx < KVB * NH * D4; idx += NCW * 32) {
+    for (int idx = tid; idx < KVB * nh * D4; idx += NCW * 32) {
       const int d4 = idx % D4;
       const int hh = idx / D4;
-      const int ks = hh / NH, h = hh % NH;
+      const int ks = hh / nh, h = hh % nh;
       const int rowoff = ks * kHeadTile + h;
       float M = kNegInf, Wsum = 0.f;
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1159,7 +1213,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
         o = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
         lse = M + logf(Wsum);
       }
-      const long long orow = urow0 + (long long)(s.kvb * KVB + ks) * p.G + h;
+      const long long orow = out_row<KIND>(p, s.b, s.kvb * KVB + ks, s.hg, h);
       reinterpret_cast<float4*>(p.out + orow * D)[d4] = o;
       if (d4 == 0 && p.lse) p.lse[orow] = lse;
     }
@@ -1192,10 +1246,11 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   if (p.sched != SCHED_SPLIT) {
     for (int b = blockIdx.x; b < p.B; b += p.grid) {
       if (plan.ntiles(b) != 0) continue;
-      for (int idx = tid; idx < p.Hq * D; idx += NCW * 32)
-        p.out[(long long)b * p.Hq * D + idx] = 0.f;
+      const long long rows = (long long)p.q_len * p.Hq;  // all tokens of sequence b
+      for (long long idx = tid; idx < rows * D; idx += NCW * 32)
+        p.out[(long long)b * rows * D + idx] = 0.f;
       if (p.lse)
-        for (int h = tid; h < p.Hq; h += NCW * 32) p.lse[(long long)b * p.Hq + h] = kNegInf;
+        for (long long h = tid; h < rows; h += NCW * 32) p.lse[(long long)b * rows + h] = kNegInf;
     }
   }
 
@@ -1211,12 +1266,11 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   while (seg_next<KIND, Gm::TOK>(p, plan, pre, it, s)) {
     if (s.i0 >= s.i1) {
       // SPLIT with no visible key: o = 0, lse = -inf
-      for (int idx = tid; idx < KVB * NH * D; idx += NCW * 32) {
+      const int nh = unit_nh(p, s.hg);
+      for (int idx = tid; idx < KVB * nh * D; idx += NCW * 32) {
         const int d = idx % D, hh = idx / D;
-        const int kv = s.kvb * KVB + hh / NH, h = hh % NH;
-        const long long pr =
-            ((long long)s.b * p.Hq + (long long)kv * p.G + s.hg * kHeadTile + h) * p.max_splits +
-            s.slot;
+        const int kv = s.kvb * KVB + hh / nh, h = hh % nh;
+        const long long pr = out_row<KIND>(p, s.b, kv, s.hg, h) * p.max_splits + s.slot;
         p.o_part[pr * D + d] = 0.f;
         if (d == 0) p.lse_part[pr] = kNegInf;
       }
@@ -1226,7 +1280,8 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
     const int kv = s.kvb * KVB + kvs;
     {
       if (!mbar_wait(qfull, qn & 1, abort_flag(misc), p.wait_ns) && lane == 0) note_abort(misc);
-      load_q<KIND, D, PK>(smem_u32(qslot + kvs * NH * D * 4), NH, qscale, r, c, q);
+      load_q<KIND, D, PK>(smem_u32(qslot + kvs * NH * D * 4), unit_nh(p, s.hg), qscale, r, c,
+                          q);
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty);
       ++qn;
@@ -1235,6 +1290,24 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
     for (int mt = 0; mt < D / 16; ++mt) a.o[mt][0] = a.o[mt][1] = a.o[mt][2] = a.o[mt][3] = 0.f;
     a.m[0] = a.m[1] = kNegInf;
     a.l[0] = a.l[1] = 0.f;
+    // several query tokens: the causal / window bounds of this lane's two
+    // score columns (padding columns take the last token's)
+    ColMask cm;
+    cm.on = KIND == KIND_PAGED_MULTI;  // the other kinds take one query token
+    cm.kbase = 0;
+    cm.lo[0] = cm.lo[1] = 0;
+    cm.hi[0] = cm.hi[1] = 0x7fffffff;
+    if (cm.on) {
+#pragma unroll
+      for (int col = 0; col < 2; ++col) {
+        const int head = (PK ? 2 * (c & 1) : 2 * c) + col;
+        int t = (s.hg * kHeadTile + head) / p.G;
+        t = t < p.q_len ? t : p.q_len - 1;
+        const long long qp = (long long)e.qp0 + t;
+        cm.lo[col] = (p.window > 0 && qp >= p.window) ? (int)(qp - p.window + 1) : 0;
+        cm.hi[col] = p.causal ? (int)(qp + 1) : 0x7fffffff;
+      }
+    }
     HotView hv;
     if constexpr (is_tiered(KIND)) {
       hv.W = p.hot_window;
@@ -1268,13 +1341,14 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
           const int j = bs <= Gm::TOK ? (k >> bg.log2R) : 0;
           return ((bad_mask >> j) & 1u) == 0;
         };
-        if constexpr (KIND == KIND_PAGED) {
+        if constexpr (is_paged(KIND)) {
           static_assert(Gm::GPW == 1, "one key group per warp in an f16 tile");
           const int k0 = 16 * tg;
           const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
           if (__any_sync(0xffffffffu, vA || vB)) {
             if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
-            group_compute<TK_PAGED, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB);
+            cm.kbase = tok0;
+            group_compute<TK_PAGED, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB, cm);
           }
         } else if constexpr (KIND == KIND_TIERED_F16) {
           // f16 cold rows, read like hot-ring rows (the tiered d order)
@@ -1283,7 +1357,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
           const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
           if (__any_sync(0xffffffffu, vA || vB)) {
             if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
-            group_compute<TK_HOT, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB);
+            group_compute<TK_HOT, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB, cm);
           }
         } else {
           // both key groups of the warp in one softmax step (int8 values are
@@ -1301,7 +1375,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
               ks[i] = __half2float(__ushort_as_half(lds16(sck + off)));
               vs[i] = __half2float(__ushort_as_half(lds16(scv + off)));
             }
-            groups_compute<TK_COLD, D, PK, 2>(km, vm, softcap2, k0, lane, q, a, v, ks, vs);
+            groups_compute<TK_COLD, D, PK, 2>(km, vm, softcap2, k0, lane, q, a, v, ks, vs, cm);
           }
         }
       } else if constexpr (is_tiered(KIND)) {
@@ -1318,7 +1392,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
         if (__any_sync(0xffffffffu, vA || vB)) {
           if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
-          group_compute<TK_HOT, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB);
+          group_compute<TK_HOT, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB, cm);
         }
       }
       __syncwarp();

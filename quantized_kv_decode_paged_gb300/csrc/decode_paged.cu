@@ -12,6 +12,16 @@ cudaError_t launch_paged_unpacked(int D, int KVB, const KParams& p, dim3 grid, i
 
 GeoInfo decode_geo(int kind, int D, int KVB) {
   GeoInfo g{0, 0, 0, 0, 0};
+  if (kind == KIND_PAGED_MULTI) {
+    if (D == 64 && KVB == 1) return geo_info<KIND_PAGED_MULTI, 64, 1>();
+    if (D == 64 && KVB == 2) return geo_info<KIND_PAGED_MULTI, 64, 2>();
+    if (D == 64 && KVB == 4) return geo_info<KIND_PAGED_MULTI, 64, 4>();
+    if (D == 128 && KVB == 1) return geo_info<KIND_PAGED_MULTI, 128, 1>();
+    if (D == 128 && KVB == 2) return geo_info<KIND_PAGED_MULTI, 128, 2>();
+    if (D == 128 && KVB == 4) return geo_info<KIND_PAGED_MULTI, 128, 4>();
+    if (D == 256 && KVB == 1) return geo_info<KIND_PAGED_MULTI, 256, 1>();
+    return g;
+  }
   if (kind == KIND_TIERED_F16) {
     if (D == 64 && KVB == 1) return geo_info<KIND_TIERED_F16, 64, 1>();
     if (D == 64 && KVB == 2) return geo_info<KIND_TIERED_F16, 64, 2>();
@@ -48,6 +58,9 @@ cudaError_t launch_decode(int kind, int D, int KVB, bool packed, const KParams& 
   if (kind == KIND_TIERED_F16)
     return packed ? launch_tiered_f16_packed(D, KVB, p, grid, smem, stream)
                   : launch_tiered_f16_unpacked(D, KVB, p, grid, smem, stream);
+  if (kind == KIND_PAGED_MULTI)
+    return packed ? launch_paged_multi_packed(D, KVB, p, grid, smem, stream)
+                  : launch_paged_multi_unpacked(D, KVB, p, grid, smem, stream);
   return packed ? launch_paged_packed(D, KVB, p, grid, smem, stream)
                 : launch_paged_unpacked(D, KVB, p, grid, smem, stream);
 }

@@ -14,10 +14,14 @@ constexpr int kMaxBatchPerLaunch = 256;  // per-sequence plan lives in shared me
 constexpr int kSmemLimit = 232448;       // 227 KB opt-in per block on sm_100-class parts
 constexpr uint32_t kRedBarrier = 1;      // named barrier id for the consumer warps
 
-// PAGED: f16 pages.  TIERED: int8 cold pages (+ f16 scales) and an f16 hot
-// ring.  TIERED_F16: f16 cold pages and an f16 hot ring.
-enum Kind : int { KIND_PAGED = 0, KIND_TIERED = 1, KIND_TIERED_F16 = 2 };
-__host__ __device__ constexpr bool is_tiered(int kind) { return kind != KIND_PAGED; }
+// PAGED: f16 pages, one query token per sequence.  PAGED_MULTI: f16 pages,
+// several query tokens per sequence.  TIERED: int8 cold pages (+ f16
+// scales) and an f16 hot ring.  TIERED_F16: f16 cold pages and an f16 hot ring.
+enum Kind : int { KIND_PAGED = 0, KIND_TIERED = 1, KIND_TIERED_F16 = 2, KIND_PAGED_MULTI = 3 };
+__host__ __device__ constexpr bool is_paged(int kind) {
+  return kind == KIND_PAGED || kind == KIND_PAGED_MULTI;
+}
+__host__ __device__ constexpr bool is_tiered(int kind) { return !is_paged(kind); }
 __host__ __device__ constexpr bool cold_int8(int kind) { return kind == KIND_TIERED; }
 // STREAM: every CTA takes an equal share of the concatenated key tiles of all
 //         units; units cut between CTAs are merged by the last CTA to finish.
@@ -80,8 +84,10 @@ struct alignas(128) KParams {
 
   int B, Hq, Hkv, D;
   int G;        // Hq / Hkv
-  int NH;       // heads per kv head in a unit: min(G, kHeadTile)
-  int HG;       // head groups per kv head: ceil(G / kHeadTile)
+  int q_len;    // query tokens per sequence (T); q, out are [B, T, Hq, D]
+  int Gv;       // query rows per kv head: T * G ("virtual heads", token-major)
+  int NH;       // Q-slot rows per kv head: min(Gv, kHeadTile)
+  int HG;       // head groups per kv head: ceil(Gv / kHeadTile); the last may be partial
   int KVB;      // kv heads per unit (equals the instantiation's KVB)
   int bs, log2_bs, max_blocks, num_blocks;
   float qscale;     // scale * log2(e): scores are kept in base-2 units
@@ -125,7 +131,8 @@ struct alignas(128) KParams {
 // Per-sequence plan entries kept in shared memory (paged kernels use the
 // first four fields only).
 struct SeqPlan {
-  int lo, hi;    // visible absolute key positions [lo, hi)
+  int lo, hi;    // visible absolute key positions [lo, hi) (union over the query tokens)
+  int qp0;       // position of query token 0
   int t0;        // first paged / cold tile
   int ntiles;    // tiles per unit
   // tiered only
@@ -174,7 +181,7 @@ __host__ __device__ inline SmemLayout make_layout(int kind, int D, int KVB, int 
   L.off_red = off;
   off += (W / 2) * red_floats(D) * 4;
   L.off_plan = off;
-  off += B * (is_tiered(kind) ? (int)sizeof(SeqPlan) : (int)sizeof(SeqPlanPaged));
+  off += B * (kind == KIND_PAGED ? (int)sizeof(SeqPlanPaged) : (int)sizeof(SeqPlan));
   L.off_pre = off;
   off += (B + 1) * 4;
   off = align_up(off, 8);

@@ -67,6 +67,19 @@ cudaError_t launch_tiered_f16_pk(int D, int KVB, const KParams& p, dim3 grid, in
   return cudaErrorInvalidValue;
 }
 
+template <bool PK>
+cudaError_t launch_paged_multi_pk(int D, int KVB, const KParams& p, dim3 grid, int smem,
+                                  cudaStream_t stream) {
+  if (D == 64 && KVB == 1) return launch_decode_impl<KIND_PAGED_MULTI, 64, 1, PK>(p, grid, smem, stream);
+  if (D == 64 && KVB == 2) return launch_decode_impl<KIND_PAGED_MULTI, 64, 2, PK>(p, grid, smem, stream);
+  if (D == 64 && KVB == 4) return launch_decode_impl<KIND_PAGED_MULTI, 64, 4, PK>(p, grid, smem, stream);
+  if (D == 128 && KVB == 1) return launch_decode_impl<KIND_PAGED_MULTI, 128, 1, PK>(p, grid, smem, stream);
+  if (D == 128 && KVB == 2) return launch_decode_impl<KIND_PAGED_MULTI, 128, 2, PK>(p, grid, smem, stream);
+  if (D == 128 && KVB == 4) return launch_decode_impl<KIND_PAGED_MULTI, 128, 4, PK>(p, grid, smem, stream);
+  if (D == 256 && KVB == 1) return launch_decode_impl<KIND_PAGED_MULTI, 256, 1, PK>(p, grid, smem, stream);
+  return cudaErrorInvalidValue;
+}
+
 // Defined in the instantiating translation units.
 cudaError_t launch_paged_unpacked(int D, int KVB, const KParams& p, dim3 grid, int smem,
                                   cudaStream_t stream);
@@ -76,6 +89,10 @@ cudaError_t launch_tiered_unpacked(int D, int KVB, const KParams& p, dim3 grid, 
                                    cudaStream_t stream);
 cudaError_t launch_tiered_packed(int D, int KVB, const KParams& p, dim3 grid, int smem,
                                  cudaStream_t stream);
+cudaError_t launch_paged_multi_unpacked(int D, int KVB, const KParams& p, dim3 grid, int smem,
+                                        cudaStream_t stream);
+cudaError_t launch_paged_multi_packed(int D, int KVB, const KParams& p, dim3 grid, int smem,
+                                      cudaStream_t stream);
 cudaError_t launch_tiered_f16_unpacked(int D, int KVB, const KParams& p, dim3 grid, int smem,
                                        cudaStream_t stream);
 cudaError_t launch_tiered_f16_packed(int D, int KVB, const KParams& p, dim3 grid, int smem,

@@ -176,7 +176,8 @@ def _assign_pages(rng, B, pages_needed, num_blocks, max_blocks):
 
 def make_paged(name, seed, B, Hq, Hkv, D, block_size, seq_lens, num_blocks=None,
                max_blocks=None, scale=0.0, softcap=0.0, sliding_window=0, causal=True,
-               q_pos=None, outlier_rate=0.0, nonfinite_tail=False) -> PagedCase:
+               q_pos=None, outlier_rate=0.0, nonfinite_tail=False, q_len=1) -> PagedCase:
+    """q_len > 1 draws q [B, q_len, Hq, D] (several query tokens per sequence)."""
     seq_lens = np.asarray(seq_lens, dtype=np.int32).reshape(B)
     pages = np.array([(max(int(L), 0) + block_size - 1) // block_size for L in seq_lens],
                      dtype=np.int64)
@@ -186,7 +187,8 @@ def make_paged(name, seed, B, Hq, Hkv, D, block_size, seq_lens, num_blocks=None,
         num_blocks = max(1, int(pages.sum()))
     meta = _rng(seed, _GLOBAL, _S_META)
     table = _assign_pages(meta, B, pages, num_blocks, max_blocks)
-    q = _rng(seed, _GLOBAL, _S_Q).standard_normal((B, Hq, D), dtype=np.float32)
+    qshape = (B, Hq, D) if q_len == 1 else (B, q_len, Hq, D)
+    q = _rng(seed, _GLOBAL, _S_Q).standard_normal(qshape, dtype=np.float32)
     return PagedCase(name=name, seed=seed, B=B, Hq=Hq, Hkv=Hkv, D=D, block_size=block_size,
                      num_blocks=int(num_blocks), q=q, block_table=table, seq_lens=seq_lens,
                      scale=scale, softcap=softcap, sliding_window=sliding_window,

@@ -29,7 +29,8 @@ def assert_parity(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
 
 
 def oracle_paged(case, rows=None):
-    seqs = None if rows is None else sorted({int(r) // case.Hq for r in rows})
+    T = case.q.shape[1] if case.q.ndim == 4 else 1  # query tokens per sequence
+    seqs = None if rows is None else sorted({int(r) // (T * case.Hq) for r in rows})
     kp, vp = case.host_pools(seqs)
     return oracle.decode_paged(case.q, kp, vp, case.block_table, case.seq_lens, case.q_pos,
                                scale=case.scale, softcap=case.softcap,
@@ -43,7 +44,13 @@ def run_paged(case, t, mode, split_tokens=256, dev_status=None):
     import torch
     kw = dict(scale=case.scale, softcap=case.softcap, sliding_window=case.sliding_window,
               causal=case.causal)
-    if mode in ("stream", "units"):
+    if t["q"].dim() == 4:
+        assert mode in ("stream", "units")
+        out, lse = qk.decode_attn_paged_multi(
+            t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], t["q_pos"],
+            max_seq_len=case.max_seq_len, workspace="auto" if mode == "stream" else None,
+            dev_status=dev_status, **kw)
+    elif mode in ("stream", "units"):
         out, lse = qk.decode_attn_paged(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
                                         t["seq_lens"], t["q_pos"], max_seq_len=case.max_seq_len,
                                         workspace="auto" if mode == "stream" else None,
