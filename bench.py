@@ -152,7 +152,8 @@ def describe(case):
     from quantized_kv_decode_paged_gb300.workloads import PagedCase
     if isinstance(case, PagedCase):
         lens = case.seq_lens
-        return {"workload": case.name, "kind": "paged f16", "B": case.B, "Hq": case.Hq,
+        T = case.q.shape[1] if case.q.ndim == 4 else 1
+        return {"workload": case.name, "kind": "paged f16", "B": case.B, "q_len": T, "Hq": case.Hq,
                 "Hkv": case.Hkv, "D": case.D, "block_size": case.block_size,
                 "num_blocks": case.num_blocks, "seq_len_min": int(lens.min()),
                 "seq_len_max": int(lens.max()), "seq_len_mean": float(lens.mean()),
@@ -172,15 +173,20 @@ def make_step(case, t):
     out = torch.empty((case.B, case.Hq, case.D), dtype=torch.float32, device="cuda")
     lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
     if isinstance(case, PagedCase):
-        params = qk.make_params(t["q"], case.block_size, case.Hkv, case.max_blocks,
-                                case.num_blocks, scale=case.scale, softcap=case.softcap,
-                                sliding_window=case.sliding_window, causal=case.causal,
-                                max_seq_len=case.max_seq_len)
+        multi = case.q.ndim == 4  # several query tokens per sequence
+        if multi:
+            out = torch.empty(case.q.shape, dtype=torch.float32, device="cuda")
+            lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
+        params = qk.make_params(t["q"][:, 0] if multi else t["q"], case.block_size, case.Hkv,
+                                case.max_blocks, case.num_blocks, scale=case.scale,
+                                softcap=case.softcap, sliding_window=case.sliding_window,
+                                causal=case.causal, max_seq_len=case.max_seq_len)
         nbytes = qk.decode_attn_workspace_size(params)
         ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+        fn = qk.decode_attn_paged_multi if multi else qk.decode_attn_paged
 
         def step(q=None, block_table=None, seq_lens=None):
-            return qk.decode_attn_paged(
+            return fn(
                 t["q"] if q is None else q, t["k_pool"], t["v_pool"],
                 t["block_table"] if block_table is None else block_table,
                 t["seq_lens"] if seq_lens is None else seq_lens, t["q_pos"],
@@ -229,18 +235,21 @@ def oracle_sample(case, target_s, max_units=None):
     if max_units is not None:
         order = order[:max_units]
     is_paged = isinstance(case, PagedCase)
+    T = case.q.shape[1] if case.q.ndim == 4 else 1  # query tokens per sequence
 
     def unit_bytes(b):
         if is_paged:
             L = int(case.seq_lens[b])
-            lo, hi = visible_range(L, L - 1, case.causal, case.sliding_window)
-            return max(0, hi - lo) * case.D * 2 * 2 + G * case.D * 8
+            lo, _ = visible_range(L, L - T, case.causal, case.sliding_window)
+            _, hi = visible_range(L, L - 1, case.causal, case.sliding_window)
+            return max(0, hi - lo) * case.D * 2 * 2 + T * G * case.D * 8
         cl, hl = int(case.cold_lens[b]), int(case.hot_lens[b])
         cold_row = case.D * 4 if case.cold_f16 else case.D * 2 + 4
         return cl * cold_row + hl * case.D * 4 + G * case.D * 8
 
     def run(sel):
-        rows = np.array([b * case.Hq + kv * G + g for (b, kv) in sel for g in range(G)])
+        rows = np.array([(b * T + t) * case.Hq + kv * G + g for (b, kv) in sel
+                         for t in range(T) for g in range(G)])
         seqs = sorted({b for b, _ in sel})
         if is_paged:
             kp, vp = case.host_pools(seqs)
@@ -491,7 +500,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["tiny", "paged", "tiered", "window", "longctx", "paged_compact",
-                             "tiered_f16"])
+                             "tiered_f16", "paged_spec2", "paged_spec4"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0,

@@ -23,18 +23,21 @@ def algorithmic_bytes(case) -> dict:
     and their scales for the cold tier), the block-table entries of the
     visible pages, Q, out, lse and the length arrays."""
     if isinstance(case, PagedCase):
+        T = case.q.shape[1] if case.q.ndim == 4 else 1  # query tokens per sequence
         kv = 0
         bt = 0
         for b in range(case.B):
             L = int(case.seq_lens[b])
-            qp = int(case.q_pos[b]) if case.q_pos is not None else L - 1
-            lo, hi = visible_range(L, qp, case.causal, case.sliding_window)
+            qp = int(case.q_pos[b]) if case.q_pos is not None else L - T
+            # union of the tokens' ranges: token 0's lower bound, token T-1's upper
+            lo, _ = visible_range(L, qp, case.causal, case.sliding_window)
+            _, hi = visible_range(L, qp + T - 1, case.causal, case.sliding_window)
             n = max(0, hi - lo)
             kv += n * case.Hkv * case.D * 2 * 2
             if n:
                 bs = case.block_size
                 bt += ((hi - 1) // bs - lo // bs + 1) * 4
-        io = case.B * case.Hq * case.D * 4 * 2 + case.B * case.Hq * 4 + case.B * 4
+        io = T * (case.B * case.Hq * case.D * 4 * 2 + case.B * case.Hq * 4) + case.B * 4
         return dict(kv=kv, table=bt, io=io, total=kv + bt + io)
     kv = 0
     bt = 0

@@ -20,6 +20,8 @@ Workloads (the shapes of the pages' serving cases):
 * ``longctx``   B=128, Hq=64, Hkv=8, D=128, L ~ lognormal(median 8192, sigma 0.8)
                 clamped to [128, 32768], bs=16, pool exactly filled and shuffled
 * ``tiered_f16`` the ``tiered`` shape with the 7168 cold keys kept as f16 rows
+* ``paged_spec2``, ``paged_spec4`` the ``paged`` shape with 2 or 4 query tokens per
+                sequence (speculative decode)
 """
 from __future__ import annotations
 
@@ -35,7 +37,8 @@ import numpy as np
 _S_K, _S_V, _S_OUTLIER, _S_Q, _S_META = 0, 1, 2, 3, 4
 _GLOBAL = 1 << 30  # "sequence" index used for batch-wide draws
 
-WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx", "tiered_f16")
+WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx", "tiered_f16", "paged_spec2",
+             "paged_spec4")
 # Same keys and values as "paged", in a pool holding exactly the used pages
 # (about 310 MB instead of 4 GiB of device memory): for profiler captures.
 VARIANTS = ("paged_compact",)
@@ -216,6 +219,12 @@ def workload(name: str):
     if name == "tiered":
         return make_tiered("tiered", 2, B=16, Hq=32, Hkv=8, D=128, block_size=16,
                            cold_len=7168, hot_len=1024, hot_window=1024, hot_start=7168)
+    if name in ("paged_spec2", "paged_spec4"):
+        # the paged workload with 2 or 4 query tokens per sequence (speculative decode)
+        meta = _rng(1, _GLOBAL, _S_META + 1)
+        lens = meta.integers(512, 4096, size=32, endpoint=True)
+        return make_paged(name, 1, B=32, Hq=32, Hkv=8, D=128, block_size=16, seq_lens=lens,
+                          num_blocks=65536, max_blocks=256, q_len=int(name[-1]))
     if name == "tiered_f16":
         return make_tiered("tiered_f16", 2, B=16, Hq=32, Hkv=8, D=128, block_size=16,
                            cold_len=7168, hot_len=1024, hot_window=1024, hot_start=7168,
