@@ -105,6 +105,30 @@ int kvb_override(int kind, int D, int Hkv, int kvb) {
   return kvb;
 }
 
+// Units of (kv heads x head groups).  With more than one head group per kv
+// head (more than kHeadTile query rows per kv head), a unit takes all of a
+// kv head's head groups when there are 2 or 4 of them: the four warp slots
+// of a KVB = 4 instantiation then split as KVU kv heads x HGU head groups
+// (KVU * HGU = 4) and every K/V byte serves all the kv head's query rows
+// (read once instead of HG times).  DA_FUSE_HG=0 in the environment keeps
+// one head group per unit (a tuning and testing knob).
+void plan_units(KParams& k, int kind) {
+  k.KVU = k.KVB;
+  k.HGU = 1;
+  k.hgu_shift = 0;
+  k.HGN = k.HG;
+  const char* e = getenv("DA_FUSE_HG");
+  if (e && e[0] == '0' && e[1] == '\0') return;
+  if (k.HG != 2 && k.HG != 4) return;
+  const int kvu = 4 / k.HG;
+  if (k.Hkv % kvu != 0 || da::decode_geo(kind, k.D, 4).W == 0) return;
+  k.KVB = 4;
+  k.KVU = kvu;
+  k.HGU = k.HG;
+  k.hgu_shift = k.HG == 2 ? 1 : 2;
+  k.HGN = 1;
+}
+
 // Whether to launch the packed variant: at most four query heads per kv
 // head leave half of the MMA's eight columns free for the remainder parts.
 // DA_PACK=0 in the environment forces the unpacked variant (a tuning and
@@ -158,6 +182,7 @@ void fill_common(KParams& k, const da_params* p) {
   k.causal = p->causal;
   k.KVB = da::decode_kvb(da::KIND_PAGED, p->head_dim, p->num_kv_heads);
   k.KVB = kvb_override(da::KIND_PAGED, p->head_dim, p->num_kv_heads, k.KVB);
+  plan_units(k, da::KIND_PAGED);
   k.wait_ns = wait_limit_ns();
   k.test_skip_arm = test_skip_arm();
 }
@@ -165,7 +190,8 @@ void fill_common(KParams& k, const da_params* p) {
 int encode_pool_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
                     long long D, long long heads, long long rows, int box_rows, int kvb);
 
-// K/V pool maps of a paged / cold cache (f16, or int8 words) for the chosen KVB.
+// K/V pool maps of a paged / cold cache (f16, or int8 words): boxes of the
+// unit's KVU kv heads.
 int encode_paged_maps(KParams& k, int kind, const void* kp, const void* vp, const da_params* p) {
   const da::GeoInfo g = da::decode_geo(kind, p->head_dim, k.KVB);
   if (g.W == 0) return DA_ERR_UNSUPPORTED;
@@ -175,10 +201,10 @@ int encode_paged_maps(KParams& k, int kind, const void* kp, const void* vp, cons
       da::cold_int8(kind) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
   const int esize = da::cold_int8(kind) ? 1 : 2;
   int st = encode_pool_map(&k.tm_k, kp, dt, esize, p->head_dim, p->num_kv_heads, rows, box_rows,
-                           k.KVB);
+                           k.KVU);
   if (st != DA_OK) return st;
   return encode_pool_map(&k.tm_v, vp, dt, esize, p->head_dim, p->num_kv_heads, rows, box_rows,
-                         k.KVB);
+                         k.KVU);
 }
 
 // 4-D map over a paged pool [rows, Hkv, D] of esize-byte elements with the
@@ -234,10 +260,13 @@ int max_stages() {
 }
 
 // Largest stage count (>= 2) whose layout fits in shared memory, or 0.
-int pick_stages(int kind, int D, int KVB, const da::GeoInfo& g, int NH, int Hkv, int nplan,
-                int* smem_out) {
+// A stage holds the K and V of the unit's KVU kv heads: REGION >> hgu_shift
+// bytes each.
+int pick_stages(int kind, int D, int KVB, const da::GeoInfo& g, int hgu_shift, int NH, int Hkv,
+                int nplan, int* smem_out) {
   for (int s = max_stages(); s >= 2; --s) {
-    SmemLayout L = da::make_layout(kind, D, KVB, g.W, g.REGION, g.TOK, NH, Hkv, s, nplan);
+    SmemLayout L = da::make_layout(kind, D, KVB, g.W, g.REGION >> hgu_shift, g.TOK, NH, Hkv, s,
+                                   nplan);
     if (L.total <= da::kSmemLimit) {
       *smem_out = L.total;
       return s;
@@ -264,12 +293,18 @@ WsLayout ws_layout(int grid, int D, int kvb) {
   return w;
 }
 
-// kv heads per unit the workspace must serve (either cache kind).
+// Warp slots per unit the workspace must serve (any cache kind, any number
+// of query tokens): the chosen KVB, or up to 4 when head groups share a unit.
 int ws_kvb(const da_params* p) {
   const int D = p->head_dim, H = p->num_kv_heads;
   int m = 0;
   for (int kind : {da::KIND_PAGED, da::KIND_TIERED, da::KIND_TIERED_F16, da::KIND_PAGED_MULTI}) {
-    const int v = kvb_override(kind, D, H, da::decode_kvb(kind, D, H));
+    int v = kvb_override(kind, D, H, da::decode_kvb(kind, D, H));
+    for (int f = 4; f > v; f /= 2)
+      if (da::decode_geo(kind, D, f).W != 0) {
+        v = f;
+        break;
+      }
     m = v > m ? v : m;
   }
   return m;
@@ -307,11 +342,11 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
     KParams k = base;
     k.B = nb;
     offset_chunk(k, b0);
-    const int units = nb * (k.Hkv / k.KVB) * k.HG;
+    const int units = nb * (k.Hkv / k.KVU) * k.HGN;
     const da::GeoInfo g = da::decode_geo(lc.kind, k.D, k.KVB);
     if (g.W == 0) return DA_ERR_UNSUPPORTED;
     int smem = 0;
-    k.stages = pick_stages(lc.kind, k.D, k.KVB, g, k.NH, k.Hkv, nb, &smem);
+    k.stages = pick_stages(lc.kind, k.D, k.KVB, g, k.hgu_shift, k.NH, k.Hkv, nb, &smem);
     if (k.stages == 0) return DA_ERR_UNSUPPORTED;
     int grid;
     if (use_ws) {
@@ -375,16 +410,17 @@ int tiered_impl(int kind, const da_params* p, const da_tier_params* t, const flo
   fill_common(k, p);
   k.KVB = kvb_override(kind, p->head_dim, p->num_kv_heads,
                        da::decode_kvb(kind, p->head_dim, p->num_kv_heads));
+  plan_units(k, kind);
   st = encode_paged_maps(k, kind, k_cold, v_cold, p);
   if (st != DA_OK) return st;
   {
     const da::GeoInfo g = da::decode_geo(kind, k.D, k.KVB);
     if (g.W == 0) return DA_ERR_UNSUPPORTED;
     st = encode_ring_map(&k.tm_kh, k_hot, p->head_dim, p->num_kv_heads, t->hot_capacity,
-                         p->batch, g.TOKH, k.KVB);
+                         p->batch, g.TOKH, k.KVU);
     if (st != DA_OK) return st;
     st = encode_ring_map(&k.tm_vh, v_hot, p->head_dim, p->num_kv_heads, t->hot_capacity,
-                         p->batch, g.TOKH, k.KVB);
+                         p->batch, g.TOKH, k.KVU);
     if (st != DA_OK) return st;
   }
   k.dev_status = dev_status;
@@ -436,6 +472,7 @@ int paged_impl(const da_params* p, int T, const float* q, const uint16_t* k_pool
   const int kind = T > 1 ? da::KIND_PAGED_MULTI : da::KIND_PAGED;
   k.KVB = kvb_override(kind, p->head_dim, p->num_kv_heads,
                        da::decode_kvb(kind, p->head_dim, p->num_kv_heads));
+  plan_units(k, kind);
   st = encode_paged_maps(k, kind, k_pool, v_pool, p);
   if (st != DA_OK) return st;
   k.dev_status = dev_status;
@@ -530,12 +567,12 @@ int decode_attn_split_partial(const da_params* p, int32_t split_tokens, int32_t 
   const da::GeoInfo g = da::decode_geo(da::KIND_PAGED, k.D, k.KVB);
   if (g.W == 0) return DA_ERR_UNSUPPORTED;
   int smem = 0;
-  k.stages = pick_stages(da::KIND_PAGED, k.D, k.KVB, g, k.NH, k.Hkv, 1, &smem);
+  k.stages = pick_stages(da::KIND_PAGED, k.D, k.KVB, g, k.hgu_shift, k.NH, k.Hkv, 1, &smem);
   if (k.stages == 0) return DA_ERR_UNSUPPORTED;
-  const long long units_total = (long long)p->batch * (k.Hkv / k.KVB) * k.HG;
+  const long long units_total = (long long)p->batch * (k.Hkv / k.KVU) * k.HGN;
   const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
   // grid.y is limited to 65535 units per launch: chunk whole sequences
-  const int upb = (k.Hkv / k.KVB) * k.HG;
+  const int upb = (k.Hkv / k.KVU) * k.HGN;
   const int seqs_per_launch = 65535 / upb > 0 ? 65535 / upb : 1;
   if (upb > 65535) return DA_ERR_UNSUPPORTED;
   (void)units_total;

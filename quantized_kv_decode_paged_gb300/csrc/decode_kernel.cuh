@@ -284,7 +284,7 @@ __device__ __forceinline__ long long stream_start(int c, long long T, int grid) 
 __device__ __forceinline__ int stream_grid(const KParams& p, long long T) {
   return (int)(T < p.grid ? T : p.grid);
 }
-__device__ __forceinline__ int units_per_seq(const KParams& p) { return (p.Hkv / p.KVB) * p.HG; }
+__device__ __forceinline__ int units_per_seq(const KParams& p) { return (p.Hkv / p.KVU) * p.HGN; }
 
 // Query rows (virtual heads) of head group hg of a kv head: kHeadTile, or
 // fewer in the last group.  Virtual head j = t*G + g is head g of the kv
@@ -292,6 +292,25 @@ __device__ __forceinline__ int units_per_seq(const KParams& p) { return (p.Hkv /
 __device__ __forceinline__ int unit_nh(const KParams& p, int hg) {
   const int n = p.Gv - hg * kHeadTile;
   return n < kHeadTile ? n : kHeadTile;
+}
+
+// kv head and head group of warp slot ks of a unit (kv-head block kvb, first
+// head group hg0).  Only the four-slot instantiations share a unit between
+// head groups; the others keep one head group per unit at compile time.
+template <int KVB>
+__device__ __forceinline__ int hgu_shift(const KParams& p) {
+  if constexpr (KVB == 4) return p.hgu_shift;
+  else return 0;
+}
+template <int KVB>
+__device__ __forceinline__ int slot_kv(const KParams& p, int kvb, int ks) {
+  if constexpr (KVB == 4) return kvb * p.KVU + (ks >> p.hgu_shift);
+  else return kvb * KVB + ks;
+}
+template <int KVB>
+__device__ __forceinline__ int slot_hg(const KParams& p, int hg0, int ks) {
+  if constexpr (KVB == 4) return hg0 + (ks & (p.HGU - 1));
+  else return hg0;
 }
 
 // Row of out / lse ([B, T, Hq]) of virtual head h of head group hg of kv head kv.
@@ -378,8 +397,8 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
     const int uib = (int)(local / nt);
     s.b = b;
     s.pidx = b;
-    s.kvb = uib / p.HG;
-    s.hg = uib % p.HG;
+    s.kvb = uib / p.HGN;
+    s.hg = (uib % p.HGN) * p.HGU;
     s.unit = b * upb + uib;
     s.i0 = (int)(local % nt);
     const long long rem = end - g;
@@ -406,8 +425,8 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
       const int uib = u % upb;
       s.b = b;
       s.pidx = b;
-      s.kvb = uib / p.HG;
-      s.hg = uib % p.HG;
+      s.kvb = uib / p.HGN;
+      s.hg = (uib % p.HGN) * p.HGU;
       s.unit = u;
       s.i0 = 0;
       s.i1 = e.ntiles;
@@ -429,8 +448,8 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
   const SeqPlan e = plan.get(0);
   s.b = b;
   s.pidx = 0;
-  s.kvb = uib / p.HG;
-  s.hg = uib % p.HG;
+  s.kvb = uib / p.HGN;
+  s.hg = (uib % p.HGN) * p.HGU;
   s.unit = u;
   s.dest = DEST_SPLIT;
   s.slot = blockIdx.x;
@@ -507,9 +526,9 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
   while (seg_next<KIND, Gm::TOK>(p, plan, pre, it, s)) {
     if (s.i0 >= s.i1) continue;
     const SeqPlan e = plan.get(s.pidx);
-    const int kv0 = s.kvb * KVB;
+    const int kv0 = s.kvb * (KVB >> hgu_shift<KVB>(p));  // first kv head of the unit's boxes
     const int* bt_row = p.block_table + (long long)s.b * max_blocks;
-    // ---- Q rows of the unit (KVB x NH heads) into the Q slot
+    // ---- Q rows of the unit (KVB slots x NH heads) into the Q slot
     {
       if (!mbar_wait(qempty, (qn & 1) ^ 1, abort_flag(misc), p.wait_ns) && lane == 0) note_abort(misc);
       const bool live = !__any_sync(0xffffffffu, *abort_flag(misc) != 0);
@@ -518,24 +537,32 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
         q_par = qn & 1;
       }
       if (lane == 0 && live) {
-        // slot layout [KVB][NH][D]; this unit fills nh rows per kv head
-        const int nh = unit_nh(p, s.hg);
+        // slot layout [KVB][NH][D]; slot j takes the nh rows of its
+        // (kv head, head group)
         const uint32_t row = (uint32_t)(D * 4);
         const uint32_t per = (uint32_t)p.NH * row;
-        mbar_arrive_expect_tx(qfull, (uint32_t)(nh * KVB) * row);
         if (KIND != KIND_PAGED_MULTI && p.HG == 1) {
           // one token, one group: the unit's KVB x G rows are contiguous
+          const int nh = unit_nh(p, 0);
+          mbar_arrive_expect_tx(qfull, (uint32_t)(nh * KVB) * row);
           bulk_load(qslot, p.q + q_row<KIND>(p, s.b, kv0, 0, 0) * D, (uint32_t)(nh * KVB) * row, qfull);
-        } else if (KIND != KIND_PAGED_MULTI) {
-          for (int j = 0; j < KVB; ++j)
-            bulk_load(qslot + j * per, p.q + q_row<KIND>(p, s.b, kv0 + j, s.hg, 0) * D,
-                      (uint32_t)nh * row, qfull);
         } else {
-          // several tokens: rows of different tokens are Hq rows apart
-          for (int j = 0; j < KVB; ++j)
-            for (int h = 0; h < nh; ++h)
-              bulk_load(qslot + j * per + h * row, p.q + q_row<KIND>(p, s.b, kv0 + j, s.hg, h) * D, row,
-                        qfull);
+          int rows = 0;
+          for (int j = 0; j < KVB; ++j) rows += unit_nh(p, slot_hg<KVB>(p, s.hg, j));
+          mbar_arrive_expect_tx(qfull, (uint32_t)rows * row);
+          for (int j = 0; j < KVB; ++j) {
+            const int kv = slot_kv<KVB>(p, s.kvb, j), hg = slot_hg<KVB>(p, s.hg, j);
+            const int nh = unit_nh(p, hg);
+            if (KIND != KIND_PAGED_MULTI) {
+              bulk_load(qslot + j * per, p.q + q_row<KIND>(p, s.b, kv, hg, 0) * D,
+                        (uint32_t)nh * row, qfull);
+            } else {
+              // several tokens: rows of different tokens are Hq rows apart
+              for (int h = 0; h < nh; ++h)
+                bulk_load(qslot + j * per + h * row, p.q + q_row<KIND>(p, s.b, kv, hg, h) * D, row,
+                          qfull);
+            }
+          }
         }
       }
       ++qn;
@@ -611,7 +638,7 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
         // ----- hot ring tile: slots [at*TOKH, at*TOKH + TOKH) of sequence b
         if (lane == 0) {
           *reinterpret_cast<volatile uint32_t*>(hdrs + stage * 16) = 0u;
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * Gm::REGION));
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * (Gm::REGION >> hgu_shift<KVB>(p))));
         }
         __syncwarp();
         iss_mask |= 1u << stage;
@@ -1085,7 +1112,8 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   const int warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
   const int kvs = warp / TG, tg = warp % TG;
-  const int nh = unit_nh(p, s.hg);  // query rows of this unit per kv head
+  const int hg = slot_hg<KVB>(p, s.hg, kvs);
+  const int nh = unit_nh(p, hg);  // query rows of this warp's slot
   if constexpr (PK) {
     // fold the remainder columns (lane c ^ 2) into the f16-part columns;
     // both lanes of a pair then hold the same state
@@ -1110,13 +1138,13 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     if (tg < st) merge_state<D>(a, red + (kvs * (TG / 2) + tg) * red_floats(D), lane);
     named_bar_sync(kRedBarrier, NCW * 32);
   }
-  const int kv = s.kvb * KVB + kvs;
+  const int kv = slot_kv<KVB>(p, s.kvb, kvs);
   if (tg == 0 && (!PK || c < 2)) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int h = 2 * c + j;
       if (h >= nh) continue;
-      const long long orow = out_row<KIND>(p, s.b, kv, s.hg, h);
+      const long long orow = out_row<KIND>(p, s.b, kv, hg, h);
       const float L = a.l[j];
       const float inv = L > 0.f ? 1.f / L : 0.f;
       const float lse = (a.m[j] == kNegInf) ? kNegInf : (a.m[j] + log2f(L)) * kLn2;
@@ -1169,10 +1197,12 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     // with a running log-sum-exp.
     constexpr int D4 = D / 4;
     const int nk = c1 - c0 + 1;
-    for (int idx = tid; idx < KVB * nh * D4; idx += NCW * 32) {
+    const int NHs = p.NH;  // rows per slot (the last head group's slots may use fewer)
+    for (int idx = tid; idx < KVB * NHs * D4; idx += NCW * 32) {
       const int d4 = idx % D4;
       const int hh = idx / D4;
-      const int ks = hh / nh, h = hh % nh;
+      const int ks = hh / NHs, h = hh % NHs;
+      if (h >= unit_nh(p, slot_hg<KVB>(p, s.hg, ks))) continue;
       const int rowoff = ks * kHeadTile + h;
       float M = kNegInf, Wsum = 0.f;
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1213,7 +1243,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
         o = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
         lse = M + logf(Wsum);
       }
-      const long long orow = out_row<KIND>(p, s.b, s.kvb * KVB + ks, s.hg, h);
+      const long long orow = out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), slot_hg<KVB>(p, s.hg, ks), h);
       reinterpret_cast<float4*>(p.out + orow * D)[d4] = o;
       if (d4 == 0 && p.lse) p.lse[orow] = lse;
     }
@@ -1266,21 +1296,26 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   while (seg_next<KIND, Gm::TOK>(p, plan, pre, it, s)) {
     if (s.i0 >= s.i1) {
       // SPLIT with no visible key: o = 0, lse = -inf
-      const int nh = unit_nh(p, s.hg);
-      for (int idx = tid; idx < KVB * nh * D; idx += NCW * 32) {
+      const int NHs = p.NH;
+      for (int idx = tid; idx < KVB * NHs * D; idx += NCW * 32) {
         const int d = idx % D, hh = idx / D;
-        const int kv = s.kvb * KVB + hh / nh, h = hh % nh;
-        const long long pr = out_row<KIND>(p, s.b, kv, s.hg, h) * p.max_splits + s.slot;
+        const int ks = hh / NHs, h = hh % NHs;
+        const int hgs = slot_hg<KVB>(p, s.hg, ks);
+        if (h >= unit_nh(p, hgs)) continue;
+        const long long pr =
+            out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h) * p.max_splits + s.slot;
         p.o_part[pr * D + d] = 0.f;
         if (d == 0) p.lse_part[pr] = kNegInf;
       }
       continue;
     }
     const SeqPlan e = plan.get(s.pidx);
-    const int kv = s.kvb * KVB + kvs;
+    const int kv = slot_kv<KVB>(p, s.kvb, kvs);
+    const int hg = slot_hg<KVB>(p, s.hg, kvs);
+    const int kvsm = kvs >> hgu_shift<KVB>(p);  // this slot's kv head in the stage's boxes
     {
       if (!mbar_wait(qfull, qn & 1, abort_flag(misc), p.wait_ns) && lane == 0) note_abort(misc);
-      load_q<KIND, D, PK>(smem_u32(qslot + kvs * NH * D * 4), unit_nh(p, s.hg), qscale, r, c,
+      load_q<KIND, D, PK>(smem_u32(qslot + kvs * NH * D * 4), unit_nh(p, hg), qscale, r, c,
                           q);
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty);
@@ -1301,7 +1336,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
 #pragma unroll
       for (int col = 0; col < 2; ++col) {
         const int head = (PK ? 2 * (c & 1) : 2 * c) + col;
-        int t = (s.hg * kHeadTile + head) / p.G;
+        int t = (hg * kHeadTile + head) / p.G;
         t = t < p.q_len ? t : p.q_len - 1;
         const long long qp = (long long)e.qp0 + t;
         cm.lo[col] = (p.window > 0 && qp >= p.window) ? (int)(qp - p.window + 1) : 0;
@@ -1331,9 +1366,9 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         km.log2R = bg.log2R;
         km.box_bytes = bg.box_bytes;
         km.cstride = bg.R * 128;
-        km.base = smem_u32(st + L.off_k) + (uint32_t)(kvs * Gm::CHN * bg.R * 128);
+        km.base = smem_u32(st + L.off_k) + (uint32_t)(kvsm * Gm::CHN * bg.R * 128);
         vm = km;
-        vm.base = smem_u32(st + L.off_v) + (uint32_t)(kvs * Gm::CHN * bg.R * 128);
+        vm.base = smem_u32(st + L.off_v) + (uint32_t)(kvsm * Gm::CHN * bg.R * 128);
         const int tok0 = at * Gm::TOK;
         auto ok = [&](int k) {
           const int t = tok0 + k;
@@ -1383,9 +1418,9 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         km.log2R = 31 - __clz(Gm::TOKH);
         km.box_bytes = 0;
         km.cstride = Gm::TOKH * 128;
-        km.base = smem_u32(st + L.off_k) + (uint32_t)(kvs * Gm::CHH * Gm::TOKH * 128);
+        km.base = smem_u32(st + L.off_k) + (uint32_t)(kvsm * Gm::CHH * Gm::TOKH * 128);
         vm = km;
-        vm.base = smem_u32(st + L.off_v) + (uint32_t)(kvs * Gm::CHH * Gm::TOKH * 128);
+        vm.base = smem_u32(st + L.off_v) + (uint32_t)(kvsm * Gm::CHH * Gm::TOKH * 128);
         const int slot0 = at * Gm::TOKH;
         auto ok = [&](int k) { return key_ok_hot(hv, slot0, k); };
         const int k0 = 16 * tg;
@@ -1419,8 +1454,8 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
   // the compiler keeps the shared address space.
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int nplan = (p.sched == SCHED_SPLIT) ? 1 : p.B;
-  const SmemLayout L = make_layout(KIND, D, KVB, NCW, Gm::REGION, Gm::TOK, p.NH, p.Hkv, p.stages,
-                                   nplan);
+  const SmemLayout L = make_layout(KIND, D, KVB, NCW, Gm::REGION >> hgu_shift<KVB>(p), Gm::TOK,
+                                   p.NH, p.Hkv, p.stages, nplan);
   uint8_t* stages = base + L.off_stages;
   uint8_t* hdrs = base + L.off_hdr;
   uint8_t* qslot = base + L.off_q;
@@ -1439,7 +1474,7 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
   bg.R = p.bs < Gm::TOK ? p.bs : Gm::TOK;
   bg.log2R = 31 - __clz(bg.R);
   bg.npg = Gm::TOK / bg.R;
-  bg.box_bytes = bg.R * Gm::CHN * KVB * 128;
+  bg.box_bytes = bg.R * Gm::CHN * (KVB >> hgu_shift<KVB>(p)) * 128;
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {

@@ -88,7 +88,12 @@ struct alignas(128) KParams {
   int Gv;       // query rows per kv head: T * G ("virtual heads", token-major)
   int NH;       // Q-slot rows per kv head: min(Gv, kHeadTile)
   int HG;       // head groups per kv head: ceil(Gv / kHeadTile); the last may be partial
-  int KVB;      // kv heads per unit (equals the instantiation's KVB)
+  int KVB;      // warp slots per unit (equals the instantiation's KVB)
+  // A unit covers KVU kv heads x HGU head groups (KVB = KVU * HGU slots;
+  // slot ks: kv head ks >> hgu_shift, head group ks & (HGU - 1)).  HGU > 1
+  // lets every head group of a kv head share each K/V byte read.
+  int KVU, HGU, hgu_shift;
+  int HGN;      // units per kv-head block: HG / HGU
   int bs, log2_bs, max_blocks, num_blocks;
   float qscale;     // scale * log2(e): scores are kept in base-2 units
   float softcap2;   // softcap * log2(e) (0 = off)

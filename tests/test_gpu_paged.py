@@ -70,6 +70,20 @@ def test_unpacked_variant_for_small_groups(D, G, monkeypatch):
         _check_all_rows(case, mode)
 
 
+@pytest.mark.parametrize("fuse", ["1", "0"])
+@pytest.mark.parametrize("D,G,Hkv", [(64, 16, 4), (128, 12, 2), (128, 16, 2), (128, 16, 4),
+                                     (128, 32, 2), (256, 16, 2)])
+def test_head_groups_sharing_a_unit(D, G, Hkv, fuse, monkeypatch):
+    """More than eight query heads per kv head: two or four head groups of
+    a kv head share one unit (each K/V byte read once); DA_FUSE_HG=0 keeps a
+    unit per head group.  Both must agree with the oracle, including a
+    partial last group (G = 12)."""
+    monkeypatch.setenv("DA_FUSE_HG", fuse)
+    case = _case(700 + D + G + Hkv, D, G * Hkv, Hkv, 16, EDGE_LENS[::2])
+    for mode in MODES:
+        _check_all_rows(case, mode)
+
+
 @pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 256])
 def test_block_sizes(bs):
     case = _case(200 + bs, 128, 8, 2, bs, [1, bs - 1, bs, bs + 1, 3 * bs + 5, 700])

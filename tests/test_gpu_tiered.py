@@ -61,6 +61,17 @@ def test_tier_group_sizes(G):
     _check(case)
 
 
+@pytest.mark.parametrize("fuse", ["1", "0"])
+@pytest.mark.parametrize("D,G,Hkv", [(128, 16, 2), (128, 16, 4), (128, 32, 2), (256, 16, 2)])
+def test_tier_head_groups_sharing_a_unit(D, G, Hkv, fuse, monkeypatch):
+    """Two or four head groups per kv head in one unit (DA_FUSE_HG=1, the
+    default) or one unit each (DA_FUSE_HG=0)."""
+    monkeypatch.setenv("DA_FUSE_HG", fuse)
+    case = wl.make_tiered(f"hg{D}_{G}_{Hkv}", 70 + G + D + Hkv, B=2, Hq=G * Hkv, Hkv=Hkv, D=D,
+                          block_size=16, cold_len=200, hot_len=70, hot_window=96, hot_start=200)
+    _check(case)
+
+
 @pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("G", [1, 3, 4])
 def test_tier_unpacked_variant_for_small_groups(D, G, monkeypatch):
