@@ -336,9 +336,28 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
   }
   const int grid_max = sms;
   const WsLayout w = ws_layout(grid_max, p->head_dim, ws_kvb(p));
-  for (int b0 = 0; b0 < p->batch; b0 += da::kMaxBatchPerLaunch) {
-    const int nb = (p->batch - b0) < da::kMaxBatchPerLaunch ? (p->batch - b0)
-                                                             : da::kMaxBatchPerLaunch;
+  // Sequences per launch.  The per-sequence plan sits in shared memory next
+  // to the pipeline stages; a launch takes at most as many sequences as
+  // leave room for the stages a small batch gets (one stage fewer costs
+  // more than another launch), split evenly over the launches.
+  int chunk = da::kMaxBatchPerLaunch;
+  {
+    const da::GeoInfo g = da::decode_geo(lc.kind, base.D, base.KVB);
+    if (g.W == 0) return DA_ERR_UNSUPPORTED;
+    int sm_small = 0, sm_c = 0;
+    const int small = p->batch < 16 ? p->batch : 16;
+    const int s_small =
+        pick_stages(lc.kind, base.D, base.KVB, g, base.hgu_shift, base.NH, base.Hkv, small, &sm_small);
+    while (chunk > small &&
+           pick_stages(lc.kind, base.D, base.KVB, g, base.hgu_shift, base.NH, base.Hkv, chunk,
+                       &sm_c) < s_small)
+      chunk -= 8;
+    if (chunk < 1) chunk = 1;
+    const int nchunks = (p->batch + chunk - 1) / chunk;
+    chunk = (p->batch + nchunks - 1) / nchunks;
+  }
+  for (int b0 = 0; b0 < p->batch; b0 += chunk) {
+    const int nb = (p->batch - b0) < chunk ? (p->batch - b0) : chunk;
     KParams k = base;
     k.B = nb;
     offset_chunk(k, b0);

@@ -1061,43 +1061,67 @@ __device__ __forceinline__ bool key_ok_hot(const HotView& hv, int slot0, int k) 
   return j >= hv.j0 && j < hv.j1;
 }
 
+// The tree merge goes through shared memory in RP parts of the O
+// fragments (m-tiles [part * MP, part * MP + MP), MP = D / 16 / RP); part 0
+// also carries m and l and fixes the two weights of the merge, which later
+// parts reuse.  A slot holds red_floats(D, RP) floats per lane set.
+struct MergeW {
+  float fa0, fb0, fa1, fb1;
+};
+
 // Combines two online-softmax states of the same heads (this warp's and a
 // partner's, read back from shared memory in the same fragment layout).
-template <int D>
-__device__ __forceinline__ void merge_state(Acc<D>& a, const float* red, int lane) {
-  constexpr int NO = D / 4;
-  const float mb0 = red[(NO + 0) * 32 + lane], mb1 = red[(NO + 1) * 32 + lane];
-  const float lb0 = red[(NO + 2) * 32 + lane], lb1 = red[(NO + 3) * 32 + lane];
-  const float mn0 = fmaxf(a.m[0], mb0), mn1 = fmaxf(a.m[1], mb1);
-  const float fa0 = (a.m[0] == kNegInf) ? 0.f : exp2f(a.m[0] - mn0);
-  const float fb0 = (mb0 == kNegInf) ? 0.f : exp2f(mb0 - mn0);
-  const float fa1 = (a.m[1] == kNegInf) ? 0.f : exp2f(a.m[1] - mn1);
-  const float fb1 = (mb1 == kNegInf) ? 0.f : exp2f(mb1 - mn1);
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) {
-    a.o[mt][0] = a.o[mt][0] * fa0 + red[(4 * mt + 0) * 32 + lane] * fb0;
-    a.o[mt][1] = a.o[mt][1] * fa1 + red[(4 * mt + 1) * 32 + lane] * fb1;
-    a.o[mt][2] = a.o[mt][2] * fa0 + red[(4 * mt + 2) * 32 + lane] * fb0;
-    a.o[mt][3] = a.o[mt][3] * fa1 + red[(4 * mt + 3) * 32 + lane] * fb1;
+template <int D, int RP>
+__device__ __forceinline__ void merge_state(Acc<D>& a, const float* red, int lane, int part,
+                                            MergeW& w) {
+  constexpr int MP = D / 16 / RP;
+  constexpr int NO = 4 * MP;
+  if (part == 0) {
+    const float mb0 = red[(NO + 0) * 32 + lane], mb1 = red[(NO + 1) * 32 + lane];
+    const float lb0 = red[(NO + 2) * 32 + lane], lb1 = red[(NO + 3) * 32 + lane];
+    const float mn0 = fmaxf(a.m[0], mb0), mn1 = fmaxf(a.m[1], mb1);
+    w.fa0 = (a.m[0] == kNegInf) ? 0.f : exp2f(a.m[0] - mn0);
+    w.fb0 = (mb0 == kNegInf) ? 0.f : exp2f(mb0 - mn0);
+    w.fa1 = (a.m[1] == kNegInf) ? 0.f : exp2f(a.m[1] - mn1);
+    w.fb1 = (mb1 == kNegInf) ? 0.f : exp2f(mb1 - mn1);
+    a.l[0] = a.l[0] * w.fa0 + lb0 * w.fb0;
+    a.l[1] = a.l[1] * w.fa1 + lb1 * w.fb1;
+    a.m[0] = mn0;
+    a.m[1] = mn1;
   }
-  a.l[0] = a.l[0] * fa0 + lb0 * fb0;
-  a.l[1] = a.l[1] * fa1 + lb1 * fb1;
-  a.m[0] = mn0;
-  a.m[1] = mn1;
+#pragma unroll
+  for (int q = 0; q < RP; ++q) {
+    if (q != part) continue;
+#pragma unroll
+    for (int i = 0; i < MP; ++i) {
+      const int mt = q * MP + i;
+      a.o[mt][0] = a.o[mt][0] * w.fa0 + red[(4 * i + 0) * 32 + lane] * w.fb0;
+      a.o[mt][1] = a.o[mt][1] * w.fa1 + red[(4 * i + 1) * 32 + lane] * w.fb1;
+      a.o[mt][2] = a.o[mt][2] * w.fa0 + red[(4 * i + 2) * 32 + lane] * w.fb0;
+      a.o[mt][3] = a.o[mt][3] * w.fa1 + red[(4 * i + 3) * 32 + lane] * w.fb1;
+    }
+  }
 }
 
-template <int D>
-__device__ __forceinline__ void store_state(const Acc<D>& a, float* red, int lane) {
-  constexpr int NO = D / 4;
+template <int D, int RP>
+__device__ __forceinline__ void store_state(const Acc<D>& a, float* red, int lane, int part) {
+  constexpr int MP = D / 16 / RP;
+  constexpr int NO = 4 * MP;
 #pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) {
+  for (int q = 0; q < RP; ++q) {
+    if (q != part) continue;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) red[(4 * mt + k) * 32 + lane] = a.o[mt][k];
+    for (int i = 0; i < MP; ++i) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) red[(4 * i + k) * 32 + lane] = a.o[q * MP + i][k];
+    }
   }
-  red[(NO + 0) * 32 + lane] = a.m[0];
-  red[(NO + 1) * 32 + lane] = a.m[1];
-  red[(NO + 2) * 32 + lane] = a.l[0];
-  red[(NO + 3) * 32 + lane] = a.l[1];
+  if (part == 0) {
+    red[(NO + 0) * 32 + lane] = a.m[0];
+    red[(NO + 1) * 32 + lane] = a.m[1];
+    red[(NO + 2) * 32 + lane] = a.l[0];
+    red[(NO + 3) * 32 + lane] = a.l[1];
+  }
 }
 
 // Merges the warps of each kv head of segment s and writes the result.
@@ -1131,12 +1155,18 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     a.l[j] = l;
   }
   // tree merge of the TG warps of each kv head; warp tg = 0 ends with the sum
+  constexpr int RP = Gm::RED_PARTS;
 #pragma unroll
   for (int st = TG / 2; st >= 1; st >>= 1) {
-    if (tg >= st && tg < 2 * st) store_state<D>(a, red + (kvs * (TG / 2) + (tg - st)) * red_floats(D), lane);
-    named_bar_sync(kRedBarrier, NCW * 32);
-    if (tg < st) merge_state<D>(a, red + (kvs * (TG / 2) + tg) * red_floats(D), lane);
-    named_bar_sync(kRedBarrier, NCW * 32);
+    MergeW w;
+#pragma unroll
+    for (int part = 0; part < RP; ++part) {
+      if (tg >= st && tg < 2 * st)
+        store_state<D, RP>(a, red + (kvs * (TG / 2) + (tg - st)) * red_floats(D, RP), lane, part);
+      named_bar_sync(kRedBarrier, NCW * 32);
+      if (tg < st) merge_state<D, RP>(a, red + (kvs * (TG / 2) + tg) * red_floats(D, RP), lane, part, w);
+      named_bar_sync(kRedBarrier, NCW * 32);
+    }
   }
   const int kv = slot_kv<KVB>(p, s.kvb, kvs);
   if (tg == 0 && (!PK || c < 2)) {

@@ -67,6 +67,7 @@ struct Geo {
   // the consumers take them (REG_PROD / REG_CONS per thread; the launch
   // gives every warp REG_LAUNCH).  Four consumer warps need no such split.
   static constexpr bool REG_SPLIT = (W == 8);
+  static constexpr int RED_PARTS = cold_int8(KIND) ? 2 : 1;  // tree-merge parts (red_parts)
   static constexpr int THREADS = REG_SPLIT ? (W + 4) * 32 : (W + 1) * 32;
   static constexpr int REG_LAUNCH = 168, REG_PROD = 72, REG_CONS = 216;
   static_assert(!REG_SPLIT || (W * REG_CONS + 4 * REG_PROD <= (W + 4) * REG_LAUNCH),
@@ -156,7 +157,7 @@ struct SmemLayout {
   int off_stages;            // from the 1024-aligned base
   int off_hdr;               // per-stage 16-byte headers
   int off_q;                 // one Q slot: [KVB][NH][D] f32
-  int off_red;               // tree-merge buffer: [W/2][red_floats(D)] f32
+  int off_red;               // tree-merge buffer: [W/2][red_floats(D, RED_PARTS)] f32
   int off_plan, off_pre;
   int off_bar, off_misc;
   int total;  // bytes to request (includes 1 KB of alignment slack)
@@ -166,7 +167,11 @@ __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a *
 
 // Floats one warp stores to hand its merge state to a partner warp: the
 // O^T fragments (D/4 per lane) plus m and l of its two heads, per lane.
-__host__ __device__ constexpr int red_floats(int D) { return (D / 4 + 4) * 32; }
+// Floats of one tree-merge slot: a part of the O fragments plus m and l.
+__host__ __device__ constexpr int red_floats(int D, int parts) { return (D / 4 / parts + 4) * 32; }
+// The int8 tiered kernels merge in two parts, so that their larger stages
+// (K, V and the scale slabs) leave room for the per-sequence plan.
+__host__ __device__ constexpr int red_parts(int kind) { return cold_int8(kind) ? 2 : 1; }
 
 __host__ __device__ inline SmemLayout make_layout(int kind, int D, int KVB, int W, int region,
                                                   int tok, int NH, int Hkv, int stages, int B) {
@@ -184,7 +189,7 @@ __host__ __device__ inline SmemLayout make_layout(int kind, int D, int KVB, int 
   L.off_q = off;
   off += align_up(KVB * NH * D * 4, 128);
   L.off_red = off;
-  off += (W / 2) * red_floats(D) * 4;
+  off += (W / 2) * red_floats(D, red_parts(kind)) * 4;
   L.off_plan = off;
   off += B * (kind == KIND_PAGED ? (int)sizeof(SeqPlanPaged) : (int)sizeof(SeqPlan));
   L.off_pre = off;

@@ -128,3 +128,16 @@ def test_tiered_workload_sampled_rows():
                       f"tiered/{mode}")
     del t
     torch.cuda.empty_cache()
+
+
+def test_tier_large_batch_is_split_over_launches():
+    """240 sequences of the int8 tiered cache: more than one launch keeps
+    the pipeline depth of a small batch (the per-sequence plan shares
+    shared memory with the stages); every row against the oracle."""
+    rng = np.random.default_rng(1240)
+    B = 240
+    cold = rng.integers(0, 120, size=B).tolist()
+    hot = rng.integers(0, 40, size=B).tolist()
+    case = wl.make_tiered("bigB", 1240, B=B, Hq=32, Hkv=8, D=128, block_size=16,
+                          cold_len=cold, hot_len=hot, hot_window=48, hot_start=cold)
+    _check(case, per_seq=True)
