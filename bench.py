@@ -165,18 +165,61 @@ def describe(case):
             "hot_window": case.hot_window, "hot_start": int(case.hot_starts[0])}
 
 
+def _packed_f32(shapes, device="cuda", pin=False):
+    """f32 tensors of the given shapes as views of one contiguous buffer
+    (each view 16-byte aligned); returns the views and, last, the buffer."""
+    import torch
+    offs, n = [], 0
+    for s in shapes:
+        offs.append(n)
+        k = 1
+        for d in s:
+            k *= int(d)
+        n += (k + 3) // 4 * 4
+    buf = torch.empty(max(n, 1), dtype=torch.float32, device=device)
+    if pin:
+        buf = buf.pin_memory()
+    views = []
+    for s, o in zip(shapes, offs):
+        k = 1
+        for d in s:
+            k *= int(d)
+        views.append(buf[o:o + k].view(*s))
+    views.append(buf)
+    return views
+
+
+def _packed_bytes(arrays, device="cuda", pin=False):
+    """Byte buffer holding the given arrays back to back (16-byte aligned);
+    returns views of each with its dtype and shape and, last, the buffer."""
+    import torch
+    offs, n = [], 0
+    for a in arrays:
+        offs.append(n)
+        n += (a.nbytes + 15) // 16 * 16
+    buf = torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+    if pin:
+        buf = buf.pin_memory()
+    views = []
+    for a, o in zip(arrays, offs):
+        dt = {"float32": torch.float32, "int32": torch.int32}[str(a.dtype)]
+        views.append(buf[o:o + a.nbytes].view(dt).view(*a.shape))
+    views.append(buf)
+    return views
+
+
 def make_step(case, t):
     """Returns step() running one decode step on the current stream."""
     import quantized_kv_decode_paged_gb300 as qk
     from quantized_kv_decode_paged_gb300.workloads import PagedCase
     import torch
-    out = torch.empty((case.B, case.Hq, case.D), dtype=torch.float32, device="cuda")
-    lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
+    # out and lse share one device buffer, so the end-to-end step reads the
+    # result back with one copy
+    multi = isinstance(case, PagedCase) and case.q.ndim == 4  # several query tokens
+    o_shape = tuple(case.q.shape) if multi else (case.B, case.Hq, case.D)
+    l_shape = tuple(case.q.shape[:3]) if multi else (case.B, case.Hq)
+    out, lse, _res = _packed_f32([o_shape, l_shape])
     if isinstance(case, PagedCase):
-        multi = case.q.ndim == 4  # several query tokens per sequence
-        if multi:
-            out = torch.empty(case.q.shape, dtype=torch.float32, device="cuda")
-            lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
         params = qk.make_params(t["q"][:, 0] if multi else t["q"], case.block_size, case.Hkv,
                                 case.max_blocks, case.num_blocks, scale=case.scale,
                                 softcap=case.softcap, sliding_window=case.sliding_window,
@@ -216,6 +259,7 @@ def make_step(case, t):
             return qk.decode_attn_tiered_int8(q, t["k_hot"], t["v_hot"], t["k_cold"],
                                               t["v_cold"], t["k_scale"], t["v_scale"],
                                               block_table, **tier)
+    step.result = _res
     return step, out, lse
 
 
@@ -387,32 +431,34 @@ def gpu_arm(args, rank, world):
     dev_ms = sum(times_ms)
     clocks = clk.summary()
 
-    # e2e: host buffers in, host result out, every step
-    q_h = torch.from_numpy(case.q).pin_memory()
-    bt_h = torch.from_numpy(case.block_table).pin_memory()
-    lens_np = case.seq_lens if hasattr(case, "seq_lens") else case.cold_lens + case.hot_lens
-    sl_h = torch.from_numpy(lens_np.astype("int32")).pin_memory()
-    q_d = torch.empty_like(t["q"])
-    bt_d = torch.empty_like(t["block_table"])
-    sl_d = torch.empty(sl_h.shape, dtype=torch.int32, device="cuda")
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    # e2e: host buffers in, host result out, every step.  The step's inputs
+    # (q, block table, sequence lengths) sit back to back in one pinned host
+    # buffer and go over in one copy; out and lse come back in one copy.
+    import numpy as np
     from quantized_kv_decode_paged_gb300.workloads import PagedCase
     paged = isinstance(case, PagedCase)
+    lens_np = (case.seq_lens if paged else case.cold_lens + case.hot_lens).astype("int32")
+    ins = [np.ascontiguousarray(case.q, dtype=np.float32),
+           np.ascontiguousarray(case.block_table, dtype=np.int32)] + ([lens_np] if paged else [])
+    *views_h, in_h = _packed_bytes(ins, device="cpu", pin=True)
+    for v, a in zip(views_h, ins):
+        v.copy_(torch.from_numpy(a))
+    *views, in_d = _packed_bytes(ins, device="cuda")
+    q_d, bt_d = views[0], views[1]
+    sl_d = views[2] if paged else None
+    res_d = step.result  # out and lse, one buffer
+    res_h = torch.empty(res_d.shape, dtype=res_d.dtype).pin_memory()
 
     def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
+        in_d.copy_(in_h, non_blocking=True)
         if paged:
-            sl_d.copy_(sl_h, non_blocking=True)
             step(q=q_d, block_table=bt_d, seq_lens=sl_d)
         else:
             step(q=q_d, block_table=bt_d)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        res_h.copy_(res_d, non_blocking=True)
 
-    h2d = q_h.numel() * 4 + bt_h.numel() * 4 + (sl_h.numel() * 4 if paged else 0)
-    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    h2d = int(in_h.numel())
+    d2h = int(res_h.numel()) * 4
     e2e_steps = max(10, min(args.steps, 500))
     for _ in range(3):
         flush.zero_()
