@@ -372,6 +372,29 @@ def reference_arm(args, rank, world):
     return 0
 
 
+# ------------------------------------------------------------ across ranks
+def aggregate_ranks(dev_ms, e2e_ms, bytes_per_step, world, device):
+    """One replica per rank (weak scaling): the job's time is the slowest
+    rank's, its bytes the sum over ranks.  Returns (device ms, end-to-end
+    ms, bytes per step) for the whole job; with one rank, the inputs."""
+    if world <= 1:
+        return float(dev_ms), float(e2e_ms), float(bytes_per_step)
+    import torch
+    import torch.distributed as dist
+    stats = torch.tensor([dev_ms, e2e_ms, float(bytes_per_step)], dtype=torch.float64,
+                         device=device)
+    mx = stats.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    tot = stats.clone()
+    dist.all_reduce(tot, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(mx[1]), float(tot[2])
+
+
+def job_gbs(total_bytes_per_step, steps, ms):
+    """Whole-job GB/s: every rank's bytes of `steps` steps over `ms`."""
+    return total_bytes_per_step * steps / (ms * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------- GPU arm
 def gpu_arm(args, rank, world):
     import torch
@@ -474,18 +497,8 @@ def gpu_arm(args, rank, world):
     barrier()
     e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps
 
-    # max over ranks
-    stats = torch.tensor([dev_ms, e2e_ms, float(bytes_per_step)], dtype=torch.float64,
-                         device="cuda")
-    if world > 1:
-        mx = stats.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        tot = stats.clone()
-        dist.all_reduce(tot, op=dist.ReduceOp.SUM)
-        dev_ms_max, e2e_ms_max = float(mx[0]), float(mx[1])
-        total_bytes = float(tot[2])
-    else:
-        dev_ms_max, e2e_ms_max, total_bytes = dev_ms, e2e_ms, float(bytes_per_step)
+    dev_ms_max, e2e_ms_max, total_bytes = aggregate_ranks(dev_ms, e2e_ms, bytes_per_step, world,
+                                                          "cuda")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -501,7 +514,7 @@ def gpu_arm(args, rank, world):
 
     if rank == 0:
         ms_per_step = dev_ms_max / args.steps
-        value = total_bytes * args.steps / (dev_ms_max * 1e-3) / 1e9
+        value = job_gbs(total_bytes, args.steps, dev_ms_max)
         per_launch_s = dev_ms / args.steps / launches_per_step * 1e-3
         achieved = bytes_per_step / launches_per_step / per_launch_s / 1e9
         peak, peak_src = measured_hbm_peak()
@@ -525,7 +538,7 @@ def gpu_arm(args, rank, world):
                          if peak_src == "measured" else "fallback",
                          "traffic": traffic},
             "cpu_baseline": cpu,
-            "e2e": {"value": round(total_bytes / (e2e_ms_max * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "e2e": {"value": round(job_gbs(total_bytes, 1, e2e_ms_max), 2), "unit": "GB/s",
                     "us_per_step": round(e2e_ms_max * 1e3, 2),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
