@@ -1176,33 +1176,49 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
       named_bar_sync(kRedBarrier, NCW * 32);
     }
   }
-  const int kv = slot_kv<KVB>(p, s.kvb, kvs);
+  // Results go out through shared memory when the merge buffer (free again
+  // after the tree merge's last barrier) holds every row of the unit: the
+  // warps holding them (tg = 0) write normalized rows there, and all
+  // consumer threads copy whole rows to global memory with 16-byte stores.
+  // Otherwise (the int8 tiered kernels with four slots, whose merge buffer
+  // is halved) the tg = 0 warps store their fragments directly.
+  constexpr int SROW = D + 4;  // floats a staged row: D values, the lse, padding
+  constexpr bool STAGED = KVB * kHeadTile * SROW <= (NCW / 2) * red_floats(D, Gm::RED_PARTS);
+  constexpr int D4 = D / 4;
+  auto row_dst = [&](int ks, int h, float*& dst, float*& ldst) {
+    const int hgs = slot_hg<KVB>(p, s.hg, ks);
+    if (s.dest == DEST_OUT) {
+      const long long orow = out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h);
+      dst = p.out + orow * D;
+      ldst = p.lse ? p.lse + orow : nullptr;
+    } else if (s.dest == DEST_SPLIT) {
+      const long long pr =
+          out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h) * p.max_splits + s.slot;
+      dst = p.o_part + pr * D;
+      ldst = p.lse_part + pr;
+    } else {
+      const long long sl =
+          ((long long)blockIdx.x * 2 + s.slot) * (KVB * kHeadTile) + ks * kHeadTile + h;
+      dst = p.ws_o + sl * D;
+      ldst = p.ws_lse + sl;
+    }
+  };
   if (tg == 0 && (!PK || c < 2)) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int h = 2 * c + j;
       if (h >= nh) continue;
-      const long long orow = out_row<KIND>(p, s.b, kv, hg, h);
       const float L = a.l[j];
       const float inv = L > 0.f ? 1.f / L : 0.f;
       const float lse = (a.m[j] == kNegInf) ? kNegInf : (a.m[j] + log2f(L)) * kLn2;
       float* dst;
       float* ldst;
-      long long ostride = 1;
-      if (s.dest == DEST_OUT) {
-        dst = p.out + orow * D;
-        ldst = p.lse ? p.lse + orow : nullptr;
-      } else if (s.dest == DEST_SPLIT) {
-        const long long pr = orow * p.max_splits + s.slot;
-        dst = p.o_part + pr * D;
-        ldst = p.lse_part + pr;
+      if constexpr (STAGED) {
+        dst = red + (kvs * kHeadTile + h) * SROW;
+        ldst = dst + D;
       } else {
-        const long long sl = ((long long)blockIdx.x * 2 + s.slot) * (KVB * kHeadTile) +
-                             kvs * kHeadTile + h;
-        dst = p.ws_o + sl * D;
-        ldst = p.ws_lse + sl;
+        row_dst(kvs, h, dst, ldst);
       }
-      (void)ostride;
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
         dst[o_row_d<KIND>(mt, r, 0)] = a.o[mt][j] * inv;
@@ -1211,8 +1227,23 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
       if (r == 0 && ldst) *ldst = lse;
     }
   }
+  if constexpr (STAGED) {
+    named_bar_sync(kRedBarrier, NCW * 32);
+    for (int idx = tid; idx < KVB * kHeadTile * D4; idx += NCW * 32) {
+      const int d4 = idx % D4, lrow = idx / D4;
+      const int ks = lrow / kHeadTile, h = lrow % kHeadTile;
+      if (h >= unit_nh(p, slot_hg<KVB>(p, s.hg, ks))) continue;
+      const float* row = red + lrow * SROW;
+      float* dst;
+      float* ldst;
+      row_dst(ks, h, dst, ldst);
+      reinterpret_cast<float4*>(dst)[d4] = *reinterpret_cast<const float4*>(row + 4 * d4);
+      if (d4 == 0 && ldst) *ldst = row[D];
+    }
+    named_bar_sync(kRedBarrier, NCW * 32);  // rows read before the buffer is written again
+  }
   if (s.dest != DEST_PARTIAL) return;
-  if (tg == 0) __threadfence();  // the warps that wrote the partial state
+  if (STAGED || tg == 0) __threadfence();  // the threads that stored the partial state
   named_bar_sync(kRedBarrier, NCW * 32);
   // ---- last-arriver merge of the unit's partial states
   const long long T = pre[p.B];
