@@ -797,14 +797,17 @@ __device__ __forceinline__ void tile_qk(const RowMap& km, int k0, int lane, cons
       qk_mma<TK, D, PK, NCH>(s4, ks, a0, a1, a2, a3, q);
     }
   } else if constexpr (TK == TK_COLD) {
-    // int8 rows of D bytes: word c of 16-byte unit ks holds d = 16ks + 4c .. +3
-    const uint32_t rb0 = km.row(k0 + r) + 4 * c;
-    const uint32_t rb1 = km.row(k0 + r + 8) + 4 * c;
+    // int8 rows of D bytes: word c of 16-byte unit ks holds d = 16ks + 4c .. +3.
+    // Rows start on 128-byte boundaries, so the swizzled unit (ks & 7) ^ r
+    // is set with an xor on a per-tile base (one logic op a load).
+    const uint32_t x0 = km.row(k0 + r) | (uint32_t)(4 * c) | (uint32_t)(r << 4);
+    const uint32_t x1 = km.row(k0 + r + 8) | (uint32_t)(4 * c) | (uint32_t)(r << 4);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      const uint32_t off = (ks >> 3) * km.cstride + (((ks & 7) ^ r) << 4);
-      const uint32_t w0 = lds32(rb0 + off) ^ 0x80808080u;
-      const uint32_t w1 = lds32(rb1 + off) ^ 0x80808080u;
+      const uint32_t cs = (ks >> 3) * km.cstride;
+      const uint32_t sw = (uint32_t)((ks & 7) << 4);
+      const uint32_t w0 = lds32((x0 + cs) ^ sw) ^ 0x80808080u;
+      const uint32_t w1 = lds32((x1 + cs) ^ sw) ^ 0x80808080u;
       const uint32_t a0 = biased_i8x2_to_h2(w0, 0x4140u), a2 = biased_i8x2_to_h2(w0, 0x4342u);
       const uint32_t a1 = biased_i8x2_to_h2(w1, 0x4140u), a3 = biased_i8x2_to_h2(w1, 0x4342u);
       qk_mma<TK, D, PK, NCH>(s4, ks, a0, a1, a2, a3, q);
@@ -853,18 +856,22 @@ __device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, floa
       pv_mma<PK>(o[mt], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
     }
   } else if constexpr (TK == TK_COLD) {
-    // word q = 8pp + r (d = 4q .. 4q+3) of keys 2c, 2c+1, 2c+8, 2c+9
+    // word q = 8pp + r (d = 4q .. 4q+3) of keys 2c, 2c+1, 2c+8, 2c+9: the
+    // unit (2(pp & 3) + (r >> 2)) ^ (key & 7) of each row, split into a
+    // per-tile part and an xor by 2(pp & 3) (rows on 128-byte boundaries)
     const int tA = k0 + 2 * c;
-    const uint32_t rA = vm.row(tA) + (r & 3) * 4, rB = vm.row(tA + 1) + (r & 3) * 4;
-    const uint32_t rC = vm.row(tA + 8) + (r & 3) * 4, rD = vm.row(tA + 9) + (r & 3) * 4;
+    const uint32_t w4 = (uint32_t)((r & 3) * 4);
+    const uint32_t uA = (uint32_t)((2 * c) | (r >> 2)) << 4, uB = uA ^ 16u;
+    const uint32_t xA = vm.row(tA) | w4 | uA, xB = vm.row(tA + 1) | w4 | uB;
+    const uint32_t xC = vm.row(tA + 8) | w4 | uA, xD = vm.row(tA + 9) | w4 | uB;
 #pragma unroll
     for (int pp = 0; pp < D / 32; ++pp) {
-      const int u = 2 * (pp & 3) + (r >> 2);
       const uint32_t cs = (pp >> 2) * vm.cstride;
-      const uint32_t WA = lds32(rA + cs + ((u ^ (2 * c)) << 4)) ^ 0x80808080u;
-      const uint32_t WB = lds32(rB + cs + ((u ^ (2 * c + 1)) << 4)) ^ 0x80808080u;
-      const uint32_t WC = lds32(rC + cs + ((u ^ (2 * c)) << 4)) ^ 0x80808080u;
-      const uint32_t WD = lds32(rD + cs + ((u ^ (2 * c + 1)) << 4)) ^ 0x80808080u;
+      const uint32_t sw = (uint32_t)((pp & 3) << 5);
+      const uint32_t WA = lds32((xA + cs) ^ sw) ^ 0x80808080u;
+      const uint32_t WB = lds32((xB + cs) ^ sw) ^ 0x80808080u;
+      const uint32_t WC = lds32((xC + cs) ^ sw) ^ 0x80808080u;
+      const uint32_t WD = lds32((xD + cs) ^ sw) ^ 0x80808080u;
       const uint32_t E = __byte_perm(WA, WB, 0x5140u), F = __byte_perm(WA, WB, 0x7362u);
       const uint32_t E2 = __byte_perm(WC, WD, 0x5140u), F2 = __byte_perm(WC, WD, 0x7362u);
       {
