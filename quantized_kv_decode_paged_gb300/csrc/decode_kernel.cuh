@@ -1429,6 +1429,9 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
       hv.j0 = j0 > 0 ? j0 : 0;
       hv.j1 = j1 < e.hot_len ? j1 : e.hot_len;
     }
+    // all ring slots below cap_eff hold visible keys (a full, unmasked ring)
+    const bool hot_all =
+        is_tiered(KIND) && hv.j0 <= 0 && hv.j1 >= (hv.W > 0 ? (long long)hv.W : (long long)hv.cap_eff);
     const int vhc = is_tiered(KIND) ? min(s.vhi, e.cold_len) : s.vhi;
 
     for (int i = s.i0; i < s.i1; ++i) {
@@ -1498,7 +1501,9 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         vm = km;
         vm.base = smem_u32(st + L.off_v) + (uint32_t)(kvsm * Gm::CHH * Gm::TOKH * 128);
         const int slot0 = at * Gm::TOKH;
-        auto ok = [&](int k) { return key_ok_hot(hv, slot0, k); };
+        // every slot of the tile holds a visible key: no per-key ring test
+        const bool all_in = hot_all && slot0 + Gm::TOKH <= hv.cap_eff;
+        auto ok = [&](int k) { return all_in || key_ok_hot(hv, slot0, k); };
         const int k0 = 16 * tg;
         const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
         if (__any_sync(0xffffffffu, vA || vB)) {
