@@ -1430,8 +1430,9 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
       hv.j1 = j1 < e.hot_len ? j1 : e.hot_len;
     }
     // all ring slots below cap_eff hold visible keys (a full, unmasked ring)
-    const bool hot_all =
-        is_tiered(KIND) && hv.j0 <= 0 && hv.j1 >= (hv.W > 0 ? (long long)hv.W : (long long)hv.cap_eff);
+    bool hot_all = false;
+    if constexpr (is_tiered(KIND))
+      hot_all = hv.j0 <= 0 && hv.j1 >= (hv.W > 0 ? (long long)hv.W : (long long)hv.cap_eff);
     const int vhc = is_tiered(KIND) ? min(s.vhi, e.cold_len) : s.vhi;
 
     for (int i = s.i0; i < s.i1; ++i) {
