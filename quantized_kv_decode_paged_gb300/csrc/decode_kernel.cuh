@@ -277,7 +277,10 @@ __device__ __forceinline__ int stream_cta_of(long long g, long long T, int grid)
   return (int)(((g + 1) * grid - 1) / T);
 }
 __device__ __forceinline__ long long stream_start(int c, long long T, int grid) {
-  return (long long)c * T / grid;
+  // floor(c * T / grid) in 32-bit steps (tile counts fit in int; c <= grid)
+  const unsigned t = (unsigned)T, g = (unsigned)grid, uc = (unsigned)c;
+  const unsigned q = t / g, r = t - q * g;
+  return (long long)(uc * q + (uc * r) / g);
 }
 // CTAs that share the key tiles in the STREAM schedule: never more than the
 // tiles, so every participating CTA owns at least one tile.
@@ -364,7 +367,8 @@ __device__ __forceinline__ void seg_init(const KParams& p, const PlanStore<KIND>
     if (it.g_end > it.g) {
       const int b = seq_of(p, pre, it.g_end - 1);
       const int nt = plan.ntiles(b);
-      const long long u0 = pre[b] + (it.g_end - 1 - pre[b]) / nt * nt;  // unit start
+      const int off = (int)(it.g_end - 1 - pre[b]);
+      const long long u0 = pre[b] + (long long)(off / nt * nt);  // unit start
       if (u0 > it.s0 && u0 + nt > it.g_end) {
         it.last0 = u0;
         it.fwd_end = u0;
@@ -394,13 +398,14 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
     const SeqPlan e = plan.get(b);
     const int nt = e.ntiles;
     const long long local = g - pre[b];
-    const int uib = (int)(local / nt);
+    const int li = (int)local;  // tile counts fit in int
+    const int uib = li / nt;
     s.b = b;
     s.pidx = b;
     s.kvb = uib / p.HGN;
     s.hg = (uib % p.HGN) * p.HGU;
     s.unit = b * upb + uib;
-    s.i0 = (int)(local % nt);
+    s.i0 = li - uib * nt;
     const long long rem = end - g;
     s.i1 = (int)((long long)s.i0 + rem < nt ? s.i0 + rem : nt);
     s.vlo = e.lo;
