@@ -96,6 +96,14 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint16_t lds16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
@@ -721,7 +729,9 @@ __device__ __forceinline__ void load_q(uint32_t qs, int NH, float qscale, int r,
       d0 = 16 * ks + 2 * c;
       d2 = d0 + 8;
     } else {
-      d0 = 16 * ks + 4 * c;
+      // tiered d order: k-steps 2j and 2j + 1 take, from lane c, the 8
+      // consecutive values d = 32j + 8c .. + 7 of a key (4 each)
+      d0 = 32 * (ks >> 1) + 8 * c + 4 * (ks & 1);
       d2 = d0 + 2;
     }
     float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
@@ -802,32 +812,44 @@ __device__ __forceinline__ void tile_qk(const RowMap& km, int k0, int lane, cons
       qk_mma<TK, D, PK, NCH>(s4, ks, a0, a1, a2, a3, q);
     }
   } else if constexpr (TK == TK_COLD) {
-    // int8 rows of D bytes: word c of 16-byte unit ks holds d = 16ks + 4c .. +3.
-    // Rows start on 128-byte boundaries, so the swizzled unit (ks & 7) ^ r
-    // is set with an xor on a per-tile base (one logic op a load).
-    const uint32_t x0 = km.row(k0 + r) | (uint32_t)(4 * c) | (uint32_t)(r << 4);
-    const uint32_t x1 = km.row(k0 + r + 8) | (uint32_t)(4 * c) | (uint32_t)(r << 4);
+    // int8 rows of D bytes; k-steps 2j and 2j + 1 take the 8 bytes
+    // d = 32j + 8c .. + 7 of rows r and r + 8 (one 8-byte load each): the
+    // 16-byte unit (2j + (c >> 1)) & 7 of slice j >> 2, at byte 8 (c & 1).
+    // Rows start on 128-byte boundaries, so the swizzled unit is set with an
+    // xor on a per-tile base.
+    const uint32_t lb = (uint32_t)(8 * (c & 1)) | (uint32_t)((((c >> 1) ^ r) & 7) << 4);
+    const uint32_t x0 = km.row(k0 + r) | lb;
+    const uint32_t x1 = km.row(k0 + r + 8) | lb;
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const uint32_t cs = (ks >> 3) * km.cstride;
-      const uint32_t sw = (uint32_t)((ks & 7) << 4);
-      const uint32_t w0 = lds32((x0 + cs) ^ sw) ^ 0x80808080u;
-      const uint32_t w1 = lds32((x1 + cs) ^ sw) ^ 0x80808080u;
-      const uint32_t a0 = biased_i8x2_to_h2(w0, 0x4140u), a2 = biased_i8x2_to_h2(w0, 0x4342u);
-      const uint32_t a1 = biased_i8x2_to_h2(w1, 0x4140u), a3 = biased_i8x2_to_h2(w1, 0x4342u);
-      qk_mma<TK, D, PK, NCH>(s4, ks, a0, a1, a2, a3, q);
+    for (int j = 0; j < D / 32; ++j) {
+      const uint32_t cs = (j >> 2) * km.cstride;
+      const uint32_t sw = (uint32_t)(((2 * j) & 7) << 4);
+      const uint2 w0 = lds64((x0 + cs) ^ sw);
+      const uint2 w1 = lds64((x1 + cs) ^ sw);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t u0 = (t ? w0.y : w0.x) ^ 0x80808080u;
+        const uint32_t u1 = (t ? w1.y : w1.x) ^ 0x80808080u;
+        const uint32_t a0 = biased_i8x2_to_h2(u0, 0x4140u), a2 = biased_i8x2_to_h2(u0, 0x4342u);
+        const uint32_t a1 = biased_i8x2_to_h2(u1, 0x4140u), a3 = biased_i8x2_to_h2(u1, 0x4342u);
+        qk_mma<TK, D, PK, NCH>(s4, 2 * j + t, a0, a1, a2, a3, q);
+      }
     }
   } else {
-    // f16 rows: 8 bytes at d = 16ks + 4c
-    const uint32_t rb0 = km.row(k0 + r) + (c & 1) * 8;
-    const uint32_t rb1 = km.row(k0 + r + 8) + (c & 1) * 8;
+    // f16 rows; k-steps 2j and 2j + 1 take the 8 values d = 32j + 8c .. + 7
+    // of rows r and r + 8 (one 16-byte load each): unit (4j + c) & 7 of
+    // slice j >> 1
+    const uint32_t lb = (uint32_t)(((c ^ r) & 7) << 4);
+    const uint32_t x0 = km.row(k0 + r) | lb;
+    const uint32_t x1 = km.row(k0 + r + 8) | lb;
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const int u = 2 * (ks & 3) + (c >> 1);
-      const uint32_t off = (ks >> 2) * km.cstride + ((u ^ r) << 4);
-      const uint2 v0 = lds64(rb0 + off);
-      const uint2 v1 = lds64(rb1 + off);
-      qk_mma<TK, D, PK, NCH>(s4, ks, v0.x, v1.x, v0.y, v1.y, q);
+    for (int j = 0; j < D / 32; ++j) {
+      const uint32_t cs = (j >> 1) * km.cstride;
+      const uint32_t sw = (uint32_t)(((4 * j) & 7) << 4);
+      const uint4 v0 = lds128((x0 + cs) ^ sw);
+      const uint4 v1 = lds128((x1 + cs) ^ sw);
+      qk_mma<TK, D, PK, NCH>(s4, 2 * j, v0.x, v1.x, v0.y, v1.y, q);
+      qk_mma<TK, D, PK, NCH>(s4, 2 * j + 1, v0.z, v1.z, v0.w, v1.w, q);
     }
   }
 }
