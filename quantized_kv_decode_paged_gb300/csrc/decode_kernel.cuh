@@ -703,14 +703,15 @@ struct QFrag {
 
 // Head-dimension index held by accumulator row r (+8 when hi8) of m-tile mt.
 // Paged f16 keys use the natural order (ldmatrix.trans fragments); the
-// tiered kernel loads V rows four values at a time, so m-tile pair
-// (2p, 2p+1) covers d = 4*(8p + r) + {0, 1, 2, 3}.
+// tiered kernel loads V rows eight values at a time, so the four m-tiles
+// 4P .. 4P+3 cover, for row r, d = 64P + 8r + {0 .. 7}: m-tile 4P + 2s + u
+// holds d = 64P + 8r + 4s + 2u (+1 when hi8).
 template <int KIND>
 __device__ __forceinline__ int o_row_d(int mt, int r, int hi8) {
   if constexpr (is_paged(KIND)) {
     return 16 * mt + r + 8 * hi8;
   } else {
-    return 4 * (8 * (mt >> 1) + r) + 2 * (mt & 1) + hi8;
+    return 64 * (mt >> 2) + 8 * r + 4 * ((mt >> 1) & 1) + 2 * (mt & 1) + hi8;
   }
 }
 
@@ -883,57 +884,65 @@ __device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, floa
       pv_mma<PK>(o[mt], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
     }
   } else if constexpr (TK == TK_COLD) {
-    // word q = 8pp + r (d = 4q .. 4q+3) of keys 2c, 2c+1, 2c+8, 2c+9: the
-    // unit (2(pp & 3) + (r >> 2)) ^ (key & 7) of each row, split into a
-    // per-tile part and an xor by 2(pp & 3) (rows on 128-byte boundaries)
+    // keys 2c, 2c+1, 2c+8, 2c+9; for m-tiles 4P .. 4P+3 the 8 bytes
+    // d = 64P + 8r .. + 7 of each row (one 8-byte load): unit
+    // (4(P & 1) + (r >> 1)) ^ (key & 7) of slice P >> 1, at byte 8 (r & 1),
+    // split into a per-tile part and an xor by 4(P & 1) (rows on 128-byte
+    // boundaries)
     const int tA = k0 + 2 * c;
-    const uint32_t w4 = (uint32_t)((r & 3) * 4);
-    const uint32_t uA = (uint32_t)((2 * c) | (r >> 2)) << 4, uB = uA ^ 16u;
-    const uint32_t xA = vm.row(tA) | w4 | uA, xB = vm.row(tA + 1) | w4 | uB;
-    const uint32_t xC = vm.row(tA + 8) | w4 | uA, xD = vm.row(tA + 9) | w4 | uB;
+    const uint32_t b8 = (uint32_t)(8 * (r & 1));
+    const uint32_t uA = (uint32_t)((((r >> 1) ^ (2 * c)) & 7) << 4), uB = uA ^ 16u;
+    const uint32_t xA = vm.row(tA) | b8 | uA, xB = vm.row(tA + 1) | b8 | uB;
+    const uint32_t xC = vm.row(tA + 8) | b8 | uA, xD = vm.row(tA + 9) | b8 | uB;
 #pragma unroll
-    for (int pp = 0; pp < D / 32; ++pp) {
-      const uint32_t cs = (pp >> 2) * vm.cstride;
-      const uint32_t sw = (uint32_t)((pp & 3) << 5);
-      const uint32_t WA = lds32((xA + cs) ^ sw) ^ 0x80808080u;
-      const uint32_t WB = lds32((xB + cs) ^ sw) ^ 0x80808080u;
-      const uint32_t WC = lds32((xC + cs) ^ sw) ^ 0x80808080u;
-      const uint32_t WD = lds32((xD + cs) ^ sw) ^ 0x80808080u;
-      const uint32_t E = __byte_perm(WA, WB, 0x5140u), F = __byte_perm(WA, WB, 0x7362u);
-      const uint32_t E2 = __byte_perm(WC, WD, 0x5140u), F2 = __byte_perm(WC, WD, 0x7362u);
-      {
-        const uint32_t a0 = biased_i8x2_to_h2(E, 0x4140u), a1 = biased_i8x2_to_h2(E, 0x4342u);
-        const uint32_t a2 = biased_i8x2_to_h2(E2, 0x4140u), a3 = biased_i8x2_to_h2(E2, 0x4342u);
-        pv_mma<PK>(o[2 * pp], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
-      }
-      {
-        const uint32_t a0 = biased_i8x2_to_h2(F, 0x4140u), a1 = biased_i8x2_to_h2(F, 0x4342u);
-        const uint32_t a2 = biased_i8x2_to_h2(F2, 0x4140u), a3 = biased_i8x2_to_h2(F2, 0x4342u);
-        pv_mma<PK>(o[2 * pp + 1], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
+    for (int P = 0; P < D / 64; ++P) {
+      const uint32_t cs = (P >> 1) * vm.cstride;
+      const uint32_t sw = (uint32_t)((4 * (P & 1)) << 4);
+      const uint2 qa = lds64((xA + cs) ^ sw), qb = lds64((xB + cs) ^ sw);
+      const uint2 qc = lds64((xC + cs) ^ sw), qd = lds64((xD + cs) ^ sw);
+#pragma unroll
+      for (int sh = 0; sh < 2; ++sh) {  // word sh: d = 64P + 8r + 4sh .. + 3
+        const uint32_t WA = (sh ? qa.y : qa.x) ^ 0x80808080u;
+        const uint32_t WB = (sh ? qb.y : qb.x) ^ 0x80808080u;
+        const uint32_t WC = (sh ? qc.y : qc.x) ^ 0x80808080u;
+        const uint32_t WD = (sh ? qd.y : qd.x) ^ 0x80808080u;
+        const uint32_t E = __byte_perm(WA, WB, 0x5140u), F = __byte_perm(WA, WB, 0x7362u);
+        const uint32_t E2 = __byte_perm(WC, WD, 0x5140u), F2 = __byte_perm(WC, WD, 0x7362u);
+        const int mt = 4 * P + 2 * sh;
+        {
+          const uint32_t a0 = biased_i8x2_to_h2(E, 0x4140u), a1 = biased_i8x2_to_h2(E, 0x4342u);
+          const uint32_t a2 = biased_i8x2_to_h2(E2, 0x4140u), a3 = biased_i8x2_to_h2(E2, 0x4342u);
+          pv_mma<PK>(o[mt], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
+        }
+        {
+          const uint32_t a0 = biased_i8x2_to_h2(F, 0x4140u), a1 = biased_i8x2_to_h2(F, 0x4342u);
+          const uint32_t a2 = biased_i8x2_to_h2(F2, 0x4140u), a3 = biased_i8x2_to_h2(F2, 0x4342u);
+          pv_mma<PK>(o[mt + 1], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
+        }
       }
     }
   } else {
-    // f16 rows, 8 bytes (d = 4q .. 4q+3, q = 8pp + r) of keys 2c, 2c+1, 2c+8, 2c+9
+    // f16 rows of keys 2c, 2c+1, 2c+8, 2c+9; for m-tiles 4P .. 4P+3 the 16
+    // bytes d = 64P + 8r .. + 7 of each row (one 16-byte load): unit r ^ (key & 7)
+    // of slice P
     const int tA = k0 + 2 * c;
-    const uint32_t rA = vm.row(tA) + (r & 1) * 8, rB = vm.row(tA + 1) + (r & 1) * 8;
-    const uint32_t rC = vm.row(tA + 8) + (r & 1) * 8, rD = vm.row(tA + 9) + (r & 1) * 8;
+    const uint32_t uA = (uint32_t)(((r ^ (2 * c)) & 7) << 4), uB = uA ^ 16u;
+    const uint32_t xA = vm.row(tA) | uA, xB = vm.row(tA + 1) | uB;
+    const uint32_t xC = vm.row(tA + 8) | uA, xD = vm.row(tA + 9) | uB;
 #pragma unroll
-    for (int pp = 0; pp < D / 32; ++pp) {
-      const int u = 4 * (pp & 1) + (r >> 1);
-      const uint32_t cs = (pp >> 1) * vm.cstride;
-      const uint2 A = lds64(rA + cs + ((u ^ (2 * c)) << 4));
-      const uint2 B = lds64(rB + cs + ((u ^ (2 * c + 1)) << 4));
-      const uint2 C = lds64(rC + cs + ((u ^ (2 * c)) << 4));
-      const uint2 E = lds64(rD + cs + ((u ^ (2 * c + 1)) << 4));
-      {
-        const uint32_t a0 = __byte_perm(A.x, B.x, 0x5410u), a1 = __byte_perm(A.x, B.x, 0x7632u);
-        const uint32_t a2 = __byte_perm(C.x, E.x, 0x5410u), a3 = __byte_perm(C.x, E.x, 0x7632u);
-        pv_mma<PK>(o[2 * pp], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
-      }
-      {
-        const uint32_t a0 = __byte_perm(A.y, B.y, 0x5410u), a1 = __byte_perm(A.y, B.y, 0x7632u);
-        const uint32_t a2 = __byte_perm(C.y, E.y, 0x5410u), a3 = __byte_perm(C.y, E.y, 0x7632u);
-        pv_mma<PK>(o[2 * pp + 1], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
+    for (int P = 0; P < D / 64; ++P) {
+      const uint32_t cs = P * vm.cstride;
+      const uint4 A = lds128(xA + cs), B = lds128(xB + cs);
+      const uint4 C = lds128(xC + cs), E = lds128(xD + cs);
+      const uint32_t w[4][4] = {{A.x, B.x, C.x, E.x}, {A.y, B.y, C.y, E.y},
+                                {A.z, B.z, C.z, E.z}, {A.w, B.w, C.w, E.w}};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {  // m-tile 4P + u: d = 64P + 8r + 2u (+1)
+        const uint32_t a0 = __byte_perm(w[u][0], w[u][1], 0x5410u);
+        const uint32_t a1 = __byte_perm(w[u][0], w[u][1], 0x7632u);
+        const uint32_t a2 = __byte_perm(w[u][2], w[u][3], 0x5410u);
+        const uint32_t a3 = __byte_perm(w[u][2], w[u][3], 0x7632u);
+        pv_mma<PK>(o[4 * P + u], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
       }
     }
   }
