@@ -701,18 +701,11 @@ struct QFrag {
   uint32_t hi[D / 16][2], lo[D / 16][2];
 };
 
-// Head-dimension index held by accumulator row r (+8 when hi8) of m-tile mt.
-// Paged f16 keys use the natural order (ldmatrix.trans fragments); the
-// tiered kernel loads V rows eight values at a time, so the four m-tiles
-// 4P .. 4P+3 cover, for row r, d = 64P + 8r + {0 .. 7}: m-tile 4P + 2s + u
-// holds d = 64P + 8r + 4s + 2u (+1 when hi8).
+// Head-dimension index held by accumulator row r (+8 when hi8) of m-tile mt:
+// every V load (f16 and int8 transposed fragments) keeps the natural order.
 template <int KIND>
 __device__ __forceinline__ int o_row_d(int mt, int r, int hi8) {
-  if constexpr (is_paged(KIND)) {
-    return 16 * mt + r + 8 * hi8;
-  } else {
-    return 64 * (mt >> 2) + 8 * r + 4 * ((mt >> 1) & 1) + 2 * (mt & 1) + hi8;
-  }
+  return 16 * mt + r + 8 * hi8;
 }
 
 // Q rows of the head group, prescaled (scale*log2 e), as hi/lo f16 B
@@ -869,8 +862,8 @@ __device__ __forceinline__ void pv_mma(float (&o)[4], uint32_t a0, uint32_t a1, 
 template <int TK, int D, bool PK>
 __device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, float (&o)[D / 16][4],
                                         uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
-  const int r = lane >> 2, c = lane & 3;
-  if constexpr (TK == TK_PAGED) {
+  if constexpr (TK == TK_PAGED || TK == TK_HOT) {
+    // f16 rows: 8x8 transposed fragments (d rows of m-tile mt, keys k0 ..)
     const int mat = lane >> 3;
     const int key = k0 + (lane & 7) + ((mat >> 1) << 3);
     const uint32_t rowaddr = vm.row(key);
@@ -883,69 +876,43 @@ __device__ __forceinline__ void tile_pv(const RowMap& vm, int k0, int lane, floa
       ldsm_x4_trans(rowaddr + (ug >> 3) * vm.cstride + (((ug & 7) ^ x) << 4), a0, a1, a2, a3);
       pv_mma<PK>(o[mt], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
     }
-  } else if constexpr (TK == TK_COLD) {
-    // keys 2c, 2c+1, 2c+8, 2c+9; for m-tiles 4P .. 4P+3 the 8 bytes
-    // d = 64P + 8r .. + 7 of each row (one 8-byte load): unit
-    // (4(P & 1) + (r >> 1)) ^ (key & 7) of slice P >> 1, at byte 8 (r & 1),
-    // split into a per-tile part and an xor by 4(P & 1) (rows on 128-byte
-    // boundaries)
-    const int tA = k0 + 2 * c;
-    const uint32_t b8 = (uint32_t)(8 * (r & 1));
-    const uint32_t uA = (uint32_t)((((r >> 1) ^ (2 * c)) & 7) << 4), uB = uA ^ 16u;
-    const uint32_t xA = vm.row(tA) | b8 | uA, xB = vm.row(tA + 1) | b8 | uB;
-    const uint32_t xC = vm.row(tA + 8) | b8 | uA, xD = vm.row(tA + 9) | b8 | uB;
-#pragma unroll
-    for (int P = 0; P < D / 64; ++P) {
-      const uint32_t cs = (P >> 1) * vm.cstride;
-      const uint32_t sw = (uint32_t)((4 * (P & 1)) << 4);
-      const uint2 qa = lds64((xA + cs) ^ sw), qb = lds64((xB + cs) ^ sw);
-      const uint2 qc = lds64((xC + cs) ^ sw), qd = lds64((xD + cs) ^ sw);
-#pragma unroll
-      for (int sh = 0; sh < 2; ++sh) {  // word sh: d = 64P + 8r + 4sh .. + 3
-        const uint32_t WA = (sh ? qa.y : qa.x) ^ 0x80808080u;
-        const uint32_t WB = (sh ? qb.y : qb.x) ^ 0x80808080u;
-        const uint32_t WC = (sh ? qc.y : qc.x) ^ 0x80808080u;
-        const uint32_t WD = (sh ? qd.y : qd.x) ^ 0x80808080u;
-        const uint32_t E = __byte_perm(WA, WB, 0x5140u), F = __byte_perm(WA, WB, 0x7362u);
-        const uint32_t E2 = __byte_perm(WC, WD, 0x5140u), F2 = __byte_perm(WC, WD, 0x7362u);
-        const int mt = 4 * P + 2 * sh;
-        {
-          const uint32_t a0 = biased_i8x2_to_h2(E, 0x4140u), a1 = biased_i8x2_to_h2(E, 0x4342u);
-          const uint32_t a2 = biased_i8x2_to_h2(E2, 0x4140u), a3 = biased_i8x2_to_h2(E2, 0x4342u);
-          pv_mma<PK>(o[mt], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
-        }
-        {
-          const uint32_t a0 = biased_i8x2_to_h2(F, 0x4140u), a1 = biased_i8x2_to_h2(F, 0x4342u);
-          const uint32_t a2 = biased_i8x2_to_h2(F2, 0x4140u), a3 = biased_i8x2_to_h2(F2, 0x4342u);
-          pv_mma<PK>(o[mt + 1], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
-        }
-      }
-    }
   } else {
-    // f16 rows of keys 2c, 2c+1, 2c+8, 2c+9; for m-tiles 4P .. 4P+3 the 16
-    // bytes d = 64P + 8r .. + 7 of each row (one 16-byte load): unit r ^ (key & 7)
-    // of slice P
-    const int tA = k0 + 2 * c;
-    const uint32_t uA = (uint32_t)(((r ^ (2 * c)) & 7) << 4), uB = uA ^ 16u;
-    const uint32_t xA = vm.row(tA) | uA, xB = vm.row(tA + 1) | uB;
-    const uint32_t xC = vm.row(tA + 8) | uA, xD = vm.row(tA + 9) | uB;
+    // int8 rows: 16 keys x 16 d bytes per transposed 8-bit load, two m-tiles
+    // at once.  Lane (r, c) gets keys k0+4c .. k0+4c+3 at d = 16 mt + r and
+    // + 8, so the MMA's k index 2c + j (+8) stands for key 4c + j (+2); the
+    // caller orders P^T the same way.  Lane l gives the address of row l & 15
+    // of m-tile 2 mp + (l >> 4): unit (mt & 7) ^ (key & 7) of slice mt >> 3,
+    // split into a per-lane part and an xor by 2 mp & 7 (rows on 128-byte
+    // boundaries).
+    const int j = lane & 15;
+    const uint32_t xb = vm.row(k0 + j) | ((uint32_t)(((lane >> 4) ^ j) & 7) << 4);
 #pragma unroll
-    for (int P = 0; P < D / 64; ++P) {
-      const uint32_t cs = P * vm.cstride;
-      const uint4 A = lds128(xA + cs), B = lds128(xB + cs);
-      const uint4 C = lds128(xC + cs), E = lds128(xD + cs);
-      const uint32_t w[4][4] = {{A.x, B.x, C.x, E.x}, {A.y, B.y, C.y, E.y},
-                                {A.z, B.z, C.z, E.z}, {A.w, B.w, C.w, E.w}};
+    for (int mp = 0; mp < D / 32; ++mp) {
+      const uint32_t addr = (xb + (mp >> 2) * vm.cstride) ^ ((uint32_t)((2 * mp) & 7) << 4);
+      uint32_t w[4];
+      ldsm_b8_x2_trans(addr, w[0], w[1], w[2], w[3]);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {  // m-tile 4P + u: d = 64P + 8r + 2u (+1)
-        const uint32_t a0 = __byte_perm(w[u][0], w[u][1], 0x5410u);
-        const uint32_t a1 = __byte_perm(w[u][0], w[u][1], 0x7632u);
-        const uint32_t a2 = __byte_perm(w[u][2], w[u][3], 0x5410u);
-        const uint32_t a3 = __byte_perm(w[u][2], w[u][3], 0x7632u);
-        pv_mma<PK>(o[4 * P + u], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
+      for (int m = 0; m < 2; ++m) {
+        const uint32_t u0 = w[2 * m] ^ 0x80808080u, u1 = w[2 * m + 1] ^ 0x80808080u;
+        const uint32_t a0 = biased_i8x2_to_h2(u0, 0x4140u), a1 = biased_i8x2_to_h2(u1, 0x4140u);
+        const uint32_t a2 = biased_i8x2_to_h2(u0, 0x4342u), a3 = biased_i8x2_to_h2(u1, 0x4342u);
+        pv_mma<PK>(o[2 * mp + m], a0, a1, a2, a3, bh0, bh1, bl0, bl1);
       }
     }
   }
+}
+
+// P^T fragments for the int8 V loads: the natural B fragments hold keys
+// (2c, 2c+1) in b0 and (2c+8, 2c+9) in b1; lane (r, c) takes keys (4c, 4c+1)
+// and (4c+2, 4c+3) instead, from lanes 2c and 2c + 1 (mod 4) of its quad:
+// their b0 for c < 2, their b1 for c >= 2.
+__device__ __forceinline__ void key_order_4c(int lane, uint32_t& b0, uint32_t& b1) {
+  const int q = lane & ~3, c = lane & 3;
+  const int s0 = q | ((2 * c) & 3), s1 = q | ((2 * c + 1) & 3);
+  const uint32_t t0 = __shfl_sync(0xffffffffu, b0, s0), t1 = __shfl_sync(0xffffffffu, b1, s0);
+  const uint32_t t2 = __shfl_sync(0xffffffffu, b0, s1), t3 = __shfl_sync(0xffffffffu, b1, s1);
+  b0 = c < 2 ? t0 : t1;
+  b1 = c < 2 ? t2 : t3;
 }
 
 // Per-column masks of a multi-token query: the lane's two score columns
@@ -1061,12 +1028,17 @@ __device__ __forceinline__ void groups_compute(const RowMap& km, const RowMap& v
     if constexpr (PK) {
       // lanes c < 2 give columns 0-3 (f16 parts), lanes c >= 2 columns 4-7
       const bool lo_cols = (lane & 2) != 0;
-      const uint32_t b0 = movmatrix_trans(lo_cols ? l01 : h01);
-      const uint32_t b1 = movmatrix_trans(lo_cols ? l23 : h23);
+      uint32_t b0 = movmatrix_trans(lo_cols ? l01 : h01);
+      uint32_t b1 = movmatrix_trans(lo_cols ? l23 : h23);
+      if constexpr (TK == TK_COLD) key_order_4c(lane, b0, b1);
       tile_pv<TK, D, PK>(vm, k0[g], lane, a.o, b0, b1, 0u, 0u);
     } else {
-      const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-      const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+      uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+      uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+      if constexpr (TK == TK_COLD) {
+        key_order_4c(lane, bh0, bh1);
+        key_order_4c(lane, bl0, bl1);
+      }
       tile_pv<TK, D, PK>(vm, k0[g], lane, a.o, bh0, bh1, bl0, bl1);
     }
   }

@@ -193,6 +193,18 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "memory");
 }
 
+// Two 16x16 byte matrices, transposed (sm_100-class parts): lanes 0-15 give
+// the 16 row addresses of the first, lanes 16-31 those of the second.
+// Lane (r = lane / 4, c = lane % 4) receives, of each matrix, rows 4c .. 4c+3
+// of column r (r0 / r2, one byte a row) and of column r + 8 (r1 / r3).
+__device__ __forceinline__ void ldsm_b8_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                                 uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
 // Transposes an 8x8 b16 matrix held in the mma fragment layout.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
