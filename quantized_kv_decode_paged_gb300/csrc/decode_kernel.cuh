@@ -1195,10 +1195,12 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   // after the tree merge's last barrier) holds every row of the unit: the
   // warps holding them (tg = 0) write normalized rows there, and all
   // consumer threads copy whole rows to global memory with 16-byte stores.
-  // Otherwise (the int8 tiered kernels with four slots, whose merge buffer
-  // is halved) the tg = 0 warps store their fragments directly.
+  // A slot has at most four rows in the packed kernels, else kHeadTile.
+  // Otherwise (the unpacked int8 tiered kernel with four slots, whose merge
+  // buffer is halved) the tg = 0 warps store their fragments directly.
   constexpr int SROW = D + 4;  // floats a staged row: D values, the lse, padding
-  constexpr bool STAGED = KVB * kHeadTile * SROW <= (NCW / 2) * red_floats(D, Gm::RED_PARTS);
+  constexpr int RPS = PK ? 4 : kHeadTile;  // staged rows a slot
+  constexpr bool STAGED = KVB * RPS * SROW <= (NCW / 2) * red_floats(D, Gm::RED_PARTS);
   constexpr int D4 = D / 4;
   auto row_dst = [&](int ks, int h, float*& dst, float*& ldst) {
     const int hgs = slot_hg<KVB>(p, s.hg, ks);
@@ -1229,7 +1231,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
       float* dst;
       float* ldst;
       if constexpr (STAGED) {
-        dst = red + (kvs * kHeadTile + h) * SROW;
+        dst = red + (kvs * RPS + h) * SROW;
         ldst = dst + D;
       } else {
         row_dst(kvs, h, dst, ldst);
@@ -1244,9 +1246,9 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   }
   if constexpr (STAGED) {
     named_bar_sync(kRedBarrier, NCW * 32);
-    for (int idx = tid; idx < KVB * kHeadTile * D4; idx += NCW * 32) {
+    for (int idx = tid; idx < KVB * RPS * D4; idx += NCW * 32) {
       const int d4 = idx % D4, lrow = idx / D4;
-      const int ks = lrow / kHeadTile, h = lrow % kHeadTile;
+      const int ks = lrow / RPS, h = lrow % RPS;
       if (h >= unit_nh(p, slot_hg<KVB>(p, s.hg, ks))) continue;
       const float* row = red + lrow * SROW;
       float* dst;
