@@ -335,6 +335,51 @@ int decode_attn_workspace_init(void* workspace, size_t workspace_bytes, void* st
 /* Static text for a da_status value. */
 const char* decode_attn_status_string(int status);
 
+/*
+ * Tuning of the kernel choice, process-wide.  These settings change which
+ * kernel instantiation and schedule a call uses, never what it computes.
+ * The pages have no counterpart; they have one kernel per variant.
+ *
+ * When the library is loaded, the fields are set from the environment
+ * variables DA_KVB, DA_FUSE_HG, DA_PACK, DA_MAX_STAGES and DA_WAIT_LIMIT_MS.
+ * The environment is read once, at load; unset or out-of-range values keep
+ * the defaults below.  decode_attn_set_tuning replaces every field;
+ * decode_attn_set_tuning(NULL) restores the load-time values.  A call that
+ * runs while another host thread changes the tuning may see a mix of old and
+ * new fields.  Each mix is a valid configuration.
+ */
+typedef struct {
+  int32_t kv_heads_per_unit; /* 0 = automatic (default); 1, 2 or 4 kv heads per
+                                work unit, used when a kernel exists and it
+                                divides num_kv_heads */
+  int32_t fuse_head_groups;  /* 1 (default): 2 or 4 head groups of 8 query rows
+                                of one kv head share a unit (each K/V byte is
+                                read once); 0: one unit per head group */
+  int32_t packed_operands;   /* 1 (default): with at most 4 query rows per kv
+                                head, the f16 and remainder parts of Q and P
+                                share one MMA operand; 0: two operands */
+  int32_t max_stages;        /* 0 (default): as many pipeline stages as fit in
+                                shared memory; else a cap in [2, 8] */
+  int32_t wait_limit_ms;     /* time limit of every wait inside the kernels,
+                                [1, 10000], default 2000; a wait that runs
+                                out sets DA_DEV_TIMEOUT (see the device flags) */
+} da_tuning;
+
+/* Copies the current tuning into *t.  DA_ERR_INVALID when t is NULL. */
+int decode_attn_get_tuning(da_tuning* t);
+
+/* Replaces the tuning (NULL: the load-time values).  DA_ERR_INVALID, with
+ * nothing changed, when a field is out of range. */
+int decode_attn_set_tuning(const da_tuning* t);
+
+/* Test hook, for tests of the bounded waits only: with on = 1, CTA 0 of
+ * every later decode launch leaves its first pipeline stage unarmed.  Its
+ * consumers' wait then runs out after wait_limit_ms.  The kernel ends in
+ * abort mode with DA_DEV_TIMEOUT set and a wrong output; nothing faults.
+ * on = 0 (the state at load) turns it off.  This hook is never set from the
+ * environment. */
+int decode_attn_testing_skip_first_arm(int32_t on);
+
 #ifdef __cplusplus
 }
 #endif

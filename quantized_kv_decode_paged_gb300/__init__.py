@@ -13,7 +13,6 @@ seq_lens i32 [B]; out f32 [B, Hq, D]; lse f32 [B, Hq].
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 from typing import Optional
@@ -26,7 +25,8 @@ __all__ = [
     "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_status_string",
     "decode_attn_paged_static_ws", "decode_attn_append_paged", "decode_attn_append_tiered_int8",
-    "decode_attn_append_tiered_f16", "DecodeAttnError", "DEV_BAD_BLOCK", "DEV_BAD_SEQ_LEN",
+    "decode_attn_append_tiered_f16", "DecodeAttnError", "DaTuning", "get_tuning", "set_tuning",
+    "tuning", "DEV_BAD_BLOCK", "DEV_BAD_SEQ_LEN",
     "DEV_BAD_QPOS", "DEV_SPLIT_OVERFLOW", "DEV_BAD_TIER", "DEV_TIMEOUT",
 ]
 
@@ -48,7 +48,8 @@ _EXPORTS = (
     "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_workspace_init",
     "decode_attn_status_string", "decode_attn_paged_static_ws", "decode_attn_append_paged",
-    "decode_attn_append_tiered_int8", "decode_attn_append_tiered_f16",
+    "decode_attn_append_tiered_int8", "decode_attn_append_tiered_f16", "decode_attn_get_tuning",
+    "decode_attn_set_tuning", "decode_attn_testing_skip_first_arm",
 )
 
 
@@ -76,6 +77,14 @@ class DaTierParams(ctypes.Structure):
         ("hot_start", ctypes.c_int32),
         ("cold_lens", ctypes.c_void_p), ("hot_lens", ctypes.c_void_p),
         ("hot_starts", ctypes.c_void_p),
+    ]
+
+
+class DaTuning(ctypes.Structure):
+    _fields_ = [
+        ("kv_heads_per_unit", ctypes.c_int32), ("fuse_head_groups", ctypes.c_int32),
+        ("packed_operands", ctypes.c_int32), ("max_stages", ctypes.c_int32),
+        ("wait_limit_ms", ctypes.c_int32),
     ]
 
 
@@ -140,6 +149,12 @@ def load_library():
         lib.decode_attn_append_tiered_f16.restype = ctypes.c_int
         lib.decode_attn_append_tiered_f16.argtypes = ([ctypes.POINTER(DaParams), i32, i32]
                                                       + [P] * 12)
+        lib.decode_attn_get_tuning.restype = ctypes.c_int
+        lib.decode_attn_get_tuning.argtypes = [ctypes.POINTER(DaTuning)]
+        lib.decode_attn_set_tuning.restype = ctypes.c_int
+        lib.decode_attn_set_tuning.argtypes = [ctypes.POINTER(DaTuning)]
+        lib.decode_attn_testing_skip_first_arm.restype = ctypes.c_int
+        lib.decode_attn_testing_skip_first_arm.argtypes = [ctypes.c_int32]
         lib.decode_attn_status_string.restype = ctypes.c_char_p
         lib.decode_attn_status_string.argtypes = [ctypes.c_int]
         _lib = lib
@@ -153,6 +168,48 @@ def decode_attn_status_string(status: int) -> str:
 def _check(fn: str, status: int):
     if status != DA_OK:
         raise DecodeAttnError(fn, status, decode_attn_status_string(status))
+
+
+# ---------------------------------------------------------------- tuning
+def get_tuning() -> dict:
+    """The library's current tuning (decode_attn_get_tuning) as a dict."""
+    t = DaTuning()
+    _check("decode_attn_get_tuning", load_library().decode_attn_get_tuning(ctypes.byref(t)))
+    return {name: int(getattr(t, name)) for name, _ in DaTuning._fields_}
+
+
+def set_tuning(**fields) -> None:
+    """Replaces the named tuning fields, keeping the others
+    (decode_attn_set_tuning).  With no fields: the load-time values."""
+    lib = load_library()
+    if not fields:
+        _check("decode_attn_set_tuning", lib.decode_attn_set_tuning(None))
+        return
+    cur = get_tuning()
+    unknown = set(fields) - set(cur)
+    if unknown:
+        raise TypeError(f"unknown tuning fields: {sorted(unknown)}")
+    cur.update(fields)
+    t = DaTuning(**{k: int(v) for k, v in cur.items()})
+    _check("decode_attn_set_tuning", lib.decode_attn_set_tuning(ctypes.byref(t)))
+
+
+class tuning:
+    """Context manager: ``with tuning(packed_operands=0): ...`` sets the named
+    fields for the block and puts the previous tuning back afterwards."""
+
+    def __init__(self, **fields):
+        self.fields = fields
+        self.saved = None
+
+    def __enter__(self):
+        self.saved = get_tuning()
+        set_tuning(**self.fields)
+        return self
+
+    def __exit__(self, *exc):
+        set_tuning(**self.saved)
+        return False
 
 
 # ---------------------------------------------------------------- marshalling
@@ -487,12 +544,6 @@ def decode_attn_split_merge(o_part, lse_part, *, out=None, lse=None, stream=None
                                      _ptr(lse), _stream(dev, stream))
     _check("decode_attn_split_merge", st)
     return out, lse
-
-
-def default_scale(head_dim: int) -> float:
-    """1/sqrt(D) rounded to f32 (what scale=0 selects)."""
-    import numpy as np
-    return float(np.float32(1.0 / math.sqrt(head_dim)))
 
 
 # ---------------------------------------------------------------------------

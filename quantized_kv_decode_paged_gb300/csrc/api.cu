@@ -8,6 +8,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/decode_attn.h"
@@ -40,19 +41,84 @@ EncodeTiledFn encode_fn() {
 
 constexpr int kMaxDevices = 128;
 
+// SM count of the current device, queried once per device.  Entries are
+// atomics: host threads making their first call together each store the same
+// value.
 int device_sms(int* sms_out) {
-  static int sms[kMaxDevices] = {0};
+  static std::atomic<int> sms[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DA_ERR_CUDA;
-  if (sms[dev] == 0) {
-    int v = 0;
+  int v = sms[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
       return DA_ERR_CUDA;
-    sms[dev] = v;
+    sms[dev].store(v, std::memory_order_relaxed);
   }
-  *sms_out = sms[dev];
+  *sms_out = v;
   return DA_OK;
 }
+
+// Process-wide tuning state.  Its initial values are read from the
+// environment once, when the library is loaded (DA_KVB, DA_FUSE_HG, DA_PACK,
+// DA_MAX_STAGES, DA_WAIT_LIMIT_MS; unset or invalid values keep the
+// defaults); decode_attn_set_tuning replaces them.  Every launch reads a
+// snapshot of the fields.  The test hook that leaves a stage unarmed is set
+// only through decode_attn_testing_skip_first_arm, never from the
+// environment.
+struct Tuning {
+  std::atomic<int> kvb{0};         // 0 = automatic, else 1, 2 or 4
+  std::atomic<int> fuse_hg{1};     // 0 = one unit per head group
+  std::atomic<int> pack{1};        // 0 = two-operand kernels always
+  std::atomic<int> max_stages{0};  // 0 = kMaxStages, else 2..kMaxStages
+  std::atomic<int> wait_ms{2000};  // 1..10000
+  std::atomic<int> skip_arm{0};    // test hook
+};
+
+bool valid_kvb(int v) { return v == 0 || v == 1 || v == 2 || v == 4; }
+bool valid_stages(int v) { return v == 0 || (v >= 2 && v <= da::kMaxStages); }
+bool valid_wait(int v) { return v >= 1 && v <= 10000; }
+
+da_tuning env_tuning() {
+  da_tuning t{0, 1, 1, 0, 2000};
+  auto env_int = [](const char* name, int* out) {
+    const char* e = getenv(name);
+    if (!e || !*e) return false;
+    char* end = nullptr;
+    const long v = strtol(e, &end, 10);
+    if (*end != '\0' || v < -1000000 || v > 1000000) return false;
+    *out = (int)v;
+    return true;
+  };
+  int v = 0;
+  if (env_int("DA_KVB", &v) && valid_kvb(v)) t.kv_heads_per_unit = v;
+  if (env_int("DA_FUSE_HG", &v) && (v == 0 || v == 1)) t.fuse_head_groups = v;
+  if (env_int("DA_PACK", &v) && (v == 0 || v == 1)) t.packed_operands = v;
+  if (env_int("DA_MAX_STAGES", &v) && valid_stages(v)) t.max_stages = v;
+  if (env_int("DA_WAIT_LIMIT_MS", &v) && valid_wait(v)) t.wait_limit_ms = v;
+  return t;
+}
+
+const da_tuning& load_time_tuning() {
+  static const da_tuning t = env_tuning();
+  return t;
+}
+
+Tuning& tuning() {
+  static Tuning* t = [] {
+    Tuning* x = new Tuning;
+    const da_tuning& e = load_time_tuning();
+    x->kvb = e.kv_heads_per_unit;
+    x->fuse_hg = e.fuse_head_groups;
+    x->pack = e.packed_operands;
+    x->max_stages = e.max_stages;
+    x->wait_ms = e.wait_limit_ms;
+    return x;
+  }();
+  return *t;
+}
+
+// Reads the environment when the library is loaded, not at the first call.
+const bool g_tuning_loaded = (tuning(), true);
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -95,12 +161,10 @@ float effective_qscale(const da_params* p) {
   return (float)s * 1.4426950408889634f;
 }
 
-// DA_KVB=n in the environment asks for n kv heads per unit (a tuning knob);
-// it is used only when an instantiation exists and n divides Hkv.
+// The tuning state's kv heads per unit, when set, replaces the automatic
+// choice if an instantiation exists and it divides Hkv.
 int kvb_override(int kind, int D, int Hkv, int kvb) {
-  const char* e = getenv("DA_KVB");
-  if (!e) return kvb;
-  const int v = atoi(e);
+  const int v = tuning().kvb.load(std::memory_order_relaxed);
   if (v >= 1 && Hkv % v == 0 && da::decode_geo(kind, D, v).W != 0) return v;
   return kvb;
 }
@@ -110,15 +174,14 @@ int kvb_override(int kind, int D, int Hkv, int kvb) {
 // kv head's head groups when there are 2 or 4 of them: the four warp slots
 // of a KVB = 4 instantiation then split as KVU kv heads x HGU head groups
 // (KVU * HGU = 4) and every K/V byte serves all the kv head's query rows
-// (read once instead of HG times).  DA_FUSE_HG=0 in the environment keeps
-// one head group per unit (a tuning and testing knob).
+// (read once instead of HG times).  The tuning state's fuse_head_groups = 0
+// keeps one head group per unit.
 void plan_units(KParams& k, int kind) {
   k.KVU = k.KVB;
   k.HGU = 1;
   k.hgu_shift = 0;
   k.HGN = k.HG;
-  const char* e = getenv("DA_FUSE_HG");
-  if (e && e[0] == '0' && e[1] == '\0') return;
+  if (tuning().fuse_hg.load(std::memory_order_relaxed) == 0) return;
   if (k.HG != 2 && k.HG != 4) return;
   const int kvu = 4 / k.HG;
   if (k.Hkv % kvu != 0 || da::decode_geo(kind, k.D, 4).W == 0) return;
@@ -131,30 +194,21 @@ void plan_units(KParams& k, int kind) {
 
 // Whether to launch the packed variant: at most four query heads per kv
 // head leave half of the MMA's eight columns free for the remainder parts.
-// DA_PACK=0 in the environment forces the unpacked variant (a tuning and
-// testing knob).
+// The tuning state's packed_operands = 0 forces the unpacked variant.
 bool use_packed(const KParams& k) {
   if (k.NH > 4) return false;
-  const char* e = getenv("DA_PACK");
-  return !(e && e[0] == '0' && e[1] == '\0');
+  return tuning().pack.load(std::memory_order_relaxed) != 0;
 }
 
-// Test knobs for the bounded waits.  DA_WAIT_LIMIT_MS sets the time limit
-// of every wait inside the kernels (default 2000 ms); DA_TEST_SKIP_ARM=1 makes
-// CTA 0 leave its first stage unarmed, so that its consumers' wait runs out
-// and the kernel ends in abort mode with DA_DEV_TIMEOUT (no copy is issued
-// for that stage and nothing faults).
+// Time limit of every wait inside the kernels (the tuning state's
+// wait_limit_ms), and the test hook that makes CTA 0 leave its first stage
+// unarmed, so that its consumers' wait runs out and the kernel ends in abort
+// mode with DA_DEV_TIMEOUT (no copy is issued for that stage and nothing
+// faults).
 unsigned long long wait_limit_ns() {
-  const char* e = getenv("DA_WAIT_LIMIT_MS");
-  long long ms = e ? atoll(e) : 2000;
-  if (ms < 1) ms = 1;
-  if (ms > 10000) ms = 10000;
-  return (unsigned long long)ms * 1000000ull;
+  return (unsigned long long)tuning().wait_ms.load(std::memory_order_relaxed) * 1000000ull;
 }
-int test_skip_arm() {
-  const char* e = getenv("DA_TEST_SKIP_ARM");
-  return (e && e[0] == '1' && e[1] == '\0') ? 1 : 0;
-}
+int test_skip_arm() { return tuning().skip_arm.load(std::memory_order_relaxed); }
 
 // T query tokens per sequence: T*G query rows per kv head, in head groups of
 // kHeadTile (the last one may be partial).
@@ -248,15 +302,11 @@ int encode_ring_map(CUtensorMap* m, const void* base, long long D, long long hea
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
-// Upper bound on pipeline stages: kMaxStages, or DA_MAX_STAGES from the
-// environment when set (a tuning knob; values below 2 are ignored).
+// Upper bound on pipeline stages: kMaxStages, or the tuning state's
+// max_stages when set.
 int max_stages() {
-  const char* e = getenv("DA_MAX_STAGES");
-  if (e) {
-    const int v = atoi(e);
-    if (v >= 2 && v <= da::kMaxStages) return v;
-  }
-  return da::kMaxStages;
+  const int v = tuning().max_stages.load(std::memory_order_relaxed);
+  return v >= 2 ? v : da::kMaxStages;
 }
 
 // Largest stage count (>= 2) whose layout fits in shared memory, or 0.
@@ -510,6 +560,16 @@ int paged_impl(const da_params* p, int T, const float* q, const uint16_t* k_pool
 
 }  // namespace
 
+namespace da {
+
+size_t workspace_ticket_bytes() {
+  int sms = 0;
+  if (device_sms(&sms) != DA_OK) return 0;
+  return ws_layout(sms, 64, 1).lse_off;
+}
+
+}  // namespace da
+
 extern "C" {
 
 const char* decode_attn_status_string(int status) {
@@ -528,6 +588,38 @@ size_t decode_attn_workspace_size(const da_params* p) {
   int sms = 0;
   if (device_sms(&sms) != DA_OK) return 0;
   return ws_layout(sms, p->head_dim, ws_kvb(p)).total;
+}
+
+int decode_attn_get_tuning(da_tuning* t) {
+  if (!t) return DA_ERR_INVALID;
+  Tuning& s = tuning();
+  t->kv_heads_per_unit = s.kvb.load();
+  t->fuse_head_groups = s.fuse_hg.load();
+  t->packed_operands = s.pack.load();
+  t->max_stages = s.max_stages.load();
+  t->wait_limit_ms = s.wait_ms.load();
+  return DA_OK;
+}
+
+int decode_attn_set_tuning(const da_tuning* t) {
+  const da_tuning& v = t ? *t : load_time_tuning();
+  if (!valid_kvb(v.kv_heads_per_unit) || (v.fuse_head_groups != 0 && v.fuse_head_groups != 1) ||
+      (v.packed_operands != 0 && v.packed_operands != 1) || !valid_stages(v.max_stages) ||
+      !valid_wait(v.wait_limit_ms))
+    return DA_ERR_INVALID;
+  Tuning& s = tuning();
+  s.kvb = v.kv_heads_per_unit;
+  s.fuse_hg = v.fuse_head_groups;
+  s.pack = v.packed_operands;
+  s.max_stages = v.max_stages;
+  s.wait_ms = v.wait_limit_ms;
+  return DA_OK;
+}
+
+int decode_attn_testing_skip_first_arm(int32_t on) {
+  if (on != 0 && on != 1) return DA_ERR_INVALID;
+  tuning().skip_arm = on;
+  return DA_OK;
 }
 
 int decode_attn_workspace_init(void* workspace, size_t bytes, void* stream) {

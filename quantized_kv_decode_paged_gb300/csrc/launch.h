@@ -29,6 +29,11 @@ GeoInfo decode_geo(int kind, int D, int KVB);
 cudaError_t launch_decode(int kind, int D, int KVB, bool packed, const KParams& p, dim3 grid,
                           int smem_bytes, cudaStream_t stream);
 
+// Bytes at the start of a stream-K workspace that hold the ticket counters
+// on the current device (they must be zero when a call starts); 0 when the
+// device cannot be queried.
+size_t workspace_ticket_bytes();
+
 // out/lse from max_splits partial states per (b, h).
 cudaError_t launch_split_merge(int rows, int max_splits, int D, const float* o_part,
                                const float* lse_part, float* out, float* lse,

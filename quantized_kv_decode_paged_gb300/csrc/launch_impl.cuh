@@ -2,22 +2,27 @@
 // the translation units that instantiate the decode kernel.
 #pragma once
 
+#include <atomic>
+
 #include "decode_kernel.cuh"
 #include "launch.h"
 
 namespace da {
 
+// The shared-memory opt-in of each instantiation is set once per device.
+// The flags are atomics: host threads making their first call together may
+// each set the (idempotent) attribute.
 template <int KIND, int D, int KVB, bool PK>
 cudaError_t launch_decode_impl(const KParams& p, dim3 grid, int smem, cudaStream_t stream) {
-  static int configured[128] = {0};
+  static std::atomic<int> configured[128];
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev >= 0 && dev < 128 && !configured[dev]) {
+  if (dev < 0 || dev >= 128 || !configured[dev].load(std::memory_order_acquire)) {
     err = cudaFuncSetAttribute(decode_attn_kernel<KIND, D, KVB, PK>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (err != cudaSuccess) return err;
-    configured[dev] = 1;
+    if (dev >= 0 && dev < 128) configured[dev].store(1, std::memory_order_release);
   }
   decode_attn_kernel<KIND, D, KVB, PK><<<grid, Geo<KIND, D, KVB>::THREADS, smem, stream>>>(p);
   return cudaGetLastError();

@@ -166,3 +166,106 @@ def test_product_package_does_not_import_the_oracle():
         assert "import oracle" not in src and "from oracle" not in src, f
     for f in list(pkg.rglob("*.cu")) + list(pkg.rglob("*.cuh")) + list(pkg.rglob("*.h")):
         assert "oracle" not in f.read_text().lower(), f
+
+
+# ---------------------------------------------------------------------------
+# tuning state
+# ---------------------------------------------------------------------------
+
+DEFAULT_TUNING = dict(kv_heads_per_unit=0, fuse_head_groups=1, packed_operands=1, max_stages=0,
+                      wait_limit_ms=2000)
+
+
+def test_tuning_defaults_set_validate_and_restore(lib):
+    qk.set_tuning()
+    assert qk.get_tuning() == DEFAULT_TUNING or os.environ.get("DA_KVB") is not None
+    with qk.tuning(packed_operands=0, max_stages=3):
+        t = qk.get_tuning()
+        assert t["packed_operands"] == 0 and t["max_stages"] == 3
+        assert t["fuse_head_groups"] == 1
+    assert qk.get_tuning()["packed_operands"] == 1
+    for bad in (dict(kv_heads_per_unit=3), dict(fuse_head_groups=2), dict(packed_operands=-1),
+                dict(max_stages=1), dict(max_stages=9), dict(wait_limit_ms=0),
+                dict(wait_limit_ms=10001)):
+        before = qk.get_tuning()
+        with pytest.raises(qk.DecodeAttnError):
+            qk.set_tuning(**bad)
+        assert qk.get_tuning() == before, bad
+    assert lib.decode_attn_get_tuning(None) == qk.DA_ERR_INVALID
+    assert lib.decode_attn_testing_skip_first_arm(2) == qk.DA_ERR_INVALID
+
+
+_LOAD_TIME_SCRIPT = r"""
+import json, os, sys
+sys.path.insert(0, sys.argv[1])
+import quantized_kv_decode_paged_gb300 as qk
+qk.load_library()
+first = qk.get_tuning()
+# the environment is read at load only: later changes have no effect
+os.environ["DA_PACK"] = "1"
+os.environ["DA_MAX_STAGES"] = "2"
+qk.set_tuning()
+print(json.dumps([first, qk.get_tuning()]))
+"""
+
+
+def test_environment_is_read_once_at_load(lib):
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, DA_PACK="0", DA_KVB="4", DA_FUSE_HG="0", DA_MAX_STAGES="5",
+               DA_WAIT_LIMIT_MS="750", DA_TEST_SKIP_ARM="1")
+    r = subprocess.run([sys.executable, "-c", _LOAD_TIME_SCRIPT, ROOT], env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    first, restored = json.loads(r.stdout.strip().splitlines()[-1])
+    want = dict(kv_heads_per_unit=4, fuse_head_groups=0, packed_operands=0, max_stages=5,
+                wait_limit_ms=750)
+    assert first == want and restored == want
+    # out-of-range values keep the defaults
+    env = dict(os.environ, DA_PACK="7", DA_KVB="3", DA_MAX_STAGES="1", DA_WAIT_LIMIT_MS="x")
+    r = subprocess.run([sys.executable, "-c", _LOAD_TIME_SCRIPT, ROOT], env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    first, _ = json.loads(r.stdout.strip().splitlines()[-1])
+    assert first == DEFAULT_TUNING
+
+
+def test_no_environment_read_per_call():
+    """The library source reads the environment in one place: the load-time
+    tuning reader."""
+    import pathlib
+    csrc = pathlib.Path(ROOT) / "quantized_kv_decode_paged_gb300" / "csrc"
+    hits = [(f.name, ln) for f in sorted(csrc.iterdir()) if f.suffix in (".cu", ".cuh", ".h")
+            for ln in f.read_text().splitlines() if "getenv" in ln]
+    assert len(hits) == 1 and hits[0][0] == "api.cu", hits
+    assert not any("DA_TEST" in f.read_text() for f in csrc.iterdir() if f.is_file())
+
+
+def test_tuning_from_many_threads(lib):
+    """Host threads setting and reading the tuning at once always see valid
+    values, and the calls return OK."""
+    import threading
+    errors = []
+
+    def worker(i):
+        try:
+            for j in range(300):
+                t = qk.DaTuning(kv_heads_per_unit=(0, 1, 2, 4)[(i + j) % 4],
+                                fuse_head_groups=j % 2, packed_operands=(j // 2) % 2,
+                                max_stages=(0, 2, 3, 8)[j % 4], wait_limit_ms=1 + j)
+                assert lib.decode_attn_set_tuning(ctypes.byref(t)) == qk.DA_OK
+                g = qk.DaTuning()
+                assert lib.decode_attn_get_tuning(ctypes.byref(g)) == qk.DA_OK
+                assert g.kv_heads_per_unit in (0, 1, 2, 4) and g.max_stages in (0, 2, 3, 8)
+                assert 1 <= g.wait_limit_ms <= 300
+        except Exception as e:  # pragma: no cover
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    qk.set_tuning()
+    assert not errors, errors

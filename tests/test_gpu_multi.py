@@ -47,12 +47,12 @@ def test_multi_token_group_sizes(T, G):
 
 
 @pytest.mark.parametrize("T,G", [(2, 8), (4, 4), (8, 4), (3, 4)])
-def test_multi_token_head_groups_one_unit_per_group(T, G, monkeypatch):
-    """DA_FUSE_HG=0: one unit per head group of T*G query rows (the default
+def test_multi_token_head_groups_one_unit_per_group(T, G):
+    """fuse_head_groups=0: one unit per head group of T*G query rows (the default
     puts 2 or 4 head groups of a kv head in one unit)."""
-    monkeypatch.setenv("DA_FUSE_HG", "0")
-    case = _case(520 + 10 * T + G, 128, 2 * G, 2, 16, LENS, T)
-    _check(case)
+    with qk.tuning(fuse_head_groups=0):
+        case = _case(520 + 10 * T + G, 128, 2 * G, 2, 16, LENS, T)
+        _check(case)
 
 
 @pytest.mark.parametrize("D", [64, 256])

@@ -59,29 +59,29 @@ def test_head_dims_and_group_sizes(D, G):
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("G", [1, 3, 4])
-def test_unpacked_variant_for_small_groups(D, G, monkeypatch):
+def test_unpacked_variant_for_small_groups(D, G):
     """Groups of at most four heads normally pack the f16 and remainder parts
-    of Q and P into one MMA operand; DA_PACK=0 selects the two-operand
-    variant, which must agree with the oracle as well."""
-    monkeypatch.setenv("DA_PACK", "0")
-    Hkv = 2
-    case = _case(150 + D + G, D, G * Hkv, Hkv, 16, EDGE_LENS[:: 2 if D == 256 else 1])
-    for mode in MODES:
-        _check_all_rows(case, mode)
+    of Q and P into one MMA operand; the tuning's packed_operands=0 selects
+    the two-operand variant, which must agree with the oracle as well."""
+    with qk.tuning(packed_operands=0):
+        Hkv = 2
+        case = _case(150 + D + G, D, G * Hkv, Hkv, 16, EDGE_LENS[:: 2 if D == 256 else 1])
+        for mode in MODES:
+            _check_all_rows(case, mode)
 
 
 @pytest.mark.parametrize("fuse", ["1", "0"])
 @pytest.mark.parametrize("D,G,Hkv", [(64, 16, 4), (128, 12, 2), (128, 16, 2), (128, 16, 4),
                                      (128, 32, 2), (256, 16, 2)])
-def test_head_groups_sharing_a_unit(D, G, Hkv, fuse, monkeypatch):
+def test_head_groups_sharing_a_unit(D, G, Hkv, fuse):
     """More than eight query heads per kv head: two or four head groups of
-    a kv head share one unit (each K/V byte read once); DA_FUSE_HG=0 keeps a
-    unit per head group.  Both must agree with the oracle, including a
+    a kv head share one unit (each K/V byte read once); the tuning's
+    fuse_head_groups=0 keeps a unit per head group.  Both must agree with the oracle, including a
     partial last group (G = 12)."""
-    monkeypatch.setenv("DA_FUSE_HG", fuse)
-    case = _case(700 + D + G + Hkv, D, G * Hkv, Hkv, 16, EDGE_LENS[::2])
-    for mode in MODES:
-        _check_all_rows(case, mode)
+    with qk.tuning(fuse_head_groups=int(fuse)):
+        case = _case(700 + D + G + Hkv, D, G * Hkv, Hkv, 16, EDGE_LENS[::2])
+        for mode in MODES:
+            _check_all_rows(case, mode)
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 256])

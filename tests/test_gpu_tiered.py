@@ -63,23 +63,23 @@ def test_tier_group_sizes(G):
 
 @pytest.mark.parametrize("fuse", ["1", "0"])
 @pytest.mark.parametrize("D,G,Hkv", [(128, 16, 2), (128, 16, 4), (128, 32, 2), (256, 16, 2)])
-def test_tier_head_groups_sharing_a_unit(D, G, Hkv, fuse, monkeypatch):
-    """Two or four head groups per kv head in one unit (DA_FUSE_HG=1, the
-    default) or one unit each (DA_FUSE_HG=0)."""
-    monkeypatch.setenv("DA_FUSE_HG", fuse)
-    case = wl.make_tiered(f"hg{D}_{G}_{Hkv}", 70 + G + D + Hkv, B=2, Hq=G * Hkv, Hkv=Hkv, D=D,
-                          block_size=16, cold_len=200, hot_len=70, hot_window=96, hot_start=200)
-    _check(case)
+def test_tier_head_groups_sharing_a_unit(D, G, Hkv, fuse):
+    """Two or four head groups per kv head in one unit (fuse_head_groups=1, the
+    default) or one unit each (fuse_head_groups=0)."""
+    with qk.tuning(fuse_head_groups=int(fuse)):
+        case = wl.make_tiered(f"hg{D}_{G}_{Hkv}", 70 + G + D + Hkv, B=2, Hq=G * Hkv, Hkv=Hkv, D=D,
+                              block_size=16, cold_len=200, hot_len=70, hot_window=96, hot_start=200)
+        _check(case)
 
 
 @pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("G", [1, 3, 4])
-def test_tier_unpacked_variant_for_small_groups(D, G, monkeypatch):
-    """DA_PACK=0: the two-operand variant for groups of at most four heads."""
-    monkeypatch.setenv("DA_PACK", "0")
-    case = wl.make_tiered(f"u{D}_{G}", 60 + G + D, B=2, Hq=2 * G, Hkv=2, D=D, block_size=16,
-                          cold_len=200, hot_len=70, hot_window=96, hot_start=200)
-    _check(case)
+def test_tier_unpacked_variant_for_small_groups(D, G):
+    """packed_operands=0 in the tuning: the two-operand variant for groups of at most four heads."""
+    with qk.tuning(packed_operands=0):
+        case = wl.make_tiered(f"u{D}_{G}", 60 + G + D, B=2, Hq=2 * G, Hkv=2, D=D, block_size=16,
+                              cold_len=200, hot_len=70, hot_window=96, hot_start=200)
+        _check(case)
 
 
 def test_tier_window_softcap_and_query_position():

@@ -66,19 +66,19 @@ def test_f16_tier_group_sizes(G):
 
 @pytest.mark.parametrize("fuse", ["1", "0"])
 @pytest.mark.parametrize("G", [16, 32])
-def test_f16_tier_head_groups_sharing_a_unit(G, fuse, monkeypatch):
-    monkeypatch.setenv("DA_FUSE_HG", fuse)
-    case = _tiered(f"fhg{G}", 155 + G, B=2, Hq=2 * G, Hkv=2, D=128, block_size=16,
-                   cold_len=200, hot_len=70, hot_window=96, hot_start=200)
-    _check(case)
+def test_f16_tier_head_groups_sharing_a_unit(G, fuse):
+    with qk.tuning(fuse_head_groups=int(fuse)):
+        case = _tiered(f"fhg{G}", 155 + G, B=2, Hq=2 * G, Hkv=2, D=128, block_size=16,
+                       cold_len=200, hot_len=70, hot_window=96, hot_start=200)
+        _check(case)
 
 
 @pytest.mark.parametrize("G", [1, 4])
-def test_f16_tier_unpacked_variant(G, monkeypatch):
-    monkeypatch.setenv("DA_PACK", "0")
-    case = _tiered(f"fu{G}", 150 + G, B=2, Hq=2 * G, Hkv=2, D=128, block_size=16,
-                   cold_len=200, hot_len=70, hot_window=96, hot_start=200)
-    _check(case)
+def test_f16_tier_unpacked_variant(G):
+    with qk.tuning(packed_operands=0):
+        case = _tiered(f"fu{G}", 150 + G, B=2, Hq=2 * G, Hkv=2, D=128, block_size=16,
+                       cold_len=200, hot_len=70, hot_window=96, hot_start=200)
+        _check(case)
 
 
 def test_f16_tier_window_softcap_and_query_position():
