@@ -37,7 +37,9 @@ if ROOT not in sys.path:
 METRIC = "decode-attn KV-cache HBM GB/s (% of GB300 peak); µs per decode step"
 SPEC_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_WORKLOAD = "paged"
+DEFAULT_WORKLOAD = "longctx"
+# The five serving shapes: every run reports each of them in "configs".
+CONFIG_WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx")
 
 
 def _env_int(name, default):
@@ -68,78 +70,113 @@ def kernel_source_hash():
 
 
 def profiled_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was taken from the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_attn_kernel_{workload}.md")
+    """DRAM bytes per launch of the decode kernel on this workload, from the
+    committed ncu record profiles/decode_attn_kernel_<workload>.json, when
+    that record was taken from the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_attn_kernel_{workload}.json")
     try:
-        txt = open(path).read()
-    except OSError:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if rec.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return float(m_bytes.group(1))
+    v = rec.get("dram_bytes_per_launch")
+    return float(v) if v is not None else None
 
 
 # --------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) during the timed region."""
+    """SM clock, power and clock-event reasons of one GPU, read in-process
+    through NVML (libnvidia-ml, read-only queries): one sample when the
+    timed region starts, one every 2 ms during it and one when it ends.
+    Nothing is changed on the GPU."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # clock-event reason bits of NVML
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index):
-        self.device_index = device_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, cuda_index):
+        self.cuda_index = cuda_index
+        self.samples = []
+        self.nvml = None
+        self.dev = None
+        self.error = None
+        self._stop = threading.Event()
+
+    def _open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        dev = ctypes.c_void_p()
+        bus = None
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(self.cuda_index)
+            bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        except Exception:
+            bus = None
+        ok = bus is not None and lib.nvmlDeviceGetHandleByPciBusId_v2(
+            bus.encode(), ctypes.byref(dev)) == 0
+        if not ok:
+            idx = self.cuda_index
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            if vis and all(x.strip().isdigit() for x in vis.split(",")):
+                idx = int(vis.split(",")[self.cuda_index])
+            if lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(dev)) != 0:
+                raise RuntimeError("no NVML handle for the device")
+        self.nvml, self.dev = lib, dev
+        mx = ctypes.c_uint()
+        self.sm_max = (float(mx.value)
+                       if lib.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx)) == 0 else None)
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons_fn = fn or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        import ctypes
+        lib, dev = self.nvml, self.dev
+        mhz, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if lib.nvmlDeviceGetClockInfo(dev, 1, ctypes.byref(mhz)) != 0:
+            return
+        p = float(mw.value) / 1e3 if lib.nvmlDeviceGetPowerUsage(dev, ctypes.byref(mw)) == 0 else None
+        r = int(rs.value) if self._reasons_fn(dev, ctypes.byref(rs)) == 0 else 0
+        self.samples.append((float(mhz.value), p, r))
+
+    def _loop(self):
+        while not self._stop.wait(0.002):
+            self.sample()
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.device_index)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
+            self._open()
+            self.sample()
+            self.t = threading.Thread(target=self._loop, daemon=True)
             self.t.start()
-        except (OSError, ValueError):
-            self.proc = None
+        except Exception as exc:  # clocks are reported as unavailable, never fatal
+            self.error = f"{type(exc).__name__}: {exc}"
+            self.nvml = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        if self.nvml is not None:
+            self._stop.set()
             self.t.join(timeout=2)
+            self.sample()
 
     def summary(self):
-        sm, smax, reasons = [], 0.0, set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax = max(smax, float(parts[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
-            return None
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "nvml", "error": self.error or "no samples"}
+        sm = sorted(x[0] for x in self.samples)
+        bits = 0
+        for _, _, r in self.samples:
+            bits |= r
+        power = [x[1] for x in self.samples if x[1] is not None]
+        return {"sm_mhz": sm[len(sm) // 2], "sm_min_mhz": sm[0], "sm_max_mhz": self.sm_max,
+                "reasons": sorted(n for b, n in self.REASONS.items() if bits & b),
+                "power_w_max": round(max(power), 1) if power else None,
+                "samples": len(sm), "source": "nvml, every 2 ms in the timed region"}
 
 
 # ------------------------------------------------------------------ workloads
@@ -396,6 +433,45 @@ def job_gbs(total_bytes_per_step, steps, ms):
 
 
 # ----------------------------------------------------------------- GPU arm
+def time_device_steps(step, flush, steps, warmup, stream, barrier, clk=None):
+    """`warmup` untimed steps, then `steps` steps each preceded by an L2
+    flush outside its CUDA events.  Returns (per-step ms, wall seconds of
+    the timed loop)."""
+    import contextlib
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with (clk if clk is not None else contextlib.nullcontext()):
+        barrier()
+        w0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        barrier()
+        wall = time.perf_counter() - w0
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], wall
+
+
+def config_entry(case, times_ms, peak):
+    """One workload's line in "configs": time per step and bandwidth."""
+    from quantized_kv_decode_paged_gb300.accounting import algorithmic_bytes
+    nbytes = algorithmic_bytes(case)["total"]
+    mean_ms = sum(times_ms) / len(times_ms)
+    gbs = nbytes / (mean_ms * 1e-3) / 1e9
+    return {"us_per_step": round(mean_ms * 1e3, 2),
+            "us_median": round(sorted(times_ms)[len(times_ms) // 2] * 1e3, 2),
+            "gb_per_s": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+            "frac_of_spec_8000": round(gbs / SPEC_HBM_GBS, 4),
+            "bytes_per_step": int(nbytes), "steps": len(times_ms),
+            "shape": describe(case)}
+
+
 def gpu_arm(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -434,23 +510,8 @@ def gpu_arm(args, rank, world):
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    barrier()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
-        barrier()
-        w0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        barrier()
-        wall = time.perf_counter() - w0
-    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    clk = ClockSampler(local)
+    times_ms, wall = time_device_steps(step, flush, args.steps, args.warmup, stream, barrier, clk)
     dev_ms = sum(times_ms)
     clocks = clk.summary()
 
@@ -499,6 +560,24 @@ def gpu_arm(args, rank, world):
 
     dev_ms_max, e2e_ms_max, total_bytes = aggregate_ranks(dev_ms, e2e_ms, bytes_per_step, world,
                                                           "cuda")
+    peak, peak_src = measured_hbm_peak()
+
+    # every serving shape, one GPU: same flush, fewer steps
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = {}
+        n_cfg = max(10, min(args.steps, args.config_steps))
+        for name in CONFIG_WORKLOADS:
+            if name == case.name:
+                configs[name] = config_entry(case, times_ms, peak)
+                continue
+            c = load_case(name)
+            tt = c.device_tensors("cuda")
+            st, _, _ = make_step(c, tt)
+            tms, _ = time_device_steps(st, flush, n_cfg, 3, stream, barrier)
+            configs[name] = config_entry(c, tms, peak)
+            del tt, st
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -517,7 +596,6 @@ def gpu_arm(args, rank, world):
         value = job_gbs(total_bytes, args.steps, dev_ms_max)
         per_launch_s = dev_ms / args.steps / launches_per_step * 1e-3
         achieved = bytes_per_step / launches_per_step / per_launch_s / 1e9
-        peak, peak_src = measured_hbm_peak()
         traffic = profiled_traffic(case.name)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -538,10 +616,12 @@ def gpu_arm(args, rank, world):
                          if peak_src == "measured" else "fallback",
                          "traffic": traffic},
             "cpu_baseline": cpu,
+            "configs": configs,
             "e2e": {"value": round(job_gbs(total_bytes, 1, e2e_ms_max), 2), "unit": "GB/s",
                     "us_per_step": round(e2e_ms_max * 1e3, 2),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
+            "kernel_source_hash": kernel_source_hash(),
             "clocks": clocks,
             "wall_s_timed_region": round(wall, 3),
             "step_us_min": round(min(times_ms) * 1e3, 2),
@@ -565,6 +645,10 @@ def main(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=4.0,
                     help="CPU work per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload entries of the five serving shapes")
+    ap.add_argument("--config-steps", type=int, default=200,
+                    help="timed steps of each entry in configs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -1,7 +1,6 @@
 """GPU parity of the multi-token query decode (T query tokens per sequence,
 each at its own position with its own causal / window bounds) against the
 double-precision oracle, plus the partial head groups it relies on."""
-import numpy as np
 import pytest
 
 import quantized_kv_decode_paged_gb300 as qk
@@ -91,23 +90,3 @@ def test_single_token_partial_head_groups(G):
         ref_out, ref_lse, _ = oracle_paged(case)
         out, lse = run_paged(case, t, mode)
         assert_parity(out.reshape(-1, case.D), lse.reshape(-1), ref_out, ref_lse, f"G{G}/{mode}")
-
-
-def test_speculative_workload_sampled_rows():
-    """The paged serving workload's shape with four query tokens per sequence
-    (speculative decoding), sampled rows against the oracle."""
-    import torch
-    meta_lens = wl.workload("paged").seq_lens
-    case = wl.make_paged("paged_spec4", 1, B=32, Hq=32, Hkv=8, D=128, block_size=16,
-                         seq_lens=meta_lens, num_blocks=65536, max_blocks=256, q_len=4)
-    t = case.device_tensors("cuda")
-    rng = np.random.default_rng(7)
-    rows = np.unique(rng.choice(case.B * 4 * case.Hq, size=64, replace=False))
-    ref_out, ref_lse, flags = oracle_paged(case, rows)
-    assert flags == 0
-    for mode in MODES:
-        out, lse = run_paged(case, t, mode)
-        assert_parity(out.reshape(-1, case.D)[rows], lse.reshape(-1)[rows], ref_out, ref_lse,
-                      f"spec4/{mode}")
-    del t
-    torch.cuda.empty_cache()

@@ -184,34 +184,6 @@ def test_repeated_calls_are_stable():
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-# --------------------------------------------------------------- full size
-def _sampled_rows(case, n, seed):
-    rng = np.random.default_rng(seed)
-    rows = rng.choice(case.B * case.Hq, size=min(n, case.B * case.Hq), replace=False)
-    # always include the longest and the shortest sequence
-    for b in (int(np.argmax(case.seq_lens)), int(np.argmin(case.seq_lens))):
-        rows = np.concatenate([rows, [b * case.Hq, b * case.Hq + case.Hq - 1]])
-    return np.unique(rows)
-
-
-@pytest.mark.parametrize("name", ["paged", "window", "longctx"])
-def test_full_size_workloads_sampled_rows(name):
-    import torch
-    case = wl.workload(name)
-    t = case.device_tensors("cuda")
-    rows = _sampled_rows(case, 40, 7)
-    ref_out, ref_lse, flags = oracle_paged(case, rows)
-    assert flags == 0
-    modes = ("stream", "units") if name != "paged" else MODES
-    for mode in modes:
-        out, lse = run_paged(case, t, mode, split_tokens=1024)
-        out = out.reshape(-1, case.D)[rows]
-        lse = lse.reshape(-1)[rows]
-        assert_parity(out, lse, ref_out, ref_lse, f"{name}/{mode}")
-    del t
-    torch.cuda.empty_cache()
-
-
 def test_workspace_reuse_across_shapes():
     """One zero-filled workspace serves calls of different head dims and
     batch shapes: only its leading ticket counters must stay zero."""

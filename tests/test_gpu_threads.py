@@ -7,7 +7,6 @@ their first call together, on a stream of their own, with a workspace of
 their own.  The threads use different cache kinds and kernels: paged, int8
 tiered and f16 tiered.  Every result must match the oracle.
 """
-import json
 import os
 import subprocess
 import sys

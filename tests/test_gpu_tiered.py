@@ -114,22 +114,6 @@ def test_tier_bad_block_is_masked_and_flagged():
     assert_parity(out.reshape(-1, case.D), lse.reshape(-1), ref_out, ref_lse, "tiered-bad")
 
 
-def test_tiered_workload_sampled_rows():
-    import torch
-    case = wl.workload("tiered")
-    t = case.device_tensors("cuda")
-    rng = np.random.default_rng(3)
-    rows = np.unique(rng.choice(case.B * case.Hq, size=48, replace=False))
-    ref_out, ref_lse, flags = oracle_tiered(case, rows)
-    assert flags == 0
-    for mode in MODES:
-        out, lse = run_tiered(case, t, mode)
-        assert_parity(out.reshape(-1, case.D)[rows], lse.reshape(-1)[rows], ref_out, ref_lse,
-                      f"tiered/{mode}")
-    del t
-    torch.cuda.empty_cache()
-
-
 def test_tier_large_batch_is_split_over_launches():
     """240 sequences of the int8 tiered cache: more than one launch keeps
     the pipeline depth of a small batch (the per-sequence plan shares
