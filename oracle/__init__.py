@@ -103,6 +103,10 @@ def _load():
             lib.oracle_decode_paged.restype = ctypes.c_int32
             lib.oracle_decode_paged.argtypes = [ctypes.POINTER(_PagedArgs), ctypes.c_void_p,
                                                 ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_decode_paged_sparse.restype = ctypes.c_int32
+            lib.oracle_decode_paged_sparse.argtypes = [
+                ctypes.POINTER(_PagedArgs), ctypes.POINTER(_SparseLayout), ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
             lib.oracle_decode_paged_split.restype = ctypes.c_int32
             lib.oracle_decode_paged_split.argtypes = [
                 ctypes.POINTER(_PagedArgs), ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
@@ -210,6 +214,37 @@ def decode_paged(q, k_pool, v_pool, block_table, seq_lens, q_pos=None, *, scale=
     out = np.zeros((n, D), dtype=np.float64)
     lse = np.zeros(n, dtype=np.float64)
     flags = _load().oracle_decode_paged(ctypes.byref(args), _ptr(rows_a), n, _ptr(out), _ptr(lse))
+    return out, lse, int(flags)
+
+
+class _SparseLayout(ctypes.Structure):
+    _fields_ = [("sparse_block", ctypes.c_int64), ("num_layouts", ctypes.c_int64),
+                ("num_rows", ctypes.c_int64), ("max_nnz", ctypes.c_int64),
+                ("row_ptr", ctypes.c_void_p), ("col_idx", ctypes.c_void_p)]
+
+
+def decode_paged_sparse(q, k_pool, v_pool, block_table, seq_lens, row_ptr, col_idx,
+                        sparse_block, q_pos=None, *, scale=0.0, softcap=0.0, sliding_window=0,
+                        causal=True, rows=None):
+    """Block-sparse paged decode (one query token): head h keeps the keys of
+    the sparse blocks that CSR row q_pos / sparse_block of layout
+    h % num_layouts lists.  row_ptr int32 [num_layouts, num_rows + 1],
+    col_idx int32 [num_layouts, max_nnz].  Returns (out [n, D], lse [n], flags)."""
+    keep = _Keep()
+    args, B, Hq, D, T = _paged_struct(keep, q, k_pool, v_pool, block_table, seq_lens, q_pos,
+                                      scale, softcap, sliding_window, causal)
+    assert T == 1
+    row_ptr = keep(row_ptr, np.int32)
+    col_idx = keep(col_idx, np.int32)
+    assert row_ptr.ndim == 2 and col_idx.ndim == 2 and row_ptr.shape[0] == col_idx.shape[0]
+    sl = _SparseLayout(int(sparse_block), row_ptr.shape[0], row_ptr.shape[1] - 1,
+                       col_idx.shape[1], _ptr(row_ptr), _ptr(col_idx))
+    rows_a = _rows_arg(rows)
+    n = B * Hq if rows_a is None else len(rows_a)
+    out = np.zeros((n, D), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    flags = _load().oracle_decode_paged_sparse(ctypes.byref(args), ctypes.byref(sl),
+                                               _ptr(rows_a), n, _ptr(out), _ptr(lse))
     return out, lse, int(flags)
 
 

@@ -33,7 +33,12 @@
  *       values are read as f16 and everything else is as in [T]).
  *   [S] com.microsoft.SparseAttention "sparse-attention.wgsl.jinja",
  *       combine_partials: m = max(m1, m2), d = d1 e^(m1-m) + d2 e^(m2-m),
- *       used here in its log-sum-exp form for the split merge.
+ *       used here in its log-sum-exp form for the split merge; and the
+ *       attention pass (main): head h reads layout h % NUM_LAYOUT, the query
+ *       at position q reads CSR row q / SPARSE_BLOCK of that layout, each
+ *       listed column c selects the SPARSE_BLOCK keys c*SPARSE_BLOCK .., the
+ *       CSR is a boolean block mask (a repeated column selects nothing
+ *       more), and causality bounds the keys at the query's position.
  *
  * Readings where the pages are silent (each also listed in the design
  * notes): the query position defaults to the last cached key; a row with no
@@ -224,6 +229,122 @@ static void paged_row(const oracle_paged_args* a, int64_t b, int64_t tq, int64_t
   free(s);
   free(rowaddr);
   free(vbuf);
+}
+
+/* ================================================================== */
+/* Block-sparse selection of key blocks [S]                            */
+/* ================================================================== */
+typedef struct {
+  int64_t sparse_block; /* keys per sparse block (SPARSE_BLOCK) */
+  int64_t num_layouts;  /* NUM_LAYOUT */
+  int64_t num_rows;     /* rows of each layout's CSR (row_ptr has num_rows + 1 entries) */
+  int64_t max_nnz;      /* column entries of each layout (COL_STRIDE) */
+  const int32_t* row_ptr; /* [num_layouts, num_rows + 1] */
+  const int32_t* col_idx; /* [num_layouts, max_nnz] */
+} oracle_sparse_layout;
+
+/*
+ * selected[c] = 1 when key block c is listed in CSR row `row` of layout
+ * `layout`, for c in [0, num_rows).  A row index outside the layout, a
+ * malformed row (start < 0, end < start or end > max_nnz) and a column id
+ * outside [0, num_rows) raise flag 1 and select nothing.
+ */
+static void sparse_row_blocks(const oracle_sparse_layout* sl, int64_t layout, int64_t row,
+                              unsigned char* selected, int32_t* flags) {
+  for (int64_t c = 0; c < sl->num_rows; ++c) selected[c] = 0;
+  if (row < 0 || row >= sl->num_rows) {
+    *flags |= ORACLE_FLAG_BAD_BLOCK;
+    return;
+  }
+  const int32_t* rp = sl->row_ptr + layout * (sl->num_rows + 1);
+  int64_t start = rp[row], end = rp[row + 1];
+  if (start < 0 || end < start || end > sl->max_nnz) {
+    *flags |= ORACLE_FLAG_BAD_BLOCK;
+    return;
+  }
+  const int32_t* cols = sl->col_idx + layout * sl->max_nnz;
+  for (int64_t e = start; e < end; ++e) {
+    int64_t c = cols[e];
+    if (c < 0 || c >= sl->num_rows) {
+      *flags |= ORACLE_FLAG_BAD_BLOCK;
+      continue;
+    }
+    selected[c] = 1;
+  }
+}
+
+/*
+ * Block-sparse paged decode, one query token: row (b, h) takes the paged
+ * row of paged_row over the keys whose sparse block is selected by CSR row
+ * qpos / sparse_block of layout h % num_layouts (qpos: q_pos[b] or
+ * seq_len - 1).  A query position that is negative empties the row (flag
+ * 4) before any layout row is read.
+ */
+static void sparse_paged_row(const oracle_paged_args* a, const oracle_sparse_layout* sl,
+                             int64_t b, int64_t h, double* out, double* lse, int32_t* flags) {
+  const int64_t D = a->D;
+  const int64_t G = a->Hq / a->Hkv;
+  const int64_t kv = h / G;
+  const double scale = effective_scale(a->scale, D);
+  int64_t L = paged_len(a, b, flags);
+  int64_t qpos = L - 1;
+  if (a->q_pos) {
+    qpos = a->q_pos[b];
+    if (qpos < 0) {
+      *flags |= ORACLE_FLAG_BAD_QPOS;
+      L = 0;
+    }
+  }
+  unsigned char* selected = (unsigned char*)malloc((size_t)(sl->num_rows + 1));
+  if (L > 0) {
+    sparse_row_blocks(sl, h % sl->num_layouts, qpos / sl->sparse_block, selected, flags);
+  } else {
+    for (int64_t c = 0; c < sl->num_rows; ++c) selected[c] = 0;
+  }
+  double* s = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+  int64_t* rowaddr = (int64_t*)malloc(sizeof(int64_t) * (size_t)(L + 1));
+  double* vbuf = (double*)malloc(sizeof(double) * (size_t)D);
+  const float* qrow = a->q + (b * a->Hq + h) * D;
+  int64_t n = 0;
+  for (int64_t t = 0; t < L; ++t) {
+    if (!key_visible(t, qpos, a->causal, a->window)) continue;
+    int64_t c = t / sl->sparse_block;
+    if (c >= sl->num_rows || !selected[c]) continue;
+    int64_t blk = a->block_table[b * a->max_blocks + t / a->block_size];
+    if (blk < 0 || blk >= a->num_blocks) {
+      *flags |= ORACLE_FLAG_BAD_BLOCK;
+      continue;
+    }
+    int64_t addr = ((blk * a->block_size + t % a->block_size) * a->Hkv + kv) * D;
+    const uint16_t* krow = a->k_pool + addr;
+    double dot = 0.0;
+    for (int64_t d = 0; d < D; ++d) dot += (double)qrow[d] * oracle_half_to_double(krow[d]);
+    s[n] = apply_softcap(scale * dot, a->softcap);
+    rowaddr[n] = addr;
+    ++n;
+  }
+  paged_vctx ctx = {a, rowaddr};
+  softmax_two_pass(s, n, D, paged_fetch_v, &ctx, vbuf, out, lse);
+  free(selected);
+  free(s);
+  free(rowaddr);
+  free(vbuf);
+}
+
+/* rows: flat row ids r = b*Hq + h (NULL => all); out [nrows, D], lse [nrows]. */
+int32_t oracle_decode_paged_sparse(const oracle_paged_args* a, const oracle_sparse_layout* sl,
+                                   const int64_t* rows, int64_t nrows, double* out,
+                                   double* lse) {
+  int32_t flags = 0;
+  if (!rows) nrows = a->B * a->Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : flags)
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t r = rows ? rows[i] : i;
+    int32_t f = 0;
+    sparse_paged_row(a, sl, r / a->Hq, r % a->Hq, out + i * a->D, lse + i, &f);
+    flags |= f;
+  }
+  return flags;
 }
 
 /*
