@@ -38,8 +38,9 @@ METRIC = "decode-attn KV-cache HBM GB/s (% of GB300 peak); µs per decode step"
 SPEC_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 DEFAULT_WORKLOAD = "longctx"
-# The five serving shapes: every run reports each of them in "configs".
-CONFIG_WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx")
+# The five serving shapes, and the paged one with block-sparse layouts: every
+# run reports each of them in "configs".
+CONFIG_WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx", "paged_sparse")
 
 
 def _env_int(name, default):
@@ -190,11 +191,15 @@ def describe(case):
     if isinstance(case, PagedCase):
         lens = case.seq_lens
         T = case.q.shape[1] if case.q.ndim == 4 else 1
-        return {"workload": case.name, "kind": "paged f16", "B": case.B, "q_len": T, "Hq": case.Hq,
-                "Hkv": case.Hkv, "D": case.D, "block_size": case.block_size,
-                "num_blocks": case.num_blocks, "seq_len_min": int(lens.min()),
-                "seq_len_max": int(lens.max()), "seq_len_mean": float(lens.mean()),
-                "sliding_window": case.sliding_window, "softcap": case.softcap}
+        d = {"workload": case.name, "kind": "paged f16", "B": case.B, "q_len": T, "Hq": case.Hq,
+             "Hkv": case.Hkv, "D": case.D, "block_size": case.block_size,
+             "num_blocks": case.num_blocks, "seq_len_min": int(lens.min()),
+             "seq_len_max": int(lens.max()), "seq_len_mean": float(lens.mean()),
+             "sliding_window": case.sliding_window, "softcap": case.softcap}
+        if case.sparse:
+            d.update(kind="paged f16, block-sparse layouts", sparse_block=case.sparse_block,
+                     num_layouts=int(case.row_ptr.shape[0]))
+        return d
     kind = "tiered f16 cold + f16 hot ring" if case.cold_f16 else "tiered int8 cold + f16 hot ring"
     return {"workload": case.name, "kind": kind, "B": case.B,
             "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D, "block_size": case.block_size,
@@ -266,6 +271,14 @@ def make_step(case, t):
         fn = qk.decode_attn_paged_multi if multi else qk.decode_attn_paged
 
         def step(q=None, block_table=None, seq_lens=None):
+            if case.sparse:
+                return qk.decode_attn_paged_sparse(
+                    t["q"] if q is None else q, t["k_pool"], t["v_pool"],
+                    t["block_table"] if block_table is None else block_table,
+                    t["seq_lens"] if seq_lens is None else seq_lens, t["row_ptr"], t["col_idx"],
+                    case.sparse_block, t["q_pos"], max_seq_len=case.max_seq_len,
+                    scale=case.scale, softcap=case.softcap, sliding_window=case.sliding_window,
+                    causal=case.causal, out=out, lse=lse, workspace=ws)
             return fn(
                 t["q"] if q is None else q, t["k_pool"], t["v_pool"],
                 t["block_table"] if block_table is None else block_table,
@@ -318,7 +331,11 @@ def oracle_sample(case, target_s, max_units=None):
     is_paged = isinstance(case, PagedCase)
     T = case.q.shape[1] if case.q.ndim == 4 else 1  # query tokens per sequence
 
-    def unit_bytes(b):
+    def unit_bytes(b, kv):
+        if is_paged and case.sparse:
+            from quantized_kv_decode_paged_gb300.accounting import sparse_selection
+            ranges, _ = sparse_selection(case, b)
+            return sum(z - a for a, z in ranges[kv]) * case.D * 2 * 2 + G * case.D * 8
         if is_paged:
             L = int(case.seq_lens[b])
             lo, _ = visible_range(L, L - T, case.causal, case.sliding_window)
@@ -332,7 +349,15 @@ def oracle_sample(case, target_s, max_units=None):
         rows = np.array([(b * T + t) * case.Hq + kv * G + g for (b, kv) in sel
                          for t in range(T) for g in range(G)])
         seqs = sorted({b for b, _ in sel})
-        if is_paged:
+        if is_paged and case.sparse:
+            kp, vp = case.host_pools(seqs)
+            t0 = time.perf_counter()
+            oracle.decode_paged_sparse(case.q, kp, vp, case.block_table, case.seq_lens,
+                                       case.row_ptr, case.col_idx, case.sparse_block, case.q_pos,
+                                       scale=case.scale, softcap=case.softcap,
+                                       sliding_window=case.sliding_window, causal=case.causal,
+                                       rows=rows)
+        elif is_paged:
             kp, vp = case.host_pools(seqs)
             t0 = time.perf_counter()
             oracle.decode_paged(case.q, kp, vp, case.block_table, case.seq_lens, case.q_pos,
@@ -372,7 +397,7 @@ def oracle_sample(case, target_s, max_units=None):
     if dt < target_s and n == len(order):
         reps = max(1, int(target_s / max(dt, 1e-6)))
         dt = sum(run(sel) for _ in range(reps))
-    nbytes = sum(unit_bytes(b) for b, _ in sel) * reps
+    nbytes = sum(unit_bytes(b, kv) for b, kv in sel) * reps
     desc = (f"{n} of {len(units)} (sequence, kv head) units of workload '{case.name}' "
             f"({n * G} query-head rows) x {reps} repetition(s), keys in logical order, "
             f"double precision")
@@ -639,7 +664,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["tiny", "paged", "tiered", "window", "longctx", "paged_compact",
-                             "tiered_f16", "paged_spec2", "paged_spec4"])
+                             "tiered_f16", "paged_spec2", "paged_spec4", "paged_sparse"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0,

@@ -147,6 +147,50 @@ int decode_attn_paged_multi(const da_params* p, int32_t q_len, const float* q,
                             size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * Block-sparse layouts for decode_attn_paged_sparse, in the CSR form of
+ * com.microsoft.SparseAttention "sparse-attention.wgsl.jinja" (the attention
+ * pass, main): query head h reads layout h % num_layouts; the query at
+ * position qpos reads row qpos / sparse_block of that layout; the row lists
+ * col_idx[layout][row_ptr[layout][row] .. row_ptr[layout][row + 1]), and
+ * each listed column c selects the sparse_block keys c*sparse_block ..
+ * (c+1)*sparse_block - 1.  The CSR is a boolean mask: a repeated column
+ * selects nothing more.  Both arrays are DEVICE pointers owned by the
+ * caller and are only read.
+ */
+typedef struct {
+  int32_t sparse_block;   /* keys per sparse block: a power of two, >= 16           */
+  int32_t num_layouts;    /* >= 1                                                  */
+  int32_t num_rows;       /* rows of every layout (row_ptr has num_rows + 1 per layout) */
+  int32_t max_nnz;        /* column entries per layout (row offsets lie in [0, max_nnz]) */
+  const int32_t* row_ptr; /* i32 [num_layouts, num_rows + 1]                        */
+  const int32_t* col_idx; /* i32 [num_layouts, max_nnz]                             */
+} da_sparse_layout;
+
+/*
+ * decode_attn_paged_sparse — block-sparse decode attention (one query token
+ * per sequence) over the f16 paged cache.  Row (b, h) attends to the keys of
+ * the blocks its layout's row selects, within the causal and sliding-window
+ * bounds of decode_attn_paged at qpos (q_pos[b], or seq_len - 1).  A row
+ * that selects no key gets out = 0 and lse = -inf.  Device-side problems
+ * never fault: a row index past num_rows, a malformed row (start < 0,
+ * end < start or end > max_nnz) and a column outside [0, num_rows) select
+ * nothing and set DA_DEV_BAD_BLOCK; a length above p->max_seq_len is
+ * clamped to it and sets DA_DEV_BAD_SEQ_LEN.
+ * Only the pages of blocks some head selects are read, once for all the
+ * query heads of a kv head.  p->max_seq_len must be > 0: it sizes the
+ * selection bitmasks each CTA keeps in shared memory, and a batch whose
+ * bitmasks do not fit is run in several launches.
+ * Everything else (layouts, workspace, q_pos, out, lse, stream) as for
+ * decode_attn_paged.  DA_ERR_INVALID for a sparse_block that is not a power
+ * of two >= 16 or a layout description out of range.
+ */
+int decode_attn_paged_sparse(const da_params* p, const da_sparse_layout* sl, const float* q,
+                             const uint16_t* k_pool, const uint16_t* v_pool,
+                             const int32_t* block_table, const int32_t* seq_lens,
+                             const int32_t* q_pos, float* out, float* lse, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * Tier geometry for decode_attn_tiered_int8 and decode_attn_tiered_f16.
  * Cold keys have absolute positions 0 .. cold_len-1 and are paged through
  * block_table (the f16 "coldPageTable" layout of doppler attention.js

@@ -21,8 +21,8 @@ from . import _build
 
 __all__ = [
     "load_library", "library_path", "build",
-    "decode_attn_paged", "decode_attn_paged_multi", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
-    "decode_attn_split_partial",
+    "decode_attn_paged", "decode_attn_paged_multi", "decode_attn_paged_sparse",
+    "decode_attn_tiered_int8", "decode_attn_tiered_f16", "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_status_string",
     "decode_attn_paged_static_ws", "decode_attn_append_paged", "decode_attn_append_tiered_int8",
     "decode_attn_append_tiered_f16", "DecodeAttnError", "DaTuning", "get_tuning", "set_tuning",
@@ -44,7 +44,7 @@ DA_ERR_WORKSPACE = -3
 DA_ERR_CUDA = -4
 
 _EXPORTS = (
-    "decode_attn_paged", "decode_attn_paged_multi", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
+    "decode_attn_paged", "decode_attn_paged_multi", "decode_attn_paged_sparse", "decode_attn_tiered_int8", "decode_attn_tiered_f16",
     "decode_attn_split_partial",
     "decode_attn_split_merge", "decode_attn_workspace_size", "decode_attn_workspace_init",
     "decode_attn_status_string", "decode_attn_paged_static_ws", "decode_attn_append_paged",
@@ -77,6 +77,14 @@ class DaTierParams(ctypes.Structure):
         ("hot_start", ctypes.c_int32),
         ("cold_lens", ctypes.c_void_p), ("hot_lens", ctypes.c_void_p),
         ("hot_starts", ctypes.c_void_p),
+    ]
+
+
+class DaSparseLayout(ctypes.Structure):
+    _fields_ = [
+        ("sparse_block", ctypes.c_int32), ("num_layouts", ctypes.c_int32),
+        ("num_rows", ctypes.c_int32), ("max_nnz", ctypes.c_int32),
+        ("row_ptr", ctypes.c_void_p), ("col_idx", ctypes.c_void_p),
     ]
 
 
@@ -121,6 +129,10 @@ def load_library():
         lib.decode_attn_paged_multi.restype = ctypes.c_int
         lib.decode_attn_paged_multi.argtypes = [ctypes.POINTER(DaParams), i32, P, P, P, P, P, P,
                                                 P, P, P, ctypes.c_size_t, P, P]
+        lib.decode_attn_paged_sparse.restype = ctypes.c_int
+        lib.decode_attn_paged_sparse.argtypes = [ctypes.POINTER(DaParams),
+                                                 ctypes.POINTER(DaSparseLayout), P, P, P, P, P,
+                                                 P, P, P, P, ctypes.c_size_t, P, P]
         lib.decode_attn_tiered_int8.restype = ctypes.c_int
         lib.decode_attn_tiered_int8.argtypes = [ctypes.POINTER(DaParams),
                                                 ctypes.POINTER(DaTierParams), P, P, P, P, P, P,
@@ -399,6 +411,56 @@ def decode_attn_paged_static_ws(q, k_pool, v_pool, block_table, seq_lens, q_pos=
                                          _ptr(q_pos), _ptr(out), _ptr(lse), _ptr(dev_status),
                                          _stream(dev, stream))
     _check("decode_attn_paged_static_ws", st)
+    return out, lse
+
+
+def decode_attn_paged_sparse(q, k_pool, v_pool, block_table, seq_lens, row_ptr, col_idx,
+                             sparse_block, q_pos=None, *, max_seq_len, scale=0.0, softcap=0.0,
+                             sliding_window=0, causal=True, out=None, lse=None, workspace="auto",
+                             dev_status=None, stream=None):
+    """Block-sparse paged decode attention (one query token per sequence).
+    Head h keeps the keys of the blocks that CSR row q_pos / sparse_block of
+    layout h % num_layouts lists.  row_ptr int32 [num_layouts, num_rows + 1]
+    and col_idx int32 [num_layouts, max_nnz] on the device; max_seq_len (> 0)
+    bounds seq_lens.  Returns (out [B, Hq, D] f32, lse [B, Hq] f32)."""
+    torch = _torch()
+    lib = load_library()
+    dev = q.device
+    _req(q, "q", torch.float32, dev, 3)
+    _req(k_pool, "k_pool", torch.float16, dev, 4)
+    _req(v_pool, "v_pool", torch.float16, dev, 4)
+    _req(block_table, "block_table", torch.int32, dev, 2)
+    _req(seq_lens, "seq_lens", torch.int32, dev, 1)
+    _req(row_ptr, "row_ptr", torch.int32, dev, 2)
+    _req(col_idx, "col_idx", torch.int32, dev, 2)
+    if q_pos is not None:
+        _req(q_pos, "q_pos", torch.int32, dev, 1)
+    if k_pool.shape != v_pool.shape:
+        raise ValueError("k_pool and v_pool shapes differ")
+    if row_ptr.shape[0] != col_idx.shape[0]:
+        raise ValueError("row_ptr and col_idx describe different numbers of layouts")
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_pool.shape
+    if D2 != D or block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _req(out, "out", torch.float32, dev, 3)
+    _req(lse, "lse", torch.float32, dev, 2)
+    if dev_status is not None:
+        _req(dev_status, "dev_status", torch.int32, dev)
+    params = make_params(q, bs, Hkv, block_table.shape[1], NB, scale=scale, softcap=softcap,
+                         sliding_window=sliding_window, causal=causal, max_seq_len=max_seq_len)
+    sl = DaSparseLayout(int(sparse_block), int(row_ptr.shape[0]), int(row_ptr.shape[1] - 1),
+                        int(col_idx.shape[1]), _ptr(row_ptr), _ptr(col_idx))
+    ws_ptr, ws_bytes = _workspace_args(workspace, params, dev)
+    st = lib.decode_attn_paged_sparse(ctypes.byref(params), ctypes.byref(sl), _ptr(q),
+                                      _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                      _ptr(seq_lens), _ptr(q_pos), _ptr(out), _ptr(lse), ws_ptr,
+                                      ws_bytes, _ptr(dev_status), _stream(dev, stream))
+    _check("decode_attn_paged_sparse", st)
     return out, lse
 
 

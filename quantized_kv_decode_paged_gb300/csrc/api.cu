@@ -313,10 +313,10 @@ int max_stages() {
 // A stage holds the K and V of the unit's KVU kv heads: REGION >> hgu_shift
 // bytes each.
 int pick_stages(int kind, int D, int KVB, const da::GeoInfo& g, int hgu_shift, int NH, int Hkv,
-                int nplan, int* smem_out) {
+                int nplan, int* smem_out, int sp_words = 0) {
   for (int s = max_stages(); s >= 2; --s) {
     SmemLayout L = da::make_layout(kind, D, KVB, g.W, g.REGION >> hgu_shift, g.TOK, NH, Hkv, s,
-                                   nplan);
+                                   nplan, sp_words);
     if (L.total <= da::kSmemLimit) {
       *smem_out = L.total;
       return s;
@@ -348,7 +348,8 @@ WsLayout ws_layout(int grid, int D, int kvb) {
 int ws_kvb(const da_params* p) {
   const int D = p->head_dim, H = p->num_kv_heads;
   int m = 0;
-  for (int kind : {da::KIND_PAGED, da::KIND_TIERED, da::KIND_TIERED_F16, da::KIND_PAGED_MULTI}) {
+  for (int kind : {da::KIND_PAGED, da::KIND_TIERED, da::KIND_TIERED_F16, da::KIND_PAGED_MULTI,
+                   da::KIND_PAGED_SPARSE}) {
     int v = kvb_override(kind, D, H, da::decode_kvb(kind, D, H));
     for (int f = 4; f > v; f /= 2)
       if (da::decode_geo(kind, D, f).W != 0) {
@@ -395,14 +396,21 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
     const da::GeoInfo g = da::decode_geo(lc.kind, base.D, base.KVB);
     if (g.W == 0) return DA_ERR_UNSUPPORTED;
     int sm_small = 0, sm_c = 0;
-    const int small = p->batch < 16 ? p->batch : 16;
-    const int s_small =
-        pick_stages(lc.kind, base.D, base.KVB, g, base.hgu_shift, base.NH, base.Hkv, small, &sm_small);
-    while (chunk > small &&
-           pick_stages(lc.kind, base.D, base.KVB, g, base.hgu_shift, base.NH, base.Hkv, chunk,
-                       &sm_c) < s_small)
-      chunk -= 8;
-    if (chunk < 1) chunk = 1;
+    int small = p->batch < 16 ? p->batch : 16;
+    auto stages_for = [&](int nplan, int* sm) {
+      return pick_stages(lc.kind, base.D, base.KVB, g, base.hgu_shift, base.NH, base.Hkv, nplan, sm,
+                         base.sp_words);
+    };
+    int s_small = stages_for(small, &sm_small);
+    // a per-sequence area too large for sixteen sequences (block-sparse
+    // bitmasks of long sequences): fewer sequences a launch
+    while (s_small == 0 && small > 1) {
+      small = (small + 1) / 2;
+      s_small = stages_for(small, &sm_small);
+    }
+    if (s_small == 0) return DA_ERR_UNSUPPORTED;
+    while (chunk > small && stages_for(chunk, &sm_c) < s_small) chunk -= 8;
+    if (chunk < small) chunk = small;
     const int nchunks = (p->batch + chunk - 1) / chunk;
     chunk = (p->batch + nchunks - 1) / nchunks;
   }
@@ -415,7 +423,7 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
     const da::GeoInfo g = da::decode_geo(lc.kind, k.D, k.KVB);
     if (g.W == 0) return DA_ERR_UNSUPPORTED;
     int smem = 0;
-    k.stages = pick_stages(lc.kind, k.D, k.KVB, g, k.hgu_shift, k.NH, k.Hkv, nb, &smem);
+    k.stages = pick_stages(lc.kind, k.D, k.KVB, g, k.hgu_shift, k.NH, k.Hkv, nb, &smem, k.sp_words);
     if (k.stages == 0) return DA_ERR_UNSUPPORTED;
     int grid;
     if (use_ws) {
@@ -558,6 +566,71 @@ int paged_impl(const da_params* p, int T, const float* q, const uint16_t* k_pool
   return run_batched(k, lc, off, static_cast<cudaStream_t>(stream));
 }
 
+// Block-sparse paged decode (one query token): the paged path with per-head
+// key blocks from the CSR layouts.
+int sparse_impl(const da_params* p, const da_sparse_layout* sl, const float* q,
+                const uint16_t* k_pool, const uint16_t* v_pool, const int32_t* block_table,
+                const int32_t* seq_lens, const int32_t* q_pos, float* out, float* lse,
+                void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  int st = check_params(p, false);
+  if (st != DA_OK) return st;
+  if (!sl || !q || !k_pool || !v_pool || !block_table || !seq_lens || !out) return DA_ERR_INVALID;
+  if (!sl->row_ptr || (!sl->col_idx && sl->max_nnz > 0)) return DA_ERR_INVALID;
+  if (sl->num_layouts < 1 || sl->num_rows < 1 || sl->max_nnz < 0) return DA_ERR_INVALID;
+  if (sl->sparse_block < 16 || sl->sparse_block > (1 << 20) || !pow2(sl->sparse_block))
+    return DA_ERR_INVALID;
+  if ((long long)sl->num_layouts * (sl->num_rows + 1) > 0x7fffffffLL ||
+      (long long)sl->num_layouts * sl->max_nnz > 0x7fffffffLL)
+    return DA_ERR_UNSUPPORTED;
+  if (p->max_seq_len <= 0) return DA_ERR_INVALID;  // sizes the selection bitmasks
+  if (!workspace && workspace_bytes) return DA_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || (q_pos && !aligned(q_pos, 4)) ||
+      (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)) ||
+      !aligned(sl->row_ptr, 4) || (sl->col_idx && !aligned(sl->col_idx, 4)))
+    return DA_ERR_INVALID;
+  if (p->batch == 0) return DA_OK;
+  KParams k;
+  memset(&k, 0, sizeof(k));
+  fill_common(k, p);
+  const int kind = da::KIND_PAGED_SPARSE;
+  k.KVB = kvb_override(kind, p->head_dim, p->num_kv_heads,
+                       da::decode_kvb(kind, p->head_dim, p->num_kv_heads));
+  plan_units(k, kind);
+  st = encode_paged_maps(k, kind, k_pool, v_pool, p);
+  if (st != DA_OK) return st;
+  const da::GeoInfo g = da::decode_geo(kind, p->head_dim, k.KVB);
+  if (g.W == 0) return DA_ERR_UNSUPPORTED;
+  k.dev_status = dev_status;
+  k.sp_row_ptr = sl->row_ptr;
+  k.sp_col_idx = sl->col_idx;
+  k.sp_nl = sl->num_layouts;
+  k.sp_nlu = sl->num_layouts < p->num_q_heads ? sl->num_layouts : p->num_q_heads;
+  k.sp_rows = sl->num_rows;
+  k.sp_nnz = sl->max_nnz;
+  k.sp_log2_block = ilog2(sl->sparse_block);
+  k.sp_max_len = p->max_seq_len;
+  {
+    const long long tiles = ((long long)p->max_seq_len + g.TOK - 1) / g.TOK;
+    long long blocks = ((long long)p->max_seq_len + sl->sparse_block - 1) / sl->sparse_block;
+    if (blocks > sl->num_rows) blocks = sl->num_rows;
+    k.sp_tw = (int)((tiles + 31) / 32);
+    k.sp_bw = (int)((blocks + 31) / 32);
+    k.sp_words = da::sparse_words(k.sp_tw, k.sp_bw, k.sp_nlu);
+  }
+  Launch lc{kind, p, workspace, workspace_bytes};
+  const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
+  auto off = [&](KParams& kk, int b0) {
+    kk.q = q + (long long)b0 * Hq * D;
+    kk.block_table = block_table + (long long)b0 * mb;
+    kk.seq_lens = seq_lens + b0;
+    kk.q_pos = q_pos ? q_pos + b0 : nullptr;
+    kk.out = out + (long long)b0 * Hq * D;
+    kk.lse = lse ? lse + (long long)b0 * Hq : nullptr;
+  };
+  return run_batched(k, lc, off, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 namespace da {
@@ -637,6 +710,15 @@ int decode_attn_paged(const da_params* p, const float* q, const uint16_t* k_pool
                       void* stream) {
   return paged_impl(p, 1, q, k_pool, v_pool, block_table, seq_lens, q_pos, out, lse, workspace,
                     workspace_bytes, dev_status, stream);
+}
+
+int decode_attn_paged_sparse(const da_params* p, const da_sparse_layout* sl, const float* q,
+                             const uint16_t* k_pool, const uint16_t* v_pool,
+                             const int32_t* block_table, const int32_t* seq_lens,
+                             const int32_t* q_pos, float* out, float* lse, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return sparse_impl(p, sl, q, k_pool, v_pool, block_table, seq_lens, q_pos, out, lse, workspace,
+                     workspace_bytes, dev_status, stream);
 }
 
 int decode_attn_paged_multi(const da_params* p, int32_t q_len, const float* q,

@@ -138,6 +138,8 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
     L = p.seq_lens[b];
     if (L < 0) { flags |= DEV_BAD_SEQ_LEN; L = 0; }
     if (L > cap) { flags |= DEV_BAD_SEQ_LEN; L = cap; }
+    // the block-sparse bitmasks cover the host's length bound
+    if (KIND == KIND_PAGED_SPARSE && L > p.sp_max_len) { flags |= DEV_BAD_SEQ_LEN; L = p.sp_max_len; }
     qp = L - p.q_len;  // query token 0; the T new tokens are the last T keys
   } else {
     cl = p.cold_lens ? p.cold_lens[b] : p.cold_len;
@@ -165,6 +167,7 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
   if (hi > 0x7fffffff) hi = 0x7fffffff;
   e.lo = (int)lo;
   e.hi = (int)hi;
+  if (is_paged(KIND)) e.cold_len = empty ? 0 : (int)L;  // the clamped length
   if (empty) return flags;
   if (is_paged(KIND)) {
     long long vh = hi < L ? hi : L;
@@ -488,9 +491,34 @@ __device__ __forceinline__ int stream_slot(int c, int c0, long long g0, long lon
   return c * 2 + j;
 }
 
-// Absolute tile of unit-local tile i (tiered: hot tiles follow cold ones).
+// Block-sparse kind: the sequence's area of `words` words (sparse_words).
+__device__ __forceinline__ const uint32_t* sparse_area(const uint32_t* sp_base, const KParams& p,
+                                                       int b) {
+  return sp_base + (size_t)b * p.sp_words;
+}
+
+// Tile of the i-th set bit of a sequence's tile bitmask: the last word
+// whose count of earlier set bits is <= i holds it.
+__device__ __forceinline__ int sparse_select(const uint32_t* area, int tw, int i) {
+  const uint32_t* pc = area + tw;
+  int lo = 0, hi = tw;  // pc[lo] <= i
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int)pc[mid] <= i) lo = mid; else hi = mid;
+  }
+  const int bit = (int)__fns(area[lo], 0u, i - (int)pc[lo] + 1);
+  return 32 * lo + bit;
+}
+
+// Absolute tile of unit-local tile i (tiered: hot tiles follow cold ones;
+// block-sparse: the i-th tile that holds a selected key).
 template <int KIND>
-__device__ __forceinline__ int tile_of(const SeqPlan& e, int i, bool& is_hot) {
+__device__ __forceinline__ int tile_of(const SeqPlan& e, int i, bool& is_hot,
+                                       const uint32_t* sp_area = nullptr, int sp_tw = 0) {
+  if constexpr (KIND == KIND_PAGED_SPARSE) {
+    is_hot = false;
+    return sparse_select(sp_area, sp_tw, i);
+  }
   if (is_tiered(KIND) && i >= e.ncold) {
     is_hot = true;
     const int hi_ = i - e.ncold;
@@ -515,7 +543,8 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
                                               const int* pre, uint8_t* stages, uint8_t* hdrs,
                                               uint8_t* qslot, const SmemLayout& L,
                                               const BoxGeo& bg, uint64_t* full, uint64_t* empty,
-                                              uint64_t* qfull, uint64_t* qempty, Misc* misc) {
+                                              uint64_t* qfull, uint64_t* qempty, Misc* misc,
+                                              const uint32_t* sp_base) {
   using Gm = Geo<KIND, D, KVB>;
   constexpr int OPS = cold_int8(KIND) ? 4 : 2;  // copies per page: K, V (+ 2 scale slabs)
   const int lane = threadIdx.x & 31;
@@ -589,7 +618,7 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
         note_abort(misc);
       uint8_t* st = stages + (size_t)stage * L.stage_bytes;
       bool is_hot;
-      const int at = tile_of<KIND>(e, i, is_hot);
+      const int at = tile_of<KIND>(e, i, is_hot, sparse_area(sp_base, p, s.pidx), p.sp_tw);
       if (__any_sync(0xffffffffu, *abort_flag(misc) != 0) ||
           (p.test_skip_arm && blockIdx.x == 0 && iss_mask == 0)) {
         // abort mode (or the test knob): no copy, the stage stays unarmed
@@ -1349,7 +1378,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
                                               uint8_t* qslot, const SmemLayout& L,
                                               const BoxGeo& bg, uint64_t* full, uint64_t* empty,
                                               uint64_t* qfull, uint64_t* qempty, float* red,
-                                              Misc* misc) {
+                                              Misc* misc, const uint32_t* sp_base) {
   using Gm = Geo<KIND, D, KVB>;
   constexpr int TG = Gm::TG;
   constexpr int NCW = Gm::W;
@@ -1419,11 +1448,27 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
     // several query tokens: the causal / window bounds of this lane's two
     // score columns (padding columns take the last token's)
     ColMask cm;
-    cm.on = KIND == KIND_PAGED_MULTI;  // the other kinds take one query token
+    // several query tokens, or per-head key blocks: per-column bounds (the
+    // other kinds take one query token and one key set per kv head)
+    cm.on = KIND == KIND_PAGED_MULTI || KIND == KIND_PAGED_SPARSE;
     cm.kbase = 0;
     cm.lo[0] = cm.lo[1] = 0;
     cm.hi[0] = cm.hi[1] = 0x7fffffff;
-    if (cm.on) {
+    // block-sparse: shared-memory address of the block bitmask of the layout
+    // each of this lane's two columns reads (0: a padding column)
+    uint32_t sp_lay[2] = {0u, 0u};
+    if constexpr (KIND == KIND_PAGED_SPARSE) {
+      const uint32_t* area = sparse_area(sp_base, p, s.pidx);
+#pragma unroll
+      for (int col = 0; col < 2; ++col) {
+        const int head = (PK ? 2 * (c & 1) : 2 * c) + col;
+        if (head < unit_nh(p, hg)) {
+          const int h = kv * p.G + hg * kHeadTile + head;  // query head of the column
+          sp_lay[col] = smem_u32(area + 2 * p.sp_tw + (h % p.sp_nl) * p.sp_bw);
+        }
+      }
+    }
+    if (KIND == KIND_PAGED_MULTI) {
 #pragma unroll
       for (int col = 0; col < 2; ++col) {
         const int head = (PK ? 2 * (c & 1) : 2 * c) + col;
@@ -1455,7 +1500,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
       uint8_t* st = stages + (size_t)stage * L.stage_bytes;
       const uint32_t bad_mask = lds32(smem_u32(hdrs + stage * 16));
       bool is_hot;
-      const int at = tile_of<KIND>(e, i, is_hot);
+      const int at = tile_of<KIND>(e, i, is_hot, sparse_area(sp_base, p, s.pidx), p.sp_tw);
       if (!is_hot) {
         RowMap km, vm;
         km.log2R = bg.log2R;
@@ -1474,7 +1519,22 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         if constexpr (is_paged(KIND)) {
           static_assert(Gm::GPW == 1, "one key group per warp in an f16 tile");
           const int k0 = 16 * tg;
-          const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
+          bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
+          if constexpr (KIND == KIND_PAGED_SPARSE) {
+            // the group's 16 keys lie in one sparse block (its size is a
+            // multiple of 16); a column whose layout does not select it sees
+            // none of them, and a group no column selects is skipped
+            const int blk = (tok0 + k0) >> p.sp_log2_block;
+            bool a0 = false, a1 = false;
+            if (blk < 32 * p.sp_bw) {
+              const uint32_t wo = (uint32_t)(blk >> 5) * 4u;
+              if (sp_lay[0]) a0 = (lds32(sp_lay[0] + wo) >> (blk & 31)) & 1u;
+              if (sp_lay[1]) a1 = (lds32(sp_lay[1] + wo) >> (blk & 31)) & 1u;
+            }
+            cm.lo[0] = a0 ? 0 : 0x7fffffff;
+            cm.lo[1] = a1 ? 0 : 0x7fffffff;
+            if (!__any_sync(0xffffffffu, a0 || a1)) vA = vB = false;
+          }
           if (__any_sync(0xffffffffu, vA || vB)) {
             if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
             cm.kbase = tok0;
@@ -1538,6 +1598,130 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   }
 }
 
+// Block-sparse selection of the launch's sequences, by every thread of the
+// CTA (com.microsoft.SparseAttention sparse-attention.wgsl.jinja, the
+// attention pass: head h reads layout h % NUM_LAYOUT, the query at qp reads
+// CSR row qp / SPARSE_BLOCK, each listed column names a block of keys, and a
+// repeated column adds nothing).  Per sequence and layout some head reads:
+// the bitmask of the blocks its row lists.  Per sequence: the bitmask of
+// the tiles of the visible range [lo, hi) that hold a key of a block some
+// layout selects, its prefix counts, and the tile count, which replaces the
+// plan's.  A row outside the layout, a malformed row and a column outside
+// [0, rows) select nothing and raise DEV_BAD_BLOCK.  Returns the device
+// flags of the sequences this CTA reports.
+template <int KIND, int TOK, int THREADS>
+__device__ int sparse_plan(const KParams& p, const PlanStore<KIND>& plan, uint32_t* sp, int tid) {
+  const int B = p.B, nlu = p.sp_nlu, tw = p.sp_tw, bw = p.sp_bw, W = p.sp_words;
+  const int lg = p.sp_log2_block;
+  const int warp = tid >> 5, lane = tid & 31;
+  constexpr int NW = THREADS / 32;
+  const int rows_off = 2 * tw + nlu * bw;  // CSR row starts, then lengths
+  int flags = 0;
+  for (int i = tid; i < B * W; i += THREADS) sp[i] = 0u;
+  __syncthreads();
+  // the CSR row of every (sequence, layout): its start and length
+  for (int q = tid; q < B * nlu; q += THREADS) {
+    const int b = q / nlu, l = q - b * nlu;
+    const SeqPlan e = plan.get(b);
+    int start = 0, len = 0, f = 0;
+    if (e.cold_len > 0 && e.qp0 >= 0) {
+      const int row = e.qp0 >> lg;
+      if (row >= p.sp_rows) {
+        f |= DEV_BAD_BLOCK;
+      } else {
+        const int* rp = p.sp_row_ptr + (long long)l * (p.sp_rows + 1);
+        const int s0 = __ldg(rp + row), s1 = __ldg(rp + row + 1);
+        if (s0 < 0 || s1 < s0 || s1 > p.sp_nnz) {
+          f |= DEV_BAD_BLOCK;
+        } else {
+          start = s0;
+          len = s1 - s0;
+        }
+      }
+    }
+    sp[(size_t)b * W + rows_off + l] = (uint32_t)start;
+    sp[(size_t)b * W + rows_off + nlu + l] = (uint32_t)len;
+    if (b % p.grid == (int)blockIdx.x) flags |= f;
+  }
+  __syncthreads();
+  // the listed columns into the layouts' block bitmasks: a warp per row,
+  // four rows at a time so that their loads are in flight together
+  for (int q0 = warp; q0 < B * nlu; q0 += 4 * NW) {
+    int start[4], len[4], b4[4], l4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = q0 + j * NW;
+      b4[j] = q / nlu;
+      l4[j] = q - b4[j] * nlu;
+      start[j] = len[j] = 0;
+      if (q < B * nlu) {
+        start[j] = (int)sp[(size_t)b4[j] * W + rows_off + l4[j]];
+        len[j] = (int)sp[(size_t)b4[j] * W + rows_off + nlu + l4[j]];
+      }
+    }
+    for (int e0 = 0;; e0 += 32) {
+      int col[4];
+      bool more = false;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        col[j] = -1;
+        if (e0 + lane < len[j])
+          col[j] = __ldg(p.sp_col_idx + (long long)l4[j] * p.sp_nnz + start[j] + e0 + lane);
+        more = more || e0 + 32 < len[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (e0 + lane >= len[j]) continue;
+        const int c = col[j];
+        if (c < 0 || c >= p.sp_rows) {
+          if (b4[j] % p.grid == (int)blockIdx.x) flags |= DEV_BAD_BLOCK;
+        } else if (c < 32 * bw) {  // blocks past the length bound hold no key
+          atomicOr(&sp[(size_t)b4[j] * W + 2 * tw + l4[j] * bw + (c >> 5)], 1u << (c & 31));
+        }
+      }
+      if (!__any_sync(0xffffffffu, more)) break;
+    }
+  }
+  __syncthreads();
+  // tiles of [lo, hi) holding a key of a block that some layout selects
+  for (int q = tid; q < B * tw; q += THREADS) {
+    const int b = q / tw, w = q - b * tw;
+    const SeqPlan e = plan.get(b);
+    const uint32_t* a = sp + (size_t)b * W;
+    uint32_t word = 0u;
+    for (int j = 0; j < 32; ++j) {
+      const int t = 32 * w + j;
+      if (t < e.t0 || t >= e.t0 + e.ntiles) continue;
+      const int ka = max(t * TOK, e.lo), kb = min(t * TOK + TOK, e.hi);
+      if (ka >= kb) continue;
+      for (int blk = ka >> lg; blk <= ((kb - 1) >> lg) && blk < 32 * bw; ++blk) {
+        uint32_t u = 0u;
+        for (int l = 0; l < nlu; ++l) u |= a[2 * tw + l * bw + (blk >> 5)];
+        if ((u >> (blk & 31)) & 1u) {
+          word |= 1u << j;
+          break;
+        }
+      }
+    }
+    sp[(size_t)b * W + w] = word;
+  }
+  __syncthreads();
+  // prefix counts and the tile count of every sequence
+  for (int b = tid; b < B; b += THREADS) {
+    uint32_t* a = sp + (size_t)b * W;
+    int run = 0;
+    for (int w = 0; w < tw; ++w) {
+      a[tw + w] = (uint32_t)run;
+      run += __popc(a[w]);
+    }
+    SeqPlan e = plan.get(b);
+    e.ntiles = run;
+    plan.put(b, e);
+  }
+  __syncthreads();
+  return flags;
+}
+
 // ================================================================ kernel
 // PK: Q/P f16 and remainder parts packed into one MMA operand (requires at
 // most four query heads per kv head).
@@ -1552,7 +1736,8 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int nplan = (p.sched == SCHED_SPLIT) ? 1 : p.B;
   const SmemLayout L = make_layout(KIND, D, KVB, NCW, Gm::REGION >> hgu_shift<KVB>(p), Gm::TOK,
-                                   p.NH, p.Hkv, p.stages, nplan);
+                                   p.NH, p.Hkv, p.stages, nplan,
+                                   KIND == KIND_PAGED_SPARSE ? p.sp_words : 0);
   uint8_t* stages = base + L.off_stages;
   uint8_t* hdrs = base + L.off_hdr;
   uint8_t* qslot = base + L.off_q;
@@ -1615,6 +1800,11 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
   }
   if (fl) atomicOr(&misc->flags, fl);
   __syncthreads();
+  uint32_t* sp_base = reinterpret_cast<uint32_t*>(base + L.off_sparse);
+  if constexpr (KIND == KIND_PAGED_SPARSE) {
+    const int sf = sparse_plan<KIND, Gm::TOK, Gm::THREADS>(p, plan, sp_base, tid);
+    if (sf) atomicOr(&misc->flags, sf);
+  }
   if (p.sched != SCHED_SPLIT && warp == 0) plan_prefix<KIND>(plan, pre, p.B, units_per_seq(p), tid & 31);
   __syncthreads();
 
@@ -1622,11 +1812,11 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
     if constexpr (Gm::REG_SPLIT) setmaxnreg_dec<Gm::REG_PROD>();
     if (warp == NCW)
       producer_loop<KIND, D, KVB>(p, plan, pre, stages, hdrs, qslot, L, bg, full, empty, qfull,
-                                  qempty, misc);
+                                  qempty, misc, sp_base);
   } else {
     if constexpr (Gm::REG_SPLIT) setmaxnreg_inc<Gm::REG_CONS>();
     consumer_loop<KIND, D, KVB, PK>(p, plan, pre, stages, hdrs, qslot, L, bg, full, empty, qfull,
-                                qempty, red, misc);
+                                qempty, red, misc, sp_base);
   }
   __syncthreads();
   if (tid == 0 && misc->flags && p.dev_status) atomicOr(p.dev_status, misc->flags);

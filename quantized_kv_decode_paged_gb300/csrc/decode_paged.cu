@@ -22,6 +22,16 @@ GeoInfo decode_geo(int kind, int D, int KVB) {
     if (D == 256 && KVB == 1) return geo_info<KIND_PAGED_MULTI, 256, 1>();
     return g;
   }
+  if (kind == KIND_PAGED_SPARSE) {
+    if (D == 64 && KVB == 1) return geo_info<KIND_PAGED_SPARSE, 64, 1>();
+    if (D == 64 && KVB == 2) return geo_info<KIND_PAGED_SPARSE, 64, 2>();
+    if (D == 64 && KVB == 4) return geo_info<KIND_PAGED_SPARSE, 64, 4>();
+    if (D == 128 && KVB == 1) return geo_info<KIND_PAGED_SPARSE, 128, 1>();
+    if (D == 128 && KVB == 2) return geo_info<KIND_PAGED_SPARSE, 128, 2>();
+    if (D == 128 && KVB == 4) return geo_info<KIND_PAGED_SPARSE, 128, 4>();
+    if (D == 256 && KVB == 1) return geo_info<KIND_PAGED_SPARSE, 256, 1>();
+    return g;
+  }
   if (kind == KIND_TIERED_F16) {
     if (D == 64 && KVB == 1) return geo_info<KIND_TIERED_F16, 64, 1>();
     if (D == 64 && KVB == 2) return geo_info<KIND_TIERED_F16, 64, 2>();
@@ -58,6 +68,9 @@ cudaError_t launch_decode(int kind, int D, int KVB, bool packed, const KParams& 
   if (kind == KIND_TIERED_F16)
     return packed ? launch_tiered_f16_packed(D, KVB, p, grid, smem, stream)
                   : launch_tiered_f16_unpacked(D, KVB, p, grid, smem, stream);
+  if (kind == KIND_PAGED_SPARSE)
+    return packed ? launch_paged_sparse_packed(D, KVB, p, grid, smem, stream)
+                  : launch_paged_sparse_unpacked(D, KVB, p, grid, smem, stream);
   if (kind == KIND_PAGED_MULTI)
     return packed ? launch_paged_multi_packed(D, KVB, p, grid, smem, stream)
                   : launch_paged_multi_unpacked(D, KVB, p, grid, smem, stream);

@@ -17,9 +17,17 @@ constexpr uint32_t kRedBarrier = 1;      // named barrier id for the consumer wa
 // PAGED: f16 pages, one query token per sequence.  PAGED_MULTI: f16 pages,
 // several query tokens per sequence.  TIERED: int8 cold pages (+ f16
 // scales) and an f16 hot ring.  TIERED_F16: f16 cold pages and an f16 hot ring.
-enum Kind : int { KIND_PAGED = 0, KIND_TIERED = 1, KIND_TIERED_F16 = 2, KIND_PAGED_MULTI = 3 };
+// PAGED_SPARSE: f16 pages, one query token, keys selected per query head by
+// a block-sparse CSR layout.
+enum Kind : int {
+  KIND_PAGED = 0,
+  KIND_TIERED = 1,
+  KIND_TIERED_F16 = 2,
+  KIND_PAGED_MULTI = 3,
+  KIND_PAGED_SPARSE = 4
+};
 __host__ __device__ constexpr bool is_paged(int kind) {
-  return kind == KIND_PAGED || kind == KIND_PAGED_MULTI;
+  return kind == KIND_PAGED || kind == KIND_PAGED_MULTI || kind == KIND_PAGED_SPARSE;
 }
 __host__ __device__ constexpr bool is_tiered(int kind) { return !is_paged(kind); }
 __host__ __device__ constexpr bool cold_int8(int kind) { return kind == KIND_TIERED; }
@@ -132,7 +140,29 @@ struct alignas(128) KParams {
   const int* cold_lens;
   const int* hot_lens;
   const int* hot_starts;
+
+  // block-sparse layouts (PAGED_SPARSE): head h reads layout h % sp_nl; the
+  // query at position qp reads CSR row qp >> sp_log2_block of it
+  const int* sp_row_ptr;  // [sp_nl][sp_rows + 1]
+  const int* sp_col_idx;  // [sp_nl][sp_nnz]
+  int sp_nl;              // layouts
+  int sp_nlu;             // layouts some head reads: min(sp_nl, Hq)
+  int sp_rows, sp_nnz;
+  int sp_log2_block;      // log2 of the keys per sparse block
+  int sp_tw;              // words of a sequence's tile bitmask
+  int sp_bw;              // words of a (sequence, layout) block bitmask
+  int sp_words;           // words of a sequence's sparse area (sparse_words)
+  int sp_max_len;         // host bound on the lengths; the bitmasks cover it
 };
+
+// Per-sequence shared-memory area of the block-sparse kind, in 32-bit words:
+//   [0, tw)                 bitmask of the tiles that hold a selected key
+//   [tw, 2 tw)              set bits of the tile bitmask before each word
+//   [2 tw, 2 tw + nlu*bw)   per layout: bitmask of its selected key blocks
+//   then nlu CSR row starts and nlu row lengths (scratch of the plan)
+__host__ __device__ constexpr int sparse_words(int tw, int bw, int nlu) {
+  return 2 * tw + nlu * bw + 2 * nlu;
+}
 
 // Per-sequence plan entries kept in shared memory (paged kernels use the
 // first four fields only).
@@ -158,7 +188,7 @@ struct SmemLayout {
   int off_hdr;               // per-stage 16-byte headers
   int off_q;                 // one Q slot: [KVB][NH][D] f32
   int off_red;               // tree-merge buffer: [W/2][red_floats(D, RED_PARTS)] f32
-  int off_plan, off_pre;
+  int off_plan, off_pre, off_sparse;
   int off_bar, off_misc;
   int total;  // bytes to request (includes 1 KB of alignment slack)
 };
@@ -174,7 +204,8 @@ __host__ __device__ constexpr int red_floats(int D, int parts) { return (D / 4 /
 __host__ __device__ constexpr int red_parts(int kind) { return cold_int8(kind) ? 2 : 1; }
 
 __host__ __device__ inline SmemLayout make_layout(int kind, int D, int KVB, int W, int region,
-                                                  int tok, int NH, int Hkv, int stages, int B) {
+                                                  int tok, int NH, int Hkv, int stages, int B,
+                                                  int sp_words = 0) {
   SmemLayout L;
   L.off_k = 0;
   L.off_v = region;
@@ -194,6 +225,8 @@ __host__ __device__ inline SmemLayout make_layout(int kind, int D, int KVB, int 
   off += B * (kind == KIND_PAGED ? (int)sizeof(SeqPlanPaged) : (int)sizeof(SeqPlan));
   L.off_pre = off;
   off += (B + 1) * 4;
+  L.off_sparse = off;
+  off += B * sp_words * 4;
   off = align_up(off, 8);
   L.off_bar = off;
   off += (2 * stages + 2) * 8;  // full[stages], empty[stages], qfull, qempty

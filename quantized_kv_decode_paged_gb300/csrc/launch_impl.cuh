@@ -85,6 +85,19 @@ cudaError_t launch_paged_multi_pk(int D, int KVB, const KParams& p, dim3 grid, i
   return cudaErrorInvalidValue;
 }
 
+template <bool PK>
+cudaError_t launch_paged_sparse_pk(int D, int KVB, const KParams& p, dim3 grid, int smem,
+                                   cudaStream_t stream) {
+  if (D == 64 && KVB == 1) return launch_decode_impl<KIND_PAGED_SPARSE, 64, 1, PK>(p, grid, smem, stream);
+  if (D == 64 && KVB == 2) return launch_decode_impl<KIND_PAGED_SPARSE, 64, 2, PK>(p, grid, smem, stream);
+  if (D == 64 && KVB == 4) return launch_decode_impl<KIND_PAGED_SPARSE, 64, 4, PK>(p, grid, smem, stream);
+  if (D == 128 && KVB == 1) return launch_decode_impl<KIND_PAGED_SPARSE, 128, 1, PK>(p, grid, smem, stream);
+  if (D == 128 && KVB == 2) return launch_decode_impl<KIND_PAGED_SPARSE, 128, 2, PK>(p, grid, smem, stream);
+  if (D == 128 && KVB == 4) return launch_decode_impl<KIND_PAGED_SPARSE, 128, 4, PK>(p, grid, smem, stream);
+  if (D == 256 && KVB == 1) return launch_decode_impl<KIND_PAGED_SPARSE, 256, 1, PK>(p, grid, smem, stream);
+  return cudaErrorInvalidValue;
+}
+
 // Defined in the instantiating translation units.
 cudaError_t launch_paged_unpacked(int D, int KVB, const KParams& p, dim3 grid, int smem,
                                   cudaStream_t stream);
@@ -102,5 +115,9 @@ cudaError_t launch_tiered_f16_unpacked(int D, int KVB, const KParams& p, dim3 gr
                                        cudaStream_t stream);
 cudaError_t launch_tiered_f16_packed(int D, int KVB, const KParams& p, dim3 grid, int smem,
                                      cudaStream_t stream);
+cudaError_t launch_paged_sparse_unpacked(int D, int KVB, const KParams& p, dim3 grid, int smem,
+                                         cudaStream_t stream);
+cudaError_t launch_paged_sparse_packed(int D, int KVB, const KParams& p, dim3 grid, int smem,
+                                       cudaStream_t stream);
 
 }  // namespace da

@@ -22,6 +22,9 @@ Workloads (the shapes of the pages' serving cases):
 * ``tiered_f16`` the ``tiered`` shape with the 7168 cold keys kept as f16 rows
 * ``paged_spec2``, ``paged_spec4`` the ``paged`` shape with 2 or 4 query tokens per
                 sequence (speculative decode)
+* ``paged_sparse`` the ``paged`` shape with four block-sparse layouts (64-key blocks,
+                the last four blocks plus every eighth block, a different eighth per
+                layout), query head h reading layout h % 4
 """
 from __future__ import annotations
 
@@ -38,7 +41,7 @@ _S_K, _S_V, _S_OUTLIER, _S_Q, _S_META = 0, 1, 2, 3, 4
 _GLOBAL = 1 << 30  # "sequence" index used for batch-wide draws
 
 WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx", "tiered_f16", "paged_spec2",
-             "paged_spec4")
+             "paged_spec4", "paged_sparse")
 # Same keys and values as "paged", in a pool holding exactly the used pages
 # (about 310 MB instead of 4 GiB of device memory): for profiler captures.
 VARIANTS = ("paged_compact",)
@@ -84,6 +87,14 @@ class PagedCase:
     outlier_rate: float = 0.0   # fraction of (b, t) keys whose K is scaled by 8
     pages_per_seq: Optional[np.ndarray] = None  # pages holding data per sequence
     nonfinite_tail: bool = False  # fill rows past seq_len in the last page with NaN/Inf
+    # block-sparse layouts (CSR): keys per block, row_ptr [NL, rows + 1], col_idx [NL, nnz]
+    sparse_block: int = 0
+    row_ptr: Optional[np.ndarray] = None
+    col_idx: Optional[np.ndarray] = None
+
+    @property
+    def sparse(self) -> bool:
+        return self.sparse_block > 0
 
     @property
     def max_blocks(self) -> int:
@@ -157,6 +168,9 @@ class PagedCase:
             seq_lens=torch.from_numpy(self.seq_lens).to(device),
             q_pos=None if self.q_pos is None else torch.from_numpy(self.q_pos).to(device),
         )
+        if self.sparse:
+            t["row_ptr"] = torch.from_numpy(self.row_ptr).to(device)
+            t["col_idx"] = torch.from_numpy(self.col_idx).to(device)
         return t
 
 
@@ -201,6 +215,54 @@ def make_paged(name, seed, B, Hq, Hkv, D, block_size, seq_lens, num_blocks=None,
                      nonfinite_tail=nonfinite_tail)
 
 
+def csr_layouts(rows_of_layouts, num_rows, max_nnz=None):
+    """CSR arrays (row_ptr [NL, num_rows + 1], col_idx [NL, max_nnz]) from, per
+    layout, a list of column lists (one per row; missing rows are empty).
+    Unused column entries hold -1."""
+    NL = len(rows_of_layouts)
+    need = max([sum(len(r) for r in lay) for lay in rows_of_layouts] + [1])
+    nnz = need if max_nnz is None else max(int(max_nnz), need)
+    row_ptr = np.zeros((NL, num_rows + 1), np.int32)
+    col_idx = np.full((NL, nnz), -1, np.int32)
+    for l, lay in enumerate(rows_of_layouts):
+        pos = 0
+        for r in range(num_rows):
+            cols = list(lay[r]) if r < len(lay) else []
+            row_ptr[l, r] = pos
+            col_idx[l, pos:pos + len(cols)] = cols
+            pos += len(cols)
+        row_ptr[l, num_rows] = pos
+    return row_ptr, col_idx
+
+
+def local_stride_layouts(num_layouts, num_rows, local_blocks, vert_stride):
+    """Block-sparse layouts of the local + vertical-stride kind: row r of
+    layout l lists the last `local_blocks` blocks up to r and every block
+    c <= r with (c + l) % vert_stride == 0 (each layout a different stride
+    phase).  Returns the per-layout lists of sorted column lists."""
+    lays = []
+    for l in range(num_layouts):
+        rows = []
+        for r in range(num_rows):
+            cols = set(range(max(0, r - local_blocks + 1), r + 1))
+            cols.update(c for c in range(r + 1) if (c + l) % vert_stride == 0)
+            rows.append(sorted(cols))
+        lays.append(rows)
+    return lays
+
+
+def make_sparse(name, seed, B, Hq, Hkv, D, block_size, seq_lens, sparse_block, layouts,
+                num_rows=None, max_nnz=None, **kw) -> PagedCase:
+    """make_paged plus block-sparse CSR layouts (lists of column lists per
+    row, one list per layout)."""
+    case = make_paged(name, seed, B, Hq, Hkv, D, block_size, seq_lens, **kw)
+    if num_rows is None:
+        num_rows = max(1, -(-max(int(np.max(case.seq_lens)), 1) // sparse_block))
+    case.sparse_block = int(sparse_block)
+    case.row_ptr, case.col_idx = csr_layouts(layouts, num_rows, max_nnz)
+    return case
+
+
 def workload(name: str):
     """The named serving workload (see the module docstring)."""
     if name == "tiny":
@@ -233,6 +295,14 @@ def workload(name: str):
         return make_paged("window", 3, B=64, Hq=16, Hkv=8, D=256, block_size=32,
                           seq_lens=[8192] * 64, num_blocks=64 * 256, max_blocks=256,
                           sliding_window=4096, softcap=50.0, outlier_rate=0.01)
+    if name == "paged_sparse":
+        meta = _rng(1, _GLOBAL, _S_META + 1)
+        lens = meta.integers(512, 4096, size=32, endpoint=True)
+        rows = 4096 // 64
+        return make_sparse("paged_sparse", 1, B=32, Hq=32, Hkv=8, D=128, block_size=16,
+                           seq_lens=lens, sparse_block=64,
+                           layouts=local_stride_layouts(4, rows, 4, 8), num_rows=rows,
+                           num_blocks=65536, max_blocks=256)
     if name == "longctx":
         meta = _rng(4, _GLOBAL, _S_META + 1)
         z = meta.standard_normal(128)

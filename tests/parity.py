@@ -107,3 +107,23 @@ def run_tiered(case, t, mode, per_seq=None, dev_status=None):
             dev_status=dev_status, **kw)
     torch.cuda.synchronize()
     return out.cpu().numpy(), lse.cpu().numpy()
+
+
+def oracle_sparse(case):
+    kp, vp = case.host_pools()
+    return oracle.decode_paged_sparse(case.q, kp, vp, case.block_table, case.seq_lens,
+                                      case.row_ptr, case.col_idx, case.sparse_block, case.q_pos,
+                                      scale=case.scale, softcap=case.softcap,
+                                      sliding_window=case.sliding_window, causal=case.causal)
+
+
+def run_sparse(case, t, mode, dev_status=None):
+    """CUDA block-sparse path: 'stream' (auto workspace) or 'units'."""
+    import torch
+    out, lse = qk.decode_attn_paged_sparse(
+        t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], t["row_ptr"],
+        t["col_idx"], case.sparse_block, t["q_pos"], max_seq_len=case.max_seq_len,
+        scale=case.scale, softcap=case.softcap, sliding_window=case.sliding_window,
+        causal=case.causal, workspace="auto" if mode == "stream" else None, dev_status=dev_status)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), lse.cpu().numpy()

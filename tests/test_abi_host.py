@@ -269,3 +269,23 @@ def test_tuning_from_many_threads(lib):
         th.join()
     qk.set_tuning()
     assert not errors, errors
+
+
+def test_sparse_rejects_bad_layouts(lib):
+    p = _params()
+    good = dict(sparse_block=64, num_layouts=2, num_rows=4, max_nnz=8, row_ptr=FAKE.value,
+                col_idx=FAKE.value)
+
+    def call(pp=p, **kw):
+        sl = qk.DaSparseLayout(**{**good, **kw})
+        return lib.decode_attn_paged_sparse(ctypes.byref(pp), ctypes.byref(sl), FAKE, FAKE, FAKE,
+                                            FAKE, FAKE, None, FAKE, None, None, 0, None, None)
+
+    for bad in (dict(sparse_block=48), dict(sparse_block=8), dict(num_layouts=0),
+                dict(num_rows=0), dict(max_nnz=-1), dict(row_ptr=None)):
+        assert call(**bad) == qk.DA_ERR_INVALID, bad
+    assert call(pp=_params(max_seq_len=0)) == qk.DA_ERR_INVALID
+    assert call(pp=_params(head_dim=96)) == qk.DA_ERR_UNSUPPORTED
+    assert lib.decode_attn_paged_sparse(ctypes.byref(p), None, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                        FAKE, None, None, 0, None, None) == qk.DA_ERR_INVALID
+    assert call(pp=_params(batch=0)) == qk.DA_OK

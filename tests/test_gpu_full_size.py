@@ -8,6 +8,8 @@ Each is run through every schedule the library has for it:
   benchmark times;
 - units: whole units per CTA, no workspace;
 - split: the explicit split-partial / merge pair, one-token paged only.
+The block-sparse workload (the paged shape with four layouts) runs stream
+and units.
 
 Every row is compared with the oracle at the parity tolerance.  The oracle
 runs once per workload.  With PARITY_REPORT set to a path, the largest
@@ -20,7 +22,8 @@ import os
 import numpy as np
 import pytest
 
-from parity import assert_parity, oracle_paged, oracle_tiered, run_paged, run_tiered
+from parity import (assert_parity, oracle_paged, oracle_sparse, oracle_tiered, run_paged,
+                    run_sparse, run_tiered)
 from quantized_kv_decode_paged_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -29,6 +32,7 @@ PAGED = {"tiny": ("stream", "units", "split"), "paged": ("stream", "units", "spl
          "window": ("stream", "units", "split"), "longctx": ("stream", "units", "split"),
          "paged_spec2": ("stream", "units"), "paged_spec4": ("stream", "units")}
 TIERED = {"tiered": ("stream", "units"), "tiered_f16": ("stream", "units")}
+SPARSE = {"paged_sparse": ("stream", "units")}
 REPORT = {}
 
 
@@ -96,5 +100,21 @@ def test_tiered_workload_every_row_every_schedule(name, per_seq):
         _record(name, tag, _errors(out, lse, ref_out, ref_lse))
         assert_parity(out.reshape(-1, case.D), lse.reshape(-1), ref_out, ref_lse,
                       f"{name}/{tag}")
+    del t
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", list(SPARSE))
+def test_sparse_workload_every_row_every_schedule(name):
+    import torch
+    case = wl.workload(name)
+    ref_out, ref_lse, flags = oracle_sparse(case)
+    assert flags == 0
+    t = case.device_tensors("cuda")
+    for mode in SPARSE[name]:
+        out, lse = run_sparse(case, t, mode)
+        _record(name, mode, _errors(out, lse, ref_out, ref_lse))
+        assert_parity(out.reshape(-1, case.D), lse.reshape(-1), ref_out, ref_lse,
+                      f"{name}/{mode}")
     del t
     torch.cuda.empty_cache()
