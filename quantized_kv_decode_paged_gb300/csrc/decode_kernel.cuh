@@ -1644,66 +1644,48 @@ __device__ int sparse_plan(const KParams& p, const PlanStore<KIND>& plan, uint32
     if (b % p.grid == (int)blockIdx.x) flags |= f;
   }
   __syncthreads();
-  // the listed columns into the layouts' block bitmasks: a warp per row,
-  // four rows at a time so that their loads are in flight together
-  for (int q0 = warp; q0 < B * nlu; q0 += 4 * NW) {
-    int start[4], len[4], b4[4], l4[4];
+  // the listed columns into the layouts' block bitmasks: a thread per row,
+  // its columns loaded eight at a time (all rows' loads in flight together)
+  for (int q = tid; q < B * nlu; q += THREADS) {
+    const int b = q / nlu, l = q - b * nlu;
+    const int start = (int)sp[(size_t)b * W + rows_off + l];
+    const int len = (int)sp[(size_t)b * W + rows_off + nlu + l];
+    const int* cols = p.sp_col_idx + (long long)l * p.sp_nnz + start;
+    uint32_t* bits = sp + (size_t)b * W + 2 * tw + l * bw;
+    int f = 0;
+    for (int e0 = 0; e0 < len; e0 += 8) {
+      int c8[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int q = q0 + j * NW;
-      b4[j] = q / nlu;
-      l4[j] = q - b4[j] * nlu;
-      start[j] = len[j] = 0;
-      if (q < B * nlu) {
-        start[j] = (int)sp[(size_t)b4[j] * W + rows_off + l4[j]];
-        len[j] = (int)sp[(size_t)b4[j] * W + rows_off + nlu + l4[j]];
+      for (int j = 0; j < 8; ++j) c8[j] = e0 + j < len ? __ldg(cols + e0 + j) : -2;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = c8[j];
+        if (e0 + j >= len) continue;
+        if (c < 0 || c >= p.sp_rows) f |= DEV_BAD_BLOCK;
+        else if (c < 32 * bw) atomicOr(&bits[c >> 5], 1u << (c & 31));  // past the bound: no key
       }
     }
-    for (int e0 = 0;; e0 += 32) {
-      int col[4];
-      bool more = false;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        col[j] = -1;
-        if (e0 + lane < len[j])
-          col[j] = __ldg(p.sp_col_idx + (long long)l4[j] * p.sp_nnz + start[j] + e0 + lane);
-        more = more || e0 + 32 < len[j];
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (e0 + lane >= len[j]) continue;
-        const int c = col[j];
-        if (c < 0 || c >= p.sp_rows) {
-          if (b4[j] % p.grid == (int)blockIdx.x) flags |= DEV_BAD_BLOCK;
-        } else if (c < 32 * bw) {  // blocks past the length bound hold no key
-          atomicOr(&sp[(size_t)b4[j] * W + 2 * tw + l4[j] * bw + (c >> 5)], 1u << (c & 31));
-        }
-      }
-      if (!__any_sync(0xffffffffu, more)) break;
-    }
+    if (b % p.grid == (int)blockIdx.x) flags |= f;
   }
   __syncthreads();
-  // tiles of [lo, hi) holding a key of a block that some layout selects
-  for (int q = tid; q < B * tw; q += THREADS) {
+  // tiles of [lo, hi) holding a key of a block that some layout selects: a
+  // warp per 32-tile word, lane j deciding tile 32w + j
+  for (int q = warp; q < B * tw; q += NW) {
     const int b = q / tw, w = q - b * tw;
     const SeqPlan e = plan.get(b);
     const uint32_t* a = sp + (size_t)b * W;
-    uint32_t word = 0u;
-    for (int j = 0; j < 32; ++j) {
-      const int t = 32 * w + j;
-      if (t < e.t0 || t >= e.t0 + e.ntiles) continue;
+    const int t = 32 * w + lane;
+    bool on = false;
+    if (t >= e.t0 && t < e.t0 + e.ntiles) {
       const int ka = max(t * TOK, e.lo), kb = min(t * TOK + TOK, e.hi);
-      if (ka >= kb) continue;
-      for (int blk = ka >> lg; blk <= ((kb - 1) >> lg) && blk < 32 * bw; ++blk) {
+      for (int blk = ka >> lg; !on && ka < kb && blk <= ((kb - 1) >> lg) && blk < 32 * bw; ++blk) {
         uint32_t u = 0u;
         for (int l = 0; l < nlu; ++l) u |= a[2 * tw + l * bw + (blk >> 5)];
-        if ((u >> (blk & 31)) & 1u) {
-          word |= 1u << j;
-          break;
-        }
+        on = (u >> (blk & 31)) & 1u;
       }
     }
-    sp[(size_t)b * W + w] = word;
+    const uint32_t word = __ballot_sync(0xffffffffu, on);
+    if (lane == 0) sp[(size_t)b * W + w] = word;
   }
   __syncthreads();
   // prefix counts and the tile count of every sequence

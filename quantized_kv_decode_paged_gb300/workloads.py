@@ -44,7 +44,7 @@ WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx", "tiered_f16", "page
              "paged_spec4", "paged_sparse")
 # Same keys and values as "paged", in a pool holding exactly the used pages
 # (about 310 MB instead of 4 GiB of device memory): for profiler captures.
-VARIANTS = ("paged_compact",)
+VARIANTS = ("paged_compact", "paged_sparse_compact")
 
 
 def _rng(seed: int, seq: int, stream: int) -> np.random.Generator:
@@ -295,14 +295,15 @@ def workload(name: str):
         return make_paged("window", 3, B=64, Hq=16, Hkv=8, D=256, block_size=32,
                           seq_lens=[8192] * 64, num_blocks=64 * 256, max_blocks=256,
                           sliding_window=4096, softcap=50.0, outlier_rate=0.01)
-    if name == "paged_sparse":
+    if name in ("paged_sparse", "paged_sparse_compact"):
+        # the compact variant keeps only the used pages (for profiler captures)
         meta = _rng(1, _GLOBAL, _S_META + 1)
         lens = meta.integers(512, 4096, size=32, endpoint=True)
         rows = 4096 // 64
-        return make_sparse("paged_sparse", 1, B=32, Hq=32, Hkv=8, D=128, block_size=16,
+        return make_sparse(name, 1, B=32, Hq=32, Hkv=8, D=128, block_size=16,
                            seq_lens=lens, sparse_block=64,
                            layouts=local_stride_layouts(4, rows, 4, 8), num_rows=rows,
-                           num_blocks=65536, max_blocks=256)
+                           num_blocks=65536 if name == "paged_sparse" else None, max_blocks=256)
     if name == "longctx":
         meta = _rng(4, _GLOBAL, _S_META + 1)
         z = meta.standard_normal(128)
