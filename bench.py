@@ -665,7 +665,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["tiny", "paged", "tiered", "window", "longctx", "paged_compact",
                              "tiered_f16", "paged_spec2", "paged_spec4", "paged_sparse",
-                             "paged_sparse_compact"])
+                             "paged_sparse_compact", "longctx_compact"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0,

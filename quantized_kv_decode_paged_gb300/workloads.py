@@ -44,7 +44,7 @@ WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx", "tiered_f16", "page
              "paged_spec4", "paged_sparse")
 # Same keys and values as "paged", in a pool holding exactly the used pages
 # (about 310 MB instead of 4 GiB of device memory): for profiler captures.
-VARIANTS = ("paged_compact", "paged_sparse_compact")
+VARIANTS = ("paged_compact", "paged_sparse_compact", "longctx_compact")
 
 
 def _rng(seed: int, seq: int, stream: int) -> np.random.Generator:
@@ -304,10 +304,15 @@ def workload(name: str):
                            seq_lens=lens, sparse_block=64,
                            layouts=local_stride_layouts(4, rows, 4, 8), num_rows=rows,
                            num_blocks=65536 if name == "paged_sparse" else None, max_blocks=256)
-    if name == "longctx":
+    if name in ("longctx", "longctx_compact"):
         meta = _rng(4, _GLOBAL, _S_META + 1)
         z = meta.standard_normal(128)
         lens = np.clip(np.rint(np.exp(math.log(8192.0) + 0.8 * z)), 128, 32768).astype(np.int32)
+        if name == "longctx_compact":
+            # the first 32 sequences (about 1.3 GB of pages): the same kernel
+            # instantiation for profiler captures that replay the launch
+            return make_paged(name, 4, B=32, Hq=64, Hkv=8, D=128, block_size=16,
+                              seq_lens=lens[:32], max_blocks=2048)
         return make_paged("longctx", 4, B=128, Hq=64, Hkv=8, D=128, block_size=16,
                           seq_lens=lens, max_blocks=2048)
     raise KeyError(name)
