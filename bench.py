@@ -483,18 +483,38 @@ def time_device_steps(step, flush, steps, warmup, stream, barrier, clk=None):
     return [a.elapsed_time(b) for a, b in zip(starts, ends)], wall
 
 
-def config_entry(case, times_ms, peak):
-    """One workload's line in "configs": time per step and bandwidth."""
+def copy_reference_us(nbytes, flush, stream, barrier, steps=50):
+    """Time of one device-to-device copy that moves nbytes of DRAM traffic
+    (nbytes/2 read, nbytes/2 written), timed like a decode step (L2 flushed
+    before each copy, CUDA events): the rate this GPU reaches on a transfer
+    of the same size, launch included."""
+    import torch
+    n = max(16, nbytes // 2 // 16 * 16)
+    src = torch.ones(n, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    tms, _ = time_device_steps(lambda: dst.copy_(src), flush, steps, 3, stream, barrier)
+    del src, dst
+    torch.cuda.empty_cache()
+    return sum(tms) / len(tms) * 1e3
+
+
+def config_entry(case, times_ms, peak, copy_us=None):
+    """One workload's line in "configs": time per step and bandwidth, and
+    the time of a plain copy of the same byte count."""
     from quantized_kv_decode_paged_gb300.accounting import algorithmic_bytes
     nbytes = algorithmic_bytes(case)["total"]
     mean_ms = sum(times_ms) / len(times_ms)
     gbs = nbytes / (mean_ms * 1e-3) / 1e9
-    return {"us_per_step": round(mean_ms * 1e3, 2),
-            "us_median": round(sorted(times_ms)[len(times_ms) // 2] * 1e3, 2),
-            "gb_per_s": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
-            "frac_of_spec_8000": round(gbs / SPEC_HBM_GBS, 4),
-            "bytes_per_step": int(nbytes), "steps": len(times_ms),
-            "shape": describe(case)}
+    e = {"us_per_step": round(mean_ms * 1e3, 2),
+         "us_median": round(sorted(times_ms)[len(times_ms) // 2] * 1e3, 2),
+         "gb_per_s": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+         "frac_of_spec_8000": round(gbs / SPEC_HBM_GBS, 4),
+         "bytes_per_step": int(nbytes), "steps": len(times_ms),
+         "shape": describe(case)}
+    if copy_us is not None:
+        e["copy_same_bytes_us"] = round(copy_us, 2)
+        e["frac_of_copy_same_bytes"] = round(copy_us / (mean_ms * 1e3), 4)
+    return e
 
 
 def gpu_arm(args, rank, world):
@@ -594,15 +614,17 @@ def gpu_arm(args, rank, world):
         n_cfg = max(10, min(args.steps, args.config_steps))
         for name in CONFIG_WORKLOADS:
             if name == case.name:
-                configs[name] = config_entry(case, times_ms, peak)
+                cp = copy_reference_us(bytes_per_step, flush, stream, barrier)
+                configs[name] = config_entry(case, times_ms, peak, cp)
                 continue
             c = load_case(name)
             tt = c.device_tensors("cuda")
             st, _, _ = make_step(c, tt)
             tms, _ = time_device_steps(st, flush, n_cfg, 3, stream, barrier)
-            configs[name] = config_entry(c, tms, peak)
             del tt, st
             torch.cuda.empty_cache()
+            cp = copy_reference_us(algorithmic_bytes(c)["total"], flush, stream, barrier)
+            configs[name] = config_entry(c, tms, peak, cp)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
