@@ -510,15 +510,32 @@ __device__ __forceinline__ int sparse_select(const uint32_t* area, int tw, int i
   return 32 * lo + bit;
 }
 
-// Absolute tile of unit-local tile i (tiered: hot tiles follow cold ones;
-// block-sparse: the i-th tile that holds a selected key).
-template <int KIND>
-__device__ __forceinline__ int tile_of(const SeqPlan& e, int i, bool& is_hot,
-                                       const uint32_t* sp_area = nullptr, int sp_tw = 0) {
-  if constexpr (KIND == KIND_PAGED_SPARSE) {
-    is_hot = false;
-    return sparse_select(sp_area, sp_tw, i);
+// The tiles of a segment of the block-sparse kind in order: the i0-th set
+// bit of the sequence's tile bitmask (a select), then each following set bit
+// (the lowest remaining bit of the current word, or of the next non-zero
+// word).  A segment asks for no more tiles than the bitmask has bits.
+struct SparseTiles {
+  const uint32_t* words;
+  int w;
+  uint32_t rest;  // bits of word w after the last tile returned
+  int first;
+  __device__ __forceinline__ void init(const uint32_t* area, int tw, int i0) {
+    first = sparse_select(area, tw, i0);
+    words = area;
+    w = first >> 5;
+    rest = area[w] & ~((2u << (first & 31)) - 1u);
   }
+  __device__ __forceinline__ int next() {
+    while (rest == 0u) rest = words[++w];
+    const int t = 32 * w + __ffs(rest) - 1;
+    rest &= rest - 1u;
+    return t;
+  }
+};
+
+// Absolute tile of unit-local tile i (tiered: hot tiles follow cold ones).
+template <int KIND>
+__device__ __forceinline__ int tile_of(const SeqPlan& e, int i, bool& is_hot) {
   if (is_tiered(KIND) && i >= e.ncold) {
     is_hot = true;
     const int hi_ = i - e.ncold;
@@ -613,12 +630,16 @@ __device__ __forceinline__ void producer_loop(const KParams& p, const PlanStore<
       }
       ++qn;
     }
+    SparseTiles spt;
+    if constexpr (KIND == KIND_PAGED_SPARSE) spt.init(sparse_area(sp_base, p, s.pidx), p.sp_tw, s.i0);
     for (int i = s.i0; i < s.i1; ++i) {
       if (!mbar_wait(&empty[stage], (round & 1) ^ 1, abort_flag(misc), p.wait_ns) && lane == 0)
         note_abort(misc);
       uint8_t* st = stages + (size_t)stage * L.stage_bytes;
-      bool is_hot;
-      const int at = tile_of<KIND>(e, i, is_hot, sparse_area(sp_base, p, s.pidx), p.sp_tw);
+      bool is_hot = false;
+      int at;
+      if constexpr (KIND == KIND_PAGED_SPARSE) at = i == s.i0 ? spt.first : spt.next();
+      else at = tile_of<KIND>(e, i, is_hot);
       if (__any_sync(0xffffffffu, *abort_flag(misc) != 0) ||
           (p.test_skip_arm && blockIdx.x == 0 && iss_mask == 0)) {
         // abort mode (or the test knob): no copy, the stage stays unarmed
@@ -1495,12 +1516,16 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
       hot_all = hv.j0 <= 0 && hv.j1 >= (hv.W > 0 ? (long long)hv.W : (long long)hv.cap_eff);
     const int vhc = is_tiered(KIND) ? min(s.vhi, e.cold_len) : s.vhi;
 
+    SparseTiles spt;
+    if constexpr (KIND == KIND_PAGED_SPARSE) spt.init(sparse_area(sp_base, p, s.pidx), p.sp_tw, s.i0);
     for (int i = s.i0; i < s.i1; ++i) {
       if (!mbar_wait(&full[stage], round & 1, abort_flag(misc), p.wait_ns) && lane == 0) note_abort(misc);
       uint8_t* st = stages + (size_t)stage * L.stage_bytes;
       const uint32_t bad_mask = lds32(smem_u32(hdrs + stage * 16));
-      bool is_hot;
-      const int at = tile_of<KIND>(e, i, is_hot, sparse_area(sp_base, p, s.pidx), p.sp_tw);
+      bool is_hot = false;
+      int at;
+      if constexpr (KIND == KIND_PAGED_SPARSE) at = i == s.i0 ? spt.first : spt.next();
+      else at = tile_of<KIND>(e, i, is_hot);
       if (!is_hot) {
         RowMap km, vm;
         km.log2R = bg.log2R;
@@ -1615,13 +1640,14 @@ __device__ int sparse_plan(const KParams& p, const PlanStore<KIND>& plan, uint32
   const int lg = p.sp_log2_block;
   const int warp = tid >> 5, lane = tid & 31;
   constexpr int NW = THREADS / 32;
-  const int rows_off = 2 * tw + nlu * bw;  // CSR row starts, then lengths
   int flags = 0;
-  for (int i = tid; i < B * W; i += THREADS) sp[i] = 0u;
-  __syncthreads();
-  // the CSR row of every (sequence, layout): its start and length
+  // every (sequence, layout) by one thread: its CSR row's bounds, then its
+  // columns, eight loads at a time, into the layout's block bitmask (which
+  // only this thread writes)
   for (int q = tid; q < B * nlu; q += THREADS) {
     const int b = q / nlu, l = q - b * nlu;
+    uint32_t* bits = sp + (size_t)b * W + 2 * tw + l * bw;
+    for (int w = 0; w < bw; ++w) bits[w] = 0u;
     const SeqPlan e = plan.get(b);
     int start = 0, len = 0, f = 0;
     if (e.cold_len > 0 && e.qp0 >= 0) {
@@ -1639,20 +1665,7 @@ __device__ int sparse_plan(const KParams& p, const PlanStore<KIND>& plan, uint32
         }
       }
     }
-    sp[(size_t)b * W + rows_off + l] = (uint32_t)start;
-    sp[(size_t)b * W + rows_off + nlu + l] = (uint32_t)len;
-    if (b % p.grid == (int)blockIdx.x) flags |= f;
-  }
-  __syncthreads();
-  // the listed columns into the layouts' block bitmasks: a thread per row,
-  // its columns loaded eight at a time (all rows' loads in flight together)
-  for (int q = tid; q < B * nlu; q += THREADS) {
-    const int b = q / nlu, l = q - b * nlu;
-    const int start = (int)sp[(size_t)b * W + rows_off + l];
-    const int len = (int)sp[(size_t)b * W + rows_off + nlu + l];
     const int* cols = p.sp_col_idx + (long long)l * p.sp_nnz + start;
-    uint32_t* bits = sp + (size_t)b * W + 2 * tw + l * bw;
-    int f = 0;
     for (int e0 = 0; e0 < len; e0 += 8) {
       int c8[8];
 #pragma unroll
@@ -1662,7 +1675,7 @@ __device__ int sparse_plan(const KParams& p, const PlanStore<KIND>& plan, uint32
         const int c = c8[j];
         if (e0 + j >= len) continue;
         if (c < 0 || c >= p.sp_rows) f |= DEV_BAD_BLOCK;
-        else if (c < 32 * bw) atomicOr(&bits[c >> 5], 1u << (c & 31));  // past the bound: no key
+        else if (c < 32 * bw) bits[c >> 5] |= 1u << (c & 31);  // past the bound: no key
       }
     }
     if (b % p.grid == (int)blockIdx.x) flags |= f;
@@ -1759,6 +1772,20 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
       prefetch_tensormap(&p.tm_kh);
       prefetch_tensormap(&p.tm_vh);
     }
+  }
+  // A block-sparse layout's CSR arrays are read by the plan, behind the
+  // lengths.  Each of their 128-byte lines (up to 16 MB of each) is
+  // prefetched into L2 by one CTA here, so those dependent reads find them
+  // in L2.
+  if constexpr (KIND == KIND_PAGED_SPARSE) {
+    const long long G = gridDim.x * gridDim.y, c = blockIdx.x + blockIdx.y * gridDim.x;
+    auto pf = [&](const void* base, long long bytes) {
+      const long long lines = min((bytes + 127) / 128, 1ll << 17);
+      for (long long l = c + (long long)tid * G; l < lines; l += G * Gm::THREADS)
+        prefetch_l2(reinterpret_cast<const char*>(base) + l * 128);
+    };
+    pf(p.sp_row_ptr, (long long)p.sp_nl * (p.sp_rows + 1) * 4);
+    pf(p.sp_col_idx, (long long)p.sp_nl * p.sp_nnz * 4);
   }
   // ---- per-sequence plan
   int fl = 0;

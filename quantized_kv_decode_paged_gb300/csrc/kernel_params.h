@@ -159,9 +159,8 @@ struct alignas(128) KParams {
 //   [0, tw)                 bitmask of the tiles that hold a selected key
 //   [tw, 2 tw)              set bits of the tile bitmask before each word
 //   [2 tw, 2 tw + nlu*bw)   per layout: bitmask of its selected key blocks
-//   then nlu CSR row starts and nlu row lengths (scratch of the plan)
 __host__ __device__ constexpr int sparse_words(int tw, int bw, int nlu) {
-  return 2 * tw + nlu * bw + 2 * nlu;
+  return 2 * tw + nlu * bw;
 }
 
 // Per-sequence plan entries kept in shared memory (paged kernels use the
