@@ -346,16 +346,16 @@ int decode_attn_split_merge(int32_t batch, int32_t num_q_heads, int32_t head_dim
 
 /*
  * decode_attn_paged_static_ws — decode_attn_paged (split path) for callers
- * that cannot allocate device memory: graph-captured regions, plugins whose
- * host framework owns every allocation, loops that cannot take
- * cudaMalloc's implicit synchronisation.  The pages have no counterpart for
- * this entry point; it only changes where the scratch lives.
+ * that cannot allocate device memory: plugins whose host framework owns
+ * every allocation, processes held to a fixed device-memory budget, loops
+ * that cannot take cudaMalloc's implicit synchronisation.  The pages have no
+ * counterpart for this entry point; it only changes where the scratch lives.
  *
  * The scratch is a buffer of DECODE_ATTN_STATIC_WS_BYTES bytes compiled into
  * the library (held by every GPU that loads it, until exit).  The call
  * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  * The first call on a device looks up the buffer's device address
- * (cudaGetSymbolAddress) and should come before any stream capture.  Each
+ * (cudaGetSymbolAddress) once per device and context.  Each
  * call clears the buffer's ticket counters on `stream` (cudaMemsetAsync)
  * and launches on `stream`; calls that overlap on the GPU share the buffer
  * and race.  Arguments, layouts, outputs and device flags are those of

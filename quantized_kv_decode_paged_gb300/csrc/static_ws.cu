@@ -2,18 +2,17 @@
 // its scratch taken from a buffer compiled into the library, for callers
 // that must not allocate device memory themselves.
 //
-// Who needs it: code that runs where cudaMalloc is not an option — inside a
-// region being captured into a CUDA graph, in an inference-server plugin
-// whose host framework owns all device memory, or in a latency-critical
-// loop that cannot afford cudaMalloc's implicit device synchronisation.
+// Who needs it: code that runs where cudaMalloc is not an option — an
+// inference-server plugin whose host framework owns all device memory, a
+// process held to a fixed device-memory budget, or a latency-critical loop
+// that cannot afford cudaMalloc's implicit device synchronisation.
 //
 // The buffer is a file-scope __device__ array of DECODE_ATTN_STATIC_WS_BYTES
 // bytes; every GPU that loads this library holds it until the process exits.
 // Host code cannot pass the array's name to a kernel (on the host it is only
 // a stand-in symbol), so the first call on each device looks up its device
 // address with cudaGetSymbolAddress, with that device current, and keeps it.
-// Because of that lookup, the first call on a device should come before any
-// stream capture.  The address is kept together with the unique id of the
+// The address is kept together with the unique id of the
 // context it was looked up in: after cudaDeviceReset the device gets a new
 // context, and the next call looks the address up again (that call is then
 // a first call).

@@ -164,3 +164,82 @@ def test_large_batch_is_split_over_launches():
     lens = rng.integers(1, 3000, size=260).tolist()
     case = _case(1100, 64, 8, 2, 16, lens, SB=32, NL=3)
     _check(case)
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_sparse_random_shapes(i):
+    """Every knob drawn from a fixed seed: head dim, kv heads, group size,
+    page size, sparse block size, layout count and density, lengths (0 and
+    1 included), window, softcap, causal, explicit query positions."""
+    rng = np.random.default_rng(9000 + i)
+    D = int(rng.choice([64, 128, 256]))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 4, 8, 16]))
+    bs = int(rng.choice([8, 16, 32, 64]))
+    SB = int(rng.choice([16, 32, 64, 128]))
+    NL = int(rng.integers(1, 9))
+    B = int(rng.integers(1, 6))
+    lens = [int(x) for x in rng.choice([0, 1, 2, SB - 1, SB, SB + 1, 97, 300, 1200], size=B)]
+    lens[0] = max(lens[0], 1)
+    L = max(lens)
+    rows = -(-L // SB)
+    lays = random_layouts(rng, NL, rows, density=float(rng.choice([0.1, 0.4, 0.9])))
+    q_pos = None
+    if rng.integers(0, 3) == 0:
+        q_pos = [int(rng.integers(0, max(x, 1))) for x in lens]
+    pages = sum((x + bs - 1) // bs for x in lens)
+    case = wl.make_sparse(f"sfz{i}", 9100 + i, B=B, Hq=G * Hkv, Hkv=Hkv, D=D, block_size=bs,
+                          seq_lens=lens, sparse_block=SB, layouts=lays, num_rows=rows,
+                          num_blocks=pages + 2, sliding_window=int(rng.choice([0, 0, 5, 100])),
+                          softcap=float(rng.choice([0.0, 0.0, 20.0])),
+                          causal=bool(rng.integers(0, 2)), q_pos=q_pos)
+    _check(case)
+
+
+def test_sparse_decode_step_in_a_cuda_graph():
+    """One block-sparse step captured into a CUDA graph (the call allocates
+    nothing and never synchronises) and replayed over new queries and a new
+    layout written into the same buffers."""
+    import torch
+    rng = np.random.default_rng(9500)
+    rows = -(-2200 // 64)
+    # room for any layout of these rows: every causal block, one block past
+    # the row and one repeat per row
+    nnz = rows * (rows + 1) // 2 + 2 * rows
+    case = _case(9500, 128, 16, 4, 16, [1000, 17, 640, 2200, 1], SB=64, NL=3, max_nnz=nnz)
+    t = case.device_tensors("cuda")
+    out = torch.empty((case.B, case.Hq, case.D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
+    params = qk.make_params(t["q"], case.block_size, case.Hkv, case.max_blocks, case.num_blocks,
+                            max_seq_len=case.max_seq_len)
+    ws = torch.zeros(qk.decode_attn_workspace_size(params), dtype=torch.uint8, device="cuda")
+
+    def step():
+        qk.decode_attn_paged_sparse(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                    t["seq_lens"], t["row_ptr"], t["col_idx"], case.sparse_block,
+                                    max_seq_len=case.max_seq_len, out=out, lse=lse, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for rep in range(3):
+        q_new = rng.standard_normal(case.q.shape).astype(np.float32)
+        t["q"].copy_(torch.from_numpy(q_new))
+        case.q = q_new
+        # a new layout with arrays of the captured shapes
+        rp, ci_full = wl.csr_layouts(random_layouts(rng, 3, rows, density=0.3), rows, nnz)
+        case.row_ptr, case.col_idx = rp, ci_full
+        t["row_ptr"].copy_(torch.from_numpy(rp))
+        t["col_idx"].copy_(torch.from_numpy(ci_full))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_lse, _ = oracle_sparse(case)
+        assert_parity(out.cpu().numpy().reshape(-1, case.D), lse.cpu().numpy().reshape(-1),
+                      ref_out, ref_lse, f"sparse graph replay {rep}")

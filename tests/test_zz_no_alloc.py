@@ -1,9 +1,10 @@
 """The entry point for callers that cannot allocate device memory.
 
 decode_attn_paged_static_ws runs the split-KV paged decode with its scratch
-in a buffer compiled into the library.  Callers that need it: code inside a
-graph-captured region, a plugin whose host framework owns every allocation,
-or a loop that cannot afford cudaMalloc's implicit synchronisation.
+in a buffer compiled into the library.  Callers that need it: a plugin whose
+host framework owns every allocation, a process held to a fixed
+device-memory budget, or a loop that cannot afford cudaMalloc's implicit
+synchronisation.
 
 This test calls it through the C ABI twice in a row.  Both calls are checked
 against decode_attn_paged with a caller-provided workspace, and against the
