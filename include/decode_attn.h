@@ -115,7 +115,11 @@ typedef struct {
  * or cudaMemsetAsync).  Its leading ticket counters are left at zero by
  * every call, so one buffer serves later calls of any shape that fit in it.
  * With it the keys of long sequences are split across CTAs (flash-decoding)
- * and the partial results are merged inside the same launch.
+ * and the partial results are merged inside the same launch.  Short
+ * sequences are not split: when 0 < p->max_seq_len <= the tuning's
+ * unsplit_max_len (512 keys by default) and the launch has at most two
+ * units per SM, whole units run per CTA and the workspace is not touched
+ * (da_tuning gives the bounds of the other paged entry points).
  * workspace = NULL and workspace_bytes = 0 selects the unsplit path (whole
  * (b, kv head) units per CTA).  Two calls that share a workspace must be
  * ordered (same stream or synchronised); calls that overlap on the GPU race
@@ -385,7 +389,8 @@ const char* decode_attn_status_string(int status);
  * The pages have no counterpart; they have one kernel per variant.
  *
  * When the library is loaded, the fields are set from the environment
- * variables DA_KVB, DA_FUSE_HG, DA_PACK, DA_MAX_STAGES and DA_WAIT_LIMIT_MS.
+ * variables DA_KVB, DA_FUSE_HG, DA_PACK, DA_MAX_STAGES, DA_WAIT_LIMIT_MS and
+ * DA_UNSPLIT_MAX_LEN.
  * The environment is read once, at load; unset or out-of-range values keep
  * the defaults below.  decode_attn_set_tuning replaces every field;
  * decode_attn_set_tuning(NULL) restores the load-time values.  A call that
@@ -407,6 +412,15 @@ typedef struct {
   int32_t wait_limit_ms;     /* time limit of every wait inside the kernels,
                                 [1, 10000], default 2000; a wait that runs
                                 out sets DA_DEV_TIMEOUT (see the device flags) */
+  int32_t unsplit_max_len;   /* keys below which a call with a workspace runs
+                                whole units per CTA (no split, no merge) when
+                                0 < max_seq_len <= the bound and the units fill
+                                at most two waves of one CTA per SM:
+                                decode_attn_paged this value,
+                                decode_attn_paged_multi twice it,
+                                decode_attn_paged_sparse four times it (one
+                                wave); tiered calls always split.  0 = always
+                                split; [0, 65536], default 512 */
 } da_tuning;
 
 /* Copies the current tuning into *t.  DA_ERR_INVALID when t is NULL. */

@@ -92,7 +92,7 @@ class DaTuning(ctypes.Structure):
     _fields_ = [
         ("kv_heads_per_unit", ctypes.c_int32), ("fuse_head_groups", ctypes.c_int32),
         ("packed_operands", ctypes.c_int32), ("max_stages", ctypes.c_int32),
-        ("wait_limit_ms", ctypes.c_int32),
+        ("wait_limit_ms", ctypes.c_int32), ("unsplit_max_len", ctypes.c_int32),
     ]
 
 

@@ -60,7 +60,7 @@ int device_sms(int* sms_out) {
 
 // Process-wide tuning state.  Its initial values are read from the
 // environment once, when the library is loaded (DA_KVB, DA_FUSE_HG, DA_PACK,
-// DA_MAX_STAGES, DA_WAIT_LIMIT_MS; unset or invalid values keep the
+// DA_MAX_STAGES, DA_WAIT_LIMIT_MS, DA_UNSPLIT_MAX_LEN; unset or invalid values keep the
 // defaults); decode_attn_set_tuning replaces them.  Every launch reads a
 // snapshot of the fields.  The test hook that leaves a stage unarmed is set
 // only through decode_attn_testing_skip_first_arm, never from the
@@ -71,15 +71,17 @@ struct Tuning {
   std::atomic<int> pack{1};        // 0 = two-operand kernels always
   std::atomic<int> max_stages{0};  // 0 = kMaxStages, else 2..kMaxStages
   std::atomic<int> wait_ms{2000};  // 1..10000
+  std::atomic<int> unsplit_len{512};  // 0..65536 keys
   std::atomic<int> skip_arm{0};    // test hook
 };
 
 bool valid_kvb(int v) { return v == 0 || v == 1 || v == 2 || v == 4; }
 bool valid_stages(int v) { return v == 0 || (v >= 2 && v <= da::kMaxStages); }
 bool valid_wait(int v) { return v >= 1 && v <= 10000; }
+bool valid_unsplit(int v) { return v >= 0 && v <= 65536; }
 
 da_tuning env_tuning() {
-  da_tuning t{0, 1, 1, 0, 2000};
+  da_tuning t{0, 1, 1, 0, 2000, 512};
   auto env_int = [](const char* name, int* out) {
     const char* e = getenv(name);
     if (!e || !*e) return false;
@@ -95,6 +97,7 @@ da_tuning env_tuning() {
   if (env_int("DA_PACK", &v) && (v == 0 || v == 1)) t.packed_operands = v;
   if (env_int("DA_MAX_STAGES", &v) && valid_stages(v)) t.max_stages = v;
   if (env_int("DA_WAIT_LIMIT_MS", &v) && valid_wait(v)) t.wait_limit_ms = v;
+  if (env_int("DA_UNSPLIT_MAX_LEN", &v) && valid_unsplit(v)) t.unsplit_max_len = v;
   return t;
 }
 
@@ -112,6 +115,7 @@ Tuning& tuning() {
     x->pack = e.packed_operands;
     x->max_stages = e.max_stages;
     x->wait_ms = e.wait_limit_ms;
+    x->unsplit_len = e.unsplit_max_len;
     return x;
   }();
   return *t;
@@ -361,6 +365,32 @@ int ws_kvb(const da_params* p) {
   return m;
 }
 
+// Whether a call with a workspace runs whole units instead of the split
+// (stream) schedule.  Splitting a short sequence costs the cross-CTA hand-off
+// and merge, more than the parallel keys save while the units fill at most
+// two waves of one CTA per SM.  Measured on GB300 (D = 128, 8 kv heads,
+// flushed L2), with lim the tuning's unsplit_max_len (512):
+// - one token: 256 keys x 64 units 24.1 -> 13.9 us, 512 keys x 16 units
+//   20.5 -> 18.5 us, 256 keys x 4 units 18.0 -> 13.9 us; at 1024 keys either
+//   schedule can win, at 2048 splitting wins (27.0 against 35.2 us for 16
+//   units), and with 1024 units splitting wins at any length: up to lim keys;
+// - two or four tokens (more work a tile and a larger merge): whole units
+//   win up to 1024 keys (four tokens, 16 units: 51.5 -> 39.2 us), tie at
+//   the least: up to 2 lim keys;
+// - block-sparse (four local + stride layouts of 64-key blocks): whole
+//   units win up to 2048 keys with 64 units (41.2 -> 37.1 us) and lose with
+//   256 units (53.5 against 55.6 us) or at 4096 keys: up to 4 lim keys and
+//   one unit per SM.
+bool run_unsplit(int kind, const da_params* p, int units, int sms) {
+  const long long lim = tuning().unsplit_len.load(std::memory_order_relaxed);
+  const long long L = p->max_seq_len;
+  if (L <= 0) return false;
+  if (kind == da::KIND_PAGED) return L <= lim && units <= 2 * sms;
+  if (kind == da::KIND_PAGED_MULTI) return L <= 2 * lim && units <= 2 * sms;
+  if (kind == da::KIND_PAGED_SPARSE) return L <= 4 * lim && units <= sms;
+  return false;
+}
+
 struct Launch {
   int kind;
   const da_params* p;
@@ -426,7 +456,7 @@ int run_batched(KParams& base, const Launch& lc, OffsetFn offset_chunk, cudaStre
     k.stages = pick_stages(lc.kind, k.D, k.KVB, g, k.hgu_shift, k.NH, k.Hkv, nb, &smem, k.sp_words);
     if (k.stages == 0) return DA_ERR_UNSUPPORTED;
     int grid;
-    if (use_ws) {
+    if (use_ws && !run_unsplit(lc.kind, p, units, sms)) {
       k.sched = da::SCHED_STREAM;
       grid = grid_max;
       if (p->max_seq_len > 0) {
@@ -671,6 +701,7 @@ int decode_attn_get_tuning(da_tuning* t) {
   t->packed_operands = s.pack.load();
   t->max_stages = s.max_stages.load();
   t->wait_limit_ms = s.wait_ms.load();
+  t->unsplit_max_len = s.unsplit_len.load();
   return DA_OK;
 }
 
@@ -678,7 +709,7 @@ int decode_attn_set_tuning(const da_tuning* t) {
   const da_tuning& v = t ? *t : load_time_tuning();
   if (!valid_kvb(v.kv_heads_per_unit) || (v.fuse_head_groups != 0 && v.fuse_head_groups != 1) ||
       (v.packed_operands != 0 && v.packed_operands != 1) || !valid_stages(v.max_stages) ||
-      !valid_wait(v.wait_limit_ms))
+      !valid_wait(v.wait_limit_ms) || !valid_unsplit(v.unsplit_max_len))
     return DA_ERR_INVALID;
   Tuning& s = tuning();
   s.kvb = v.kv_heads_per_unit;
@@ -686,6 +717,7 @@ int decode_attn_set_tuning(const da_tuning* t) {
   s.pack = v.packed_operands;
   s.max_stages = v.max_stages;
   s.wait_ms = v.wait_limit_ms;
+  s.unsplit_len = v.unsplit_max_len;
   return DA_OK;
 }
 

@@ -39,22 +39,27 @@ def oracle_paged(case, rows=None):
 
 def run_paged(case, t, mode, split_tokens=256, dev_status=None):
     """Runs the CUDA path on device tensors ``t`` in one of the schedules:
-    'stream' (auto workspace), 'units' (no workspace) or 'split'
-    (split_partial + split_merge).  Returns (out, lse) as numpy."""
+    'stream' (auto workspace, keys split across CTAs whatever the lengths),
+    'auto' (auto workspace, the library's default choice: short sequences
+    run whole units), 'units' (no workspace) or 'split' (split_partial +
+    split_merge).  Returns (out, lse) as numpy."""
     import torch
     kw = dict(scale=case.scale, softcap=case.softcap, sliding_window=case.sliding_window,
               causal=case.causal)
     if t["q"].dim() == 4:
-        assert mode in ("stream", "units")
-        out, lse = qk.decode_attn_paged_multi(
-            t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], t["q_pos"],
-            max_seq_len=case.max_seq_len, workspace="auto" if mode == "stream" else None,
-            dev_status=dev_status, **kw)
-    elif mode in ("stream", "units"):
-        out, lse = qk.decode_attn_paged(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
-                                        t["seq_lens"], t["q_pos"], max_seq_len=case.max_seq_len,
-                                        workspace="auto" if mode == "stream" else None,
-                                        dev_status=dev_status, **kw)
+        assert mode in ("stream", "auto", "units")
+        with qk.tuning(**({"unsplit_max_len": 0} if mode == "stream" else {})):
+            out, lse = qk.decode_attn_paged_multi(
+                t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], t["q_pos"],
+                max_seq_len=case.max_seq_len, workspace=None if mode == "units" else "auto",
+                dev_status=dev_status, **kw)
+    elif mode in ("stream", "auto", "units"):
+        with qk.tuning(**({"unsplit_max_len": 0} if mode == "stream" else {})):
+            out, lse = qk.decode_attn_paged(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                            t["seq_lens"], t["q_pos"],
+                                            max_seq_len=case.max_seq_len,
+                                            workspace=None if mode == "units" else "auto",
+                                            dev_status=dev_status, **kw)
     else:
         S = max(1, -(-max(case.max_seq_len, 1) // split_tokens))
         op, lp = qk.decode_attn_split_partial(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
@@ -118,12 +123,15 @@ def oracle_sparse(case):
 
 
 def run_sparse(case, t, mode, dev_status=None):
-    """CUDA block-sparse path: 'stream' (auto workspace) or 'units'."""
+    """CUDA block-sparse path: 'stream' (auto workspace, always split),
+    'auto' (auto workspace, the library's choice) or 'units'."""
     import torch
-    out, lse = qk.decode_attn_paged_sparse(
-        t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], t["row_ptr"],
-        t["col_idx"], case.sparse_block, t["q_pos"], max_seq_len=case.max_seq_len,
-        scale=case.scale, softcap=case.softcap, sliding_window=case.sliding_window,
-        causal=case.causal, workspace="auto" if mode == "stream" else None, dev_status=dev_status)
+    with qk.tuning(**({"unsplit_max_len": 0} if mode == "stream" else {})):
+        out, lse = qk.decode_attn_paged_sparse(
+            t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], t["row_ptr"],
+            t["col_idx"], case.sparse_block, t["q_pos"], max_seq_len=case.max_seq_len,
+            scale=case.scale, softcap=case.softcap, sliding_window=case.sliding_window,
+            causal=case.causal, workspace=None if mode == "units" else "auto",
+            dev_status=dev_status)
     torch.cuda.synchronize()
     return out.cpu().numpy(), lse.cpu().numpy()

@@ -173,7 +173,7 @@ def test_product_package_does_not_import_the_oracle():
 # ---------------------------------------------------------------------------
 
 DEFAULT_TUNING = dict(kv_heads_per_unit=0, fuse_head_groups=1, packed_operands=1, max_stages=0,
-                      wait_limit_ms=2000)
+                      wait_limit_ms=2000, unsplit_max_len=512)
 
 
 def test_tuning_defaults_set_validate_and_restore(lib):
@@ -186,7 +186,8 @@ def test_tuning_defaults_set_validate_and_restore(lib):
     assert qk.get_tuning()["packed_operands"] == 1
     for bad in (dict(kv_heads_per_unit=3), dict(fuse_head_groups=2), dict(packed_operands=-1),
                 dict(max_stages=1), dict(max_stages=9), dict(wait_limit_ms=0),
-                dict(wait_limit_ms=10001)):
+                dict(wait_limit_ms=10001), dict(unsplit_max_len=-1),
+                dict(unsplit_max_len=65537)):
         before = qk.get_tuning()
         with pytest.raises(qk.DecodeAttnError):
             qk.set_tuning(**bad)
@@ -214,16 +215,17 @@ def test_environment_is_read_once_at_load(lib):
     import subprocess
     import sys
     env = dict(os.environ, DA_PACK="0", DA_KVB="4", DA_FUSE_HG="0", DA_MAX_STAGES="5",
-               DA_WAIT_LIMIT_MS="750", DA_TEST_SKIP_ARM="1")
+               DA_WAIT_LIMIT_MS="750", DA_UNSPLIT_MAX_LEN="0", DA_TEST_SKIP_ARM="1")
     r = subprocess.run([sys.executable, "-c", _LOAD_TIME_SCRIPT, ROOT], env=env,
                        capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     first, restored = json.loads(r.stdout.strip().splitlines()[-1])
     want = dict(kv_heads_per_unit=4, fuse_head_groups=0, packed_operands=0, max_stages=5,
-                wait_limit_ms=750)
+                wait_limit_ms=750, unsplit_max_len=0)
     assert first == want and restored == want
     # out-of-range values keep the defaults
-    env = dict(os.environ, DA_PACK="7", DA_KVB="3", DA_MAX_STAGES="1", DA_WAIT_LIMIT_MS="x")
+    env = dict(os.environ, DA_PACK="7", DA_KVB="3", DA_MAX_STAGES="1", DA_WAIT_LIMIT_MS="x",
+               DA_UNSPLIT_MAX_LEN="70000")
     r = subprocess.run([sys.executable, "-c", _LOAD_TIME_SCRIPT, ROOT], env=env,
                        capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
@@ -253,12 +255,13 @@ def test_tuning_from_many_threads(lib):
             for j in range(300):
                 t = qk.DaTuning(kv_heads_per_unit=(0, 1, 2, 4)[(i + j) % 4],
                                 fuse_head_groups=j % 2, packed_operands=(j // 2) % 2,
-                                max_stages=(0, 2, 3, 8)[j % 4], wait_limit_ms=1 + j)
+                                max_stages=(0, 2, 3, 8)[j % 4], wait_limit_ms=1 + j,
+                                unsplit_max_len=(0, 512, 65536)[j % 3])
                 assert lib.decode_attn_set_tuning(ctypes.byref(t)) == qk.DA_OK
                 g = qk.DaTuning()
                 assert lib.decode_attn_get_tuning(ctypes.byref(g)) == qk.DA_OK
                 assert g.kv_heads_per_unit in (0, 1, 2, 4) and g.max_stages in (0, 2, 3, 8)
-                assert 1 <= g.wait_limit_ms <= 300
+                assert 1 <= g.wait_limit_ms <= 300 and g.unsplit_max_len in (0, 512, 65536)
         except Exception as e:  # pragma: no cover
             errors.append(e)
 

@@ -5,7 +5,9 @@ paged, int8 tiered, window with softcap and outliers, long-context mix,
 f16 tiered, and the paged shape with 2 or 4 query tokens per sequence.
 Each is run through every schedule the library has for it:
 - stream: stream-K with the in-kernel merge, the launch configuration the
-  benchmark times;
+  benchmark times for every workload but tiny;
+- auto: the library's default choice with a workspace; for tiny (256 keys)
+  that is whole units per CTA, the configuration the benchmark times there;
 - units: whole units per CTA, no workspace;
 - split: the explicit split-partial / merge pair, one-token paged only.
 The block-sparse workload (the paged shape with four layouts) runs stream
@@ -28,7 +30,7 @@ from quantized_kv_decode_paged_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-PAGED = {"tiny": ("stream", "units", "split"), "paged": ("stream", "units", "split"),
+PAGED = {"tiny": ("stream", "auto", "units", "split"), "paged": ("stream", "units", "split"),
          "window": ("stream", "units", "split"), "longctx": ("stream", "units", "split"),
          "paged_spec2": ("stream", "units"), "paged_spec4": ("stream", "units")}
 TIERED = {"tiered": ("stream", "units"), "tiered_f16": ("stream", "units")}

@@ -9,7 +9,7 @@ from parity import assert_parity, oracle_paged, run_paged
 
 pytestmark = pytest.mark.gpu
 
-MODES = ("stream", "units")
+MODES = ("stream", "auto", "units")
 
 
 @pytest.fixture(autouse=True)

@@ -10,7 +10,7 @@ from parity import assert_parity, oracle_paged, run_paged
 
 pytestmark = pytest.mark.gpu
 
-MODES = ("stream", "units", "split")
+MODES = ("stream", "auto", "units", "split")
 
 
 @pytest.fixture(autouse=True)

@@ -6,7 +6,7 @@ h % num_layouts, the query reads CSR row qpos / sparse_block, and each listed
 column selects one block of keys.  The cases cover head dimensions, group
 sizes, layout counts, block sizes, unsorted and repeated columns, columns
 past the query's row, windows, softcaps, explicit query positions, the
-non-causal case, invalid CSR entries, empty selections, both schedules, both
+non-causal case, invalid CSR entries, empty selections, every schedule, both
 operand packings, head groups sharing a unit, and batches split over
 several launches.
 """
@@ -20,7 +20,7 @@ from parity import assert_parity, oracle_sparse, run_paged, run_sparse
 
 pytestmark = pytest.mark.gpu
 
-MODES = ("stream", "units")
+MODES = ("stream", "auto", "units")
 
 
 @pytest.fixture(autouse=True)
