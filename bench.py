@@ -91,6 +91,9 @@ class ClockSampler:
     """SM clock, power and clock-event reasons of one GPU, read in-process
     through NVML (libnvidia-ml, read-only queries): one sample when the
     timed region starts, one every 2 ms during it and one when it ends.
+    prepare() opens NVML and takes a first sample of every query before the
+    warm-up, so that first-call costs of the driver's management interface
+    (seconds on a freshly booted machine) stay out of the timed region.
     Nothing is changed on the GPU."""
 
     # clock-event reason bits of NVML
@@ -148,13 +151,27 @@ class ClockSampler:
         while not self._stop.wait(0.002):
             self.sample()
 
-    def __enter__(self):
+    def prepare(self):
+        if self.nvml is not None or self.error is not None:
+            return self
         try:
             self._open()
             self.sample()
+            self.samples.clear()  # the first sample only warms the queries
+        except Exception as exc:  # clocks are reported as unavailable, never fatal
+            self.error = f"{type(exc).__name__}: {exc}"
+            self.nvml = None
+        return self
+
+    def __enter__(self):
+        self.prepare()
+        if self.nvml is None:
+            return self
+        try:
+            self.sample()
             self.t = threading.Thread(target=self._loop, daemon=True)
             self.t.start()
-        except Exception as exc:  # clocks are reported as unavailable, never fatal
+        except Exception as exc:
             self.error = f"{type(exc).__name__}: {exc}"
             self.nvml = None
         return self
@@ -555,7 +572,7 @@ def gpu_arm(args, rank, world):
             dist.barrier()
         torch.cuda.synchronize()
 
-    clk = ClockSampler(local)
+    clk = ClockSampler(local).prepare()
     times_ms, wall = time_device_steps(step, flush, args.steps, args.warmup, stream, barrier, clk)
     dev_ms = sum(times_ms)
     clocks = clk.summary()
@@ -687,7 +704,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["tiny", "paged", "tiered", "window", "longctx", "paged_compact",
                              "tiered_f16", "paged_spec2", "paged_spec4", "paged_sparse",
-                             "paged_sparse_compact", "longctx_compact"])
+                             "paged_sparse_compact", "longctx_compact", "window_compact"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0,

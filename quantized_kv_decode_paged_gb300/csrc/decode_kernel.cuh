@@ -974,6 +974,17 @@ struct ColMask {
   int lo[2], hi[2];
 };
 
+// Softcap in base-2 score units: cap2 * tanh(x / cap2), cap2 = cap * log2(e),
+// from the identity tanh(y) = 1 - 2 / (e^(2y) + 1) with e^(2y) = 2^(x k),
+// k = 2 log2(e) / cap2: one exp2 and one approximate division.  Near y = 0
+// the absolute error is about 3e-7 * cap2 (the rounding of 2^(x k) next to
+// 1), about 2e-5 for cap = 50; the form saturates to +-cap2 without
+// overflow (2^(x k) = inf gives cap2, 0 gives -cap2) and keeps a NaN score
+// NaN.
+__device__ __forceinline__ float softcap_b2(float x, float cap2, float k) {
+  return cap2 - __fdividef(2.f * cap2, exp2f(x * k) + 1.f);
+}
+
 // NG 16-key groups of this warp (keys k0[g] .. k0[g]+15) in one online-
 // softmax step: the QK products, one running-max update, then the PV
 // products.  v[2g], v[2g+1]: validity of keys k0[g]+r and k0[g]+r+8;
@@ -982,7 +993,7 @@ struct ColMask {
 // warp two independent QK chains to interleave.
 template <int TK, int D, bool PK, int NG>
 __device__ __forceinline__ void groups_compute(const RowMap& km, const RowMap& vm,
-                                               float softcap2, const int (&k0)[NG], int lane,
+                                               float2 cap, const int (&k0)[NG], int lane,
                                                const QFrag<D>& q, Acc<D>& a,
                                                const bool (&v)[2 * NG],
                                                const float (&ks)[2 * NG],
@@ -1007,7 +1018,7 @@ __device__ __forceinline__ void groups_compute(const RowMap& km, const RowMap& v
       // packed: column h + 4 (lane c ^ 2) holds the remainder part of head h
       if constexpr (PK) x += __shfl_xor_sync(0xffffffffu, x, 2);
       if constexpr (TK == TK_COLD) x *= ks[2 * g + (j >> 1)];
-      if (softcap2 > 0.f) x = softcap2 * tanhf(x / softcap2);
+      if (cap.x > 0.f) x = softcap_b2(x, cap.x, cap.y);
       sc[g][j] = x;
     }
     if (!v[2 * g]) sc[g][0] = sc[g][1] = kNegInf;
@@ -1096,13 +1107,13 @@ __device__ __forceinline__ void groups_compute(const RowMap& km, const RowMap& v
 
 // One 16-key group (keys k0 .. k0+15) of an f16 tile.
 template <int TK, int D, bool PK>
-__device__ __forceinline__ void group_compute(const RowMap& km, const RowMap& vm, float softcap2,
+__device__ __forceinline__ void group_compute(const RowMap& km, const RowMap& vm, float2 cap,
                                               int k0, int lane, const QFrag<D>& q, Acc<D>& a,
                                               bool vA, bool vB, const ColMask& cm) {
   const int k0s[1] = {k0};
   const bool v[2] = {vA, vB};
   const float one[2] = {1.f, 1.f};
-  groups_compute<TK, D, PK, 1>(km, vm, softcap2, k0s, lane, q, a, v, one, one, cm);
+  groups_compute<TK, D, PK, 1>(km, vm, cap, k0s, lane, q, a, v, one, one, cm);
 }
 
 // Zeroes the f16 V rows of masked keys among k0..k0+15 of this warp's head,
@@ -1409,7 +1420,8 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   const int kvs = warp / TG, tg = warp % TG;
   const int nstages = p.stages;
   const int bs = p.bs;
-  const float softcap2 = p.softcap2, qscale = p.qscale;
+  const float2 cap = make_float2(p.softcap2, p.softcap_k);
+  const float qscale = p.qscale;
   const int NH = p.NH;
   const int Hkv = p.Hkv;
 
@@ -1563,7 +1575,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
           if (__any_sync(0xffffffffu, vA || vB)) {
             if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
             cm.kbase = tok0;
-            group_compute<TK_PAGED, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB, cm);
+            group_compute<TK_PAGED, D, PK>(km, vm, cap, k0, lane, q, a, vA, vB, cm);
           }
         } else if constexpr (KIND == KIND_TIERED_F16) {
           // f16 cold rows, read like hot-ring rows (the tiered d order)
@@ -1572,7 +1584,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
           const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
           if (__any_sync(0xffffffffu, vA || vB)) {
             if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
-            group_compute<TK_HOT, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB, cm);
+            group_compute<TK_HOT, D, PK>(km, vm, cap, k0, lane, q, a, vA, vB, cm);
           }
         } else {
           // both key groups of the warp in one softmax step (int8 values are
@@ -1590,7 +1602,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
               ks[i] = __half2float(__ushort_as_half(lds16(sck + off)));
               vs[i] = __half2float(__ushort_as_half(lds16(scv + off)));
             }
-            groups_compute<TK_COLD, D, PK, 2>(km, vm, softcap2, k0, lane, q, a, v, ks, vs, cm);
+            groups_compute<TK_COLD, D, PK, 2>(km, vm, cap, k0, lane, q, a, v, ks, vs, cm);
           }
         }
       } else if constexpr (is_tiered(KIND)) {
@@ -1609,7 +1621,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
         if (__any_sync(0xffffffffu, vA || vB)) {
           if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
-          group_compute<TK_HOT, D, PK>(km, vm, softcap2, k0, lane, q, a, vA, vB, cm);
+          group_compute<TK_HOT, D, PK>(km, vm, cap, k0, lane, q, a, vA, vB, cm);
         }
       }
       __syncwarp();

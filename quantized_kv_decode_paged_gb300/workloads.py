@@ -42,9 +42,12 @@ _GLOBAL = 1 << 30  # "sequence" index used for batch-wide draws
 
 WORKLOADS = ("tiny", "paged", "tiered", "window", "longctx", "tiered_f16", "paged_spec2",
              "paged_spec4", "paged_sparse")
-# Same keys and values as "paged", in a pool holding exactly the used pages
-# (about 310 MB instead of 4 GiB of device memory): for profiler captures.
-VARIANTS = ("paged_compact", "paged_sparse_compact", "longctx_compact")
+# Smaller or tighter copies of serving workloads for profiler captures that
+# replay a launch: the same kernel instantiation on a few GB at most.
+# paged_compact: the keys and values of "paged" in a pool of exactly the used
+# pages (about 310 MB instead of 4 GiB); window_compact: 16 of the 64
+# sequences of "window".
+VARIANTS = ("paged_compact", "paged_sparse_compact", "longctx_compact", "window_compact")
 
 
 def _rng(seed: int, seq: int, stream: int) -> np.random.Generator:
@@ -291,9 +294,10 @@ def workload(name: str):
         return make_tiered("tiered_f16", 2, B=16, Hq=32, Hkv=8, D=128, block_size=16,
                            cold_len=7168, hot_len=1024, hot_window=1024, hot_start=7168,
                            cold_f16=True)
-    if name == "window":
-        return make_paged("window", 3, B=64, Hq=16, Hkv=8, D=256, block_size=32,
-                          seq_lens=[8192] * 64, num_blocks=64 * 256, max_blocks=256,
+    if name in ("window", "window_compact"):
+        B = 64 if name == "window" else 16
+        return make_paged(name, 3, B=B, Hq=16, Hkv=8, D=256, block_size=32,
+                          seq_lens=[8192] * B, num_blocks=B * 256, max_blocks=256,
                           sliding_window=4096, softcap=50.0, outlier_rate=0.01)
     if name in ("paged_sparse", "paged_sparse_compact"):
         # the compact variant keeps only the used pages (for profiler captures)
