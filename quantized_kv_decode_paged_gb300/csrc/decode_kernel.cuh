@@ -982,7 +982,7 @@ struct ColMask {
 // overflow (2^(x k) = inf gives cap2, 0 gives -cap2) and keeps a NaN score
 // NaN.
 __device__ __forceinline__ float softcap_b2(float x, float cap2, float k) {
-  return cap2 - __fdividef(2.f * cap2, exp2f(x * k) + 1.f);
+  return cap2 - __fdividef(2.f * cap2, ex2_ftz(x * k) + 1.f);
 }
 
 // NG 16-key groups of this warp (keys k0[g] .. k0[g]+15) in one online-
@@ -1044,18 +1044,18 @@ __device__ __forceinline__ void groups_compute(const RowMap& km, const RowMap& v
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
   }
   const float mn0 = fmaxf(a.m[0], mx0), mn1 = fmaxf(a.m[1], mx1);
-  const float al0 = (mn0 == kNegInf) ? 1.f : exp2f(a.m[0] - mn0);
-  const float al1 = (mn1 == kNegInf) ? 1.f : exp2f(a.m[1] - mn1);
+  const float al0 = (mn0 == kNegInf) ? 1.f : ex2_ftz(a.m[0] - mn0);
+  const float al1 = (mn1 == kNegInf) ? 1.f : ex2_ftz(a.m[1] - mn1);
   const float mu0 = (mn0 == kNegInf) ? 0.f : mn0;
   const float mu1 = (mn1 == kNegInf) ? 0.f : mn1;
   float pr[NG][4];
   float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
-    pr[g][0] = exp2f(sc[g][0] - mu0);
-    pr[g][1] = exp2f(sc[g][1] - mu1);
-    pr[g][2] = exp2f(sc[g][2] - mu0);
-    pr[g][3] = exp2f(sc[g][3] - mu1);
+    pr[g][0] = ex2_ftz(sc[g][0] - mu0);
+    pr[g][1] = ex2_ftz(sc[g][1] - mu1);
+    pr[g][2] = ex2_ftz(sc[g][2] - mu0);
+    pr[g][3] = ex2_ftz(sc[g][3] - mu1);
     ls0 += pr[g][0] + pr[g][2];
     ls1 += pr[g][1] + pr[g][3];
   }

@@ -229,6 +229,15 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32
 }
 
 // --------------------------------------------------------------- numerics
+// 2^x by the special-function unit's instruction (ex2.approx.ftz.f32, a
+// few units in the last place of relative error): subnormal results are
+// flushed to 0 and -inf gives 0.  Softmax weights below 2^-126 of the running maximum carry
+// nothing the f32 sums could hold anyway.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
