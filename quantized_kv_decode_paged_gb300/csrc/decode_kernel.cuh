@@ -769,7 +769,7 @@ __device__ __forceinline__ void load_q(uint32_t qs, int NH, float qscale, int r,
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     int d0, d2;
-    if constexpr (is_paged(KIND)) {
+    if constexpr (!cold_int8(KIND)) {
       d0 = 16 * ks + 2 * c;
       d2 = d0 + 8;
     } else {
@@ -1584,7 +1584,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
           const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
           if (__any_sync(0xffffffffu, vA || vB)) {
             if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
-            group_compute<TK_HOT, D, PK>(km, vm, cap, k0, lane, q, a, vA, vB, cm);
+            group_compute<TK_PAGED, D, PK>(km, vm, cap, k0, lane, q, a, vA, vB, cm);
           }
         } else {
           // both key groups of the warp in one softmax step (int8 values are
@@ -1621,7 +1621,8 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
         const bool vA = ok(k0 + r), vB = ok(k0 + r + 8);
         if (__any_sync(0xffffffffu, vA || vB)) {
           if (!__all_sync(0xffffffffu, vA && vB)) zero_masked_v_rows<D>(vm, k0, lane, ok);
-          group_compute<TK_HOT, D, PK>(km, vm, cap, k0, lane, q, a, vA, vB, cm);
+          group_compute<KIND == KIND_TIERED_F16 ? TK_PAGED : TK_HOT, D, PK>(km, vm, cap, k0, lane,
+                                                                            q, a, vA, vB, cm);
         }
       }
       __syncwarp();
