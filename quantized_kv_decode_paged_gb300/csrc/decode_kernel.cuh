@@ -1238,6 +1238,81 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     l += __shfl_xor_sync(0xffffffffu, l, 16);
     a.l[j] = l;
   }
+  constexpr int SROW = D + 4;  // floats a staged row: D values, the lse, padding
+  constexpr int D4 = D / 4;
+  auto row_dst = [&](int ks, int h, float*& dst, float*& ldst) {
+    const int hgs = slot_hg<KVB>(p, s.hg, ks);
+    if (s.dest == DEST_OUT) {
+      const long long orow = out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h);
+      dst = p.out + orow * D;
+      ldst = p.lse ? p.lse + orow : nullptr;
+    } else if (s.dest == DEST_SPLIT) {
+      const long long pr =
+          out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h) * p.max_splits + s.slot;
+      dst = p.o_part + pr * D;
+      ldst = p.lse_part + pr;
+    } else {
+      const long long sl =
+          ((long long)blockIdx.x * 2 + s.slot) * (KVB * kHeadTile) + ks * kHeadTile + h;
+      dst = p.ws_o + sl * D;
+      ldst = p.ws_lse + sl;
+    }
+  };
+  // Flat merge (packed kernels, at most four rows a slot, when every warp's
+  // rows fit in the merge buffer): every warp writes its unnormalised rows
+  // and its (m, l) to shared memory, then each consumer thread merges one
+  // float4 of one row over the TG warps of its slot and stores it.  Two
+  // barriers; the tree merge below takes 2 log2(TG) + 2.
+  constexpr int RPS = PK ? 4 : kHeadTile;  // staged rows a slot (tree path)
+  constexpr bool STAGED = KVB * RPS * SROW <= (NCW / 2) * red_floats(D, Gm::RED_PARTS);
+  constexpr int FR = 4;  // rows a slot in the flat buffer
+  constexpr bool FLAT =
+      PK && (TG * KVB * FR * SROW + 2 * TG * KVB * FR) <= (NCW / 2) * red_floats(D, Gm::RED_PARTS);
+  if constexpr (FLAT) {
+    float* ml = red + TG * KVB * FR * SROW;  // [kvs][tg][row][m, l]
+    if (c < 2) {
+      float* fb = red + ((kvs * TG + tg) * FR) * SROW;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int h = 2 * c + j;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          fb[h * SROW + o_row_d<KIND>(mt, r, 0)] = a.o[mt][j];
+          fb[h * SROW + o_row_d<KIND>(mt, r, 1)] = a.o[mt][2 + j];
+        }
+        if (r == 0) {
+          ml[((kvs * TG + tg) * FR + h) * 2 + 0] = a.m[j];
+          ml[((kvs * TG + tg) * FR + h) * 2 + 1] = a.l[j];
+        }
+      }
+    }
+    named_bar_sync(kRedBarrier, NCW * 32);
+    for (int idx = tid; idx < KVB * FR * D4; idx += NCW * 32) {
+      const int d4 = idx % D4, lrow = idx / D4;
+      const int ks = lrow / FR, h = lrow % FR;
+      if (h >= unit_nh(p, slot_hg<KVB>(p, s.hg, ks))) continue;
+      float M = kNegInf;
+#pragma unroll
+      for (int w = 0; w < TG; ++w) M = fmaxf(M, ml[((ks * TG + w) * FR + h) * 2]);
+      float L = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < TG; ++w) {
+        const float mw = ml[((ks * TG + w) * FR + h) * 2];
+        const float sc = (mw == kNegInf) ? 0.f : ex2_ftz(mw - M);
+        L += ml[((ks * TG + w) * FR + h) * 2 + 1] * sc;
+        const float4 v = *reinterpret_cast<const float4*>(red + ((ks * TG + w) * FR + h) * SROW + 4 * d4);
+        O.x += sc * v.x; O.y += sc * v.y; O.z += sc * v.z; O.w += sc * v.w;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      float* dst;
+      float* ldst;
+      row_dst(ks, h, dst, ldst);
+      reinterpret_cast<float4*>(dst)[d4] = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+      if (d4 == 0 && ldst) *ldst = (M == kNegInf) ? kNegInf : (M + log2f(L)) * kLn2;
+    }
+    named_bar_sync(kRedBarrier, NCW * 32);  // rows read before the buffer is written again
+  } else {
   // tree merge of the TG warps of each kv head; warp tg = 0 ends with the sum
   constexpr int RP = Gm::RED_PARTS;
 #pragma unroll
@@ -1259,28 +1334,6 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
   // A slot has at most four rows in the packed kernels, else kHeadTile.
   // Otherwise (the unpacked int8 tiered kernel with four slots, whose merge
   // buffer is halved) the tg = 0 warps store their fragments directly.
-  constexpr int SROW = D + 4;  // floats a staged row: D values, the lse, padding
-  constexpr int RPS = PK ? 4 : kHeadTile;  // staged rows a slot
-  constexpr bool STAGED = KVB * RPS * SROW <= (NCW / 2) * red_floats(D, Gm::RED_PARTS);
-  constexpr int D4 = D / 4;
-  auto row_dst = [&](int ks, int h, float*& dst, float*& ldst) {
-    const int hgs = slot_hg<KVB>(p, s.hg, ks);
-    if (s.dest == DEST_OUT) {
-      const long long orow = out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h);
-      dst = p.out + orow * D;
-      ldst = p.lse ? p.lse + orow : nullptr;
-    } else if (s.dest == DEST_SPLIT) {
-      const long long pr =
-          out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h) * p.max_splits + s.slot;
-      dst = p.o_part + pr * D;
-      ldst = p.lse_part + pr;
-    } else {
-      const long long sl =
-          ((long long)blockIdx.x * 2 + s.slot) * (KVB * kHeadTile) + ks * kHeadTile + h;
-      dst = p.ws_o + sl * D;
-      ldst = p.ws_lse + sl;
-    }
-  };
   if (tg == 0 && (!PK || c < 2)) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -1320,8 +1373,9 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     }
     named_bar_sync(kRedBarrier, NCW * 32);  // rows read before the buffer is written again
   }
+  }
   if (s.dest != DEST_PARTIAL) return;
-  if (STAGED || tg == 0) __threadfence();  // the threads that stored the partial state
+  if (FLAT || STAGED || tg == 0) __threadfence();  // the threads that stored the partial state
   named_bar_sync(kRedBarrier, NCW * 32);
   // ---- last-arriver merge of the unit's partial states
   const long long T = pre[p.B];

@@ -202,3 +202,46 @@ def test_workspace_reuse_across_shapes():
         ref_out, ref_lse, _ = oracle_paged(case)
         assert_parity(out.cpu().numpy().reshape(-1, case.D), lse.cpu().numpy().reshape(-1),
                       ref_out, ref_lse, f"reuse/{case.name}")
+
+
+@pytest.mark.parametrize("kind", ["paged", "multi", "sparse"])
+def test_short_sequences_leave_the_workspace_untouched(kind):
+    """With a workspace, short sequences run whole units: the call writes no
+    partial state, so a zero workspace stays all zero, and the result equals
+    the oracle.  Forced to split (unsplit_max_len = 0) the same call cuts
+    every unit and writes partial states.  Both schedules give the oracle's
+    result."""
+    import torch
+    lens = [300, 17, 512, 64]
+    if kind == "sparse":
+        rows = -(-512 // 64)
+        lays = [[list(range(r + 1)) for r in range(rows)], [[r] for r in range(rows)]]
+        case = wl.make_sparse("short_sparse", 43, B=4, Hq=32, Hkv=8, D=128, block_size=16,
+                              seq_lens=lens, sparse_block=64, layouts=lays, num_rows=rows)
+    else:
+        case = _case(42, 128, 32, 8, 16, lens, q_len=2 if kind == "multi" else 1)
+    t = case.device_tensors("cuda")
+    q2 = t["q"][:, 0] if kind == "multi" else t["q"]
+    params = qk.make_params(q2, case.block_size, case.Hkv, case.max_blocks, case.num_blocks,
+                            max_seq_len=case.max_seq_len)
+    from parity import oracle_sparse
+    ref_out, ref_lse, _ = oracle_sparse(case) if kind == "sparse" else oracle_paged(case)
+
+    def call(ws):
+        kw = dict(max_seq_len=case.max_seq_len, workspace=ws)
+        if kind == "sparse":
+            return qk.decode_attn_paged_sparse(t["q"], t["k_pool"], t["v_pool"], t["block_table"],
+                                               t["seq_lens"], t["row_ptr"], t["col_idx"],
+                                               case.sparse_block, **kw)
+        fn = qk.decode_attn_paged_multi if kind == "multi" else qk.decode_attn_paged
+        return fn(t["q"], t["k_pool"], t["v_pool"], t["block_table"], t["seq_lens"], **kw)
+
+    for forced_split in (False, True):
+        ws = torch.zeros(qk.decode_attn_workspace_size(params), dtype=torch.uint8, device="cuda")
+        with qk.tuning(**({"unsplit_max_len": 0} if forced_split else {})):
+            out, lse = call(ws)
+        torch.cuda.synchronize()
+        touched = bool(ws.any().item())
+        assert touched == forced_split, (kind, forced_split)
+        assert_parity(out.cpu().numpy().reshape(-1, case.D), lse.cpu().numpy().reshape(-1),
+                      ref_out, ref_lse, f"{kind} split={forced_split}")
