@@ -236,7 +236,7 @@ void fill_common(KParams& k, const da_params* p) {
   k.num_blocks = p->num_blocks;
   k.qscale = effective_qscale(p);
   k.softcap2 = p->softcap > 0.f ? p->softcap * 1.4426950408889634f : 0.f;
-  k.softcap_k = k.softcap2 > 0.f ? (float)(2.0 * 1.4426950408889634 / (double)k.softcap2) : 0.f;
+  k.softcap_inv = k.softcap2 > 0.f ? (float)(1.0 / (double)k.softcap2) : 0.f;
   k.window = p->sliding_window;
   k.causal = p->causal;
   k.KVB = da::decode_kvb(da::KIND_PAGED, p->head_dim, p->num_kv_heads);

@@ -974,15 +974,36 @@ struct ColMask {
   int lo[2], hi[2];
 };
 
-// Softcap in base-2 score units: cap2 * tanh(x / cap2), cap2 = cap * log2(e),
-// from the identity tanh(y) = 1 - 2 / (e^(2y) + 1) with e^(2y) = 2^(x k),
-// k = 2 log2(e) / cap2: one exp2 and one approximate division.  Near y = 0
-// the absolute error is about 3e-7 * cap2 (the rounding of 2^(x k) next to
-// 1), about 2e-5 for cap = 50; the form saturates to +-cap2 without
-// overflow (2^(x k) = inf gives cap2, 0 gives -cap2) and keeps a NaN score
-// NaN.
-__device__ __forceinline__ float softcap_b2(float x, float cap2, float k) {
-  return cap2 - __fdividef(2.f * cap2, ex2_ftz(x * k) + 1.f);
+// Softcap in base-2 score units: cap2 * tanh(y), y = x / cap2, cap2 = cap *
+// log2(e).  tanh comes from the identity tanh(y) = 1 - 2 / (e^(2y) + 1),
+// e^(2y) = 2^(2 log2(e) y): one exp2 and one approximate division.  Its
+// absolute error, about 3e-7 (the rounding of e^(2y) next to 1), becomes
+// 3e-7 * cap2 in the score: at most 3e-5 up to cap2 = 100, and the form
+// saturates to +-1 without overflow and keeps NaN.  Above cap2 = 100, where
+// that error would grow with the cap, |y| <= 1/2 takes the Taylor series of
+// tanh about 0 instead (coefficients 2^2n (2^2n - 1) B_2n / (2n)! from the
+// Bernoulli numbers, through y^13: the first omitted term is below 1e-7 of
+// tanh(y) at |y| = 1/2), whose error is relative to y; beyond |y| = 1/2 the
+// identity's 3e-7 is below 1e-6 of tanh(y).  The cap is uniform across a
+// launch, so the branch is too.
+constexpr float kSoftcapSeriesAbove = 100.f;
+
+__device__ __forceinline__ float tanh_series(float y) {
+  const float y2 = y * y;
+  float t = 21844.f / 6081075.f;
+  t = fmaf(t, y2, -1382.f / 155925.f);
+  t = fmaf(t, y2, 62.f / 2835.f);
+  t = fmaf(t, y2, -17.f / 315.f);
+  t = fmaf(t, y2, 2.f / 15.f);
+  t = fmaf(t, y2, -1.f / 3.f);
+  return fmaf(t * y2, y, y);
+}
+
+__device__ __forceinline__ float softcap_b2(float x, float cap2, float inv_cap2) {
+  const float y = x * inv_cap2;
+  float t = 1.f - __fdividef(2.f, ex2_ftz(y * 2.8853900817779268f) + 1.f);
+  if (cap2 > kSoftcapSeriesAbove && fabsf(y) <= 0.5f) t = tanh_series(y);
+  return cap2 * t;
 }
 
 // NG 16-key groups of this warp (keys k0[g] .. k0[g]+15) in one online-
@@ -1474,7 +1495,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   const int kvs = warp / TG, tg = warp % TG;
   const int nstages = p.stages;
   const int bs = p.bs;
-  const float2 cap = make_float2(p.softcap2, p.softcap_k);
+  const float2 cap = make_float2(p.softcap2, p.softcap_inv);
   const float qscale = p.qscale;
   const int NH = p.NH;
   const int Hkv = p.Hkv;

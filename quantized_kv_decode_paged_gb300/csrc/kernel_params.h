@@ -106,7 +106,7 @@ struct alignas(128) KParams {
   int bs, log2_bs, max_blocks, num_blocks;
   float qscale;     // scale * log2(e): scores are kept in base-2 units
   float softcap2;   // softcap * log2(e) (0 = off)
-  float softcap_k;  // 2 log2(e) / softcap2 (the softcap's exp2 argument scale)
+  float softcap_inv;  // 1 / softcap2
   int window, causal;
   int stages;
   int sched;

@@ -1,5 +1,7 @@
 """GPU parity of the f16 paged decode path against the double-precision
 oracle, through the C ABI (via the ctypes binding)."""
+import math
+
 import numpy as np
 import pytest
 
@@ -245,3 +247,16 @@ def test_short_sequences_leave_the_workspace_untouched(kind):
         assert touched == forced_split, (kind, forced_split)
         assert_parity(out.cpu().numpy().reshape(-1, case.D), lse.cpu().numpy().reshape(-1),
                       ref_out, ref_lse, f"{kind} split={forced_split}")
+
+
+@pytest.mark.parametrize("softcap", [0.5, 30.0, 70.0, 200.0, 1e3, 1e6, 1e12])
+def test_softcap_from_small_to_huge(softcap):
+    """The softcap over its whole range, with outlier keys (K scaled by 8)
+    so that scores reach both the saturated and the linear part of tanh:
+    small caps saturate nearly every score; large caps leave the scores
+    almost unchanged, which the kernels compute with the series branch of
+    tanh; 1e12 equals no softcap."""
+    case = _case(900 + int(math.log10(softcap) * 10), 128, 16, 4, 16, [1, 77, 1000, 3000],
+                 softcap=softcap, outlier_rate=0.05)
+    for mode in ("stream", "units"):
+        _check_all_rows(case, mode)
