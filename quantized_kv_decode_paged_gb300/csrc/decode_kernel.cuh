@@ -1334,66 +1334,66 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     }
     named_bar_sync(kRedBarrier, NCW * 32);  // rows read before the buffer is written again
   } else {
-  // tree merge of the TG warps of each kv head; warp tg = 0 ends with the sum
-  constexpr int RP = Gm::RED_PARTS;
+    // tree merge of the TG warps of each kv head; warp tg = 0 ends with the sum
+    constexpr int RP = Gm::RED_PARTS;
 #pragma unroll
-  for (int st = TG / 2; st >= 1; st >>= 1) {
-    MergeW w;
+    for (int st = TG / 2; st >= 1; st >>= 1) {
+      MergeW w;
 #pragma unroll
-    for (int part = 0; part < RP; ++part) {
-      if (tg >= st && tg < 2 * st)
-        store_state<D, RP>(a, red + (kvs * (TG / 2) + (tg - st)) * red_floats(D, RP), lane, part);
-      named_bar_sync(kRedBarrier, NCW * 32);
-      if (tg < st) merge_state<D, RP>(a, red + (kvs * (TG / 2) + tg) * red_floats(D, RP), lane, part, w);
-      named_bar_sync(kRedBarrier, NCW * 32);
-    }
-  }
-  // Results go out through shared memory when the merge buffer (free again
-  // after the tree merge's last barrier) holds every row of the unit: the
-  // warps holding them (tg = 0) write normalized rows there, and all
-  // consumer threads copy whole rows to global memory with 16-byte stores.
-  // A slot has at most four rows in the packed kernels, else kHeadTile.
-  // Otherwise (the unpacked int8 tiered kernel with four slots, whose merge
-  // buffer is halved) the tg = 0 warps store their fragments directly.
-  if (tg == 0 && (!PK || c < 2)) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int h = 2 * c + j;
-      if (h >= nh) continue;
-      const float L = a.l[j];
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const float lse = (a.m[j] == kNegInf) ? kNegInf : (a.m[j] + log2f(L)) * kLn2;
-      float* dst;
-      float* ldst;
-      if constexpr (STAGED) {
-        dst = red + (kvs * RPS + h) * SROW;
-        ldst = dst + D;
-      } else {
-        row_dst(kvs, h, dst, ldst);
+      for (int part = 0; part < RP; ++part) {
+        if (tg >= st && tg < 2 * st)
+          store_state<D, RP>(a, red + (kvs * (TG / 2) + (tg - st)) * red_floats(D, RP), lane, part);
+        named_bar_sync(kRedBarrier, NCW * 32);
+        if (tg < st) merge_state<D, RP>(a, red + (kvs * (TG / 2) + tg) * red_floats(D, RP), lane, part, w);
+        named_bar_sync(kRedBarrier, NCW * 32);
       }
+    }
+    // Results go out through shared memory when the merge buffer (free again
+    // after the tree merge's last barrier) holds every row of the unit: the
+    // warps holding them (tg = 0) write normalized rows there, and all
+    // consumer threads copy whole rows to global memory with 16-byte stores.
+    // A slot has at most four rows in the packed kernels, else kHeadTile.
+    // Otherwise (the unpacked int8 tiered kernel with four slots, whose merge
+    // buffer is halved) the tg = 0 warps store their fragments directly.
+    if (tg == 0 && (!PK || c < 2)) {
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        dst[o_row_d<KIND>(mt, r, 0)] = a.o[mt][j] * inv;
-        dst[o_row_d<KIND>(mt, r, 1)] = a.o[mt][2 + j] * inv;
+      for (int j = 0; j < 2; ++j) {
+        const int h = 2 * c + j;
+        if (h >= nh) continue;
+        const float L = a.l[j];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float lse = (a.m[j] == kNegInf) ? kNegInf : (a.m[j] + log2f(L)) * kLn2;
+        float* dst;
+        float* ldst;
+        if constexpr (STAGED) {
+          dst = red + (kvs * RPS + h) * SROW;
+          ldst = dst + D;
+        } else {
+          row_dst(kvs, h, dst, ldst);
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          dst[o_row_d<KIND>(mt, r, 0)] = a.o[mt][j] * inv;
+          dst[o_row_d<KIND>(mt, r, 1)] = a.o[mt][2 + j] * inv;
+        }
+        if (r == 0 && ldst) *ldst = lse;
       }
-      if (r == 0 && ldst) *ldst = lse;
     }
-  }
-  if constexpr (STAGED) {
-    named_bar_sync(kRedBarrier, NCW * 32);
-    for (int idx = tid; idx < KVB * RPS * D4; idx += NCW * 32) {
-      const int d4 = idx % D4, lrow = idx / D4;
-      const int ks = lrow / RPS, h = lrow % RPS;
-      if (h >= unit_nh(p, slot_hg<KVB>(p, s.hg, ks))) continue;
-      const float* row = red + lrow * SROW;
-      float* dst;
-      float* ldst;
-      row_dst(ks, h, dst, ldst);
-      reinterpret_cast<float4*>(dst)[d4] = *reinterpret_cast<const float4*>(row + 4 * d4);
-      if (d4 == 0 && ldst) *ldst = row[D];
+    if constexpr (STAGED) {
+      named_bar_sync(kRedBarrier, NCW * 32);
+      for (int idx = tid; idx < KVB * RPS * D4; idx += NCW * 32) {
+        const int d4 = idx % D4, lrow = idx / D4;
+        const int ks = lrow / RPS, h = lrow % RPS;
+        if (h >= unit_nh(p, slot_hg<KVB>(p, s.hg, ks))) continue;
+        const float* row = red + lrow * SROW;
+        float* dst;
+        float* ldst;
+        row_dst(ks, h, dst, ldst);
+        reinterpret_cast<float4*>(dst)[d4] = *reinterpret_cast<const float4*>(row + 4 * d4);
+        if (d4 == 0 && ldst) *ldst = row[D];
+      }
+      named_bar_sync(kRedBarrier, NCW * 32);  // rows read before the buffer is written again
     }
-    named_bar_sync(kRedBarrier, NCW * 32);  // rows read before the buffer is written again
-  }
   }
   if (s.dest != DEST_PARTIAL) return;
   if (FLAT || STAGED || tg == 0) __threadfence();  // the threads that stored the partial state
