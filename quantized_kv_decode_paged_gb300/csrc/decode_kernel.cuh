@@ -456,6 +456,7 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
     return false;
   }
   // SCHED_SPLIT (paged only): one segment, split blockIdx.x of unit blockIdx.y
+  if constexpr (KIND != KIND_PAGED) return false;
   if (it.n > 0) return false;
   it.n = 1;
   const int u = blockIdx.y;
@@ -1267,7 +1268,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
       const long long orow = out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h);
       dst = p.out + orow * D;
       ldst = p.lse ? p.lse + orow : nullptr;
-    } else if (s.dest == DEST_SPLIT) {
+    } else if (KIND == KIND_PAGED && s.dest == DEST_SPLIT) {
       const long long pr =
           out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h) * p.max_splits + s.slot;
       dst = p.o_part + pr * D;
@@ -1522,7 +1523,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   QFrag<D> q;
 
   while (seg_next<KIND, Gm::TOK>(p, plan, pre, it, s)) {
-    if (s.i0 >= s.i1) {
+    if (KIND == KIND_PAGED && s.i0 >= s.i1) {
       // SPLIT with no visible key: o = 0, lse = -inf
       const int NHs = p.NH;
       for (int idx = tid; idx < KVB * NHs * D; idx += NCW * 32) {
@@ -1877,7 +1878,7 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
   }
   // ---- per-sequence plan
   int fl = 0;
-  if (p.sched == SCHED_SPLIT) {
+  if (KIND == KIND_PAGED && p.sched == SCHED_SPLIT) {
     if (tid == 0) {
       const int b = blockIdx.y / units_per_seq(p);
       SeqPlan e;
