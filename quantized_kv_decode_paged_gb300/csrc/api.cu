@@ -793,7 +793,7 @@ int decode_attn_split_partial(const da_params* p, int32_t split_tokens, int32_t 
   const da::GeoInfo g = da::decode_geo(da::KIND_PAGED, k.D, k.KVB);
   if (g.W == 0) return DA_ERR_UNSUPPORTED;
   int smem = 0;
-  k.stages = pick_stages(da::KIND_PAGED, k.D, k.KVB, g, k.hgu_shift, k.NH, k.Hkv, 1, &smem);
+  k.stages = pick_stages(da::KIND_PAGED_SPLIT, k.D, k.KVB, g, k.hgu_shift, k.NH, k.Hkv, 1, &smem);
   if (k.stages == 0) return DA_ERR_UNSUPPORTED;
   const long long units_total = (long long)p->batch * (k.Hkv / k.KVU) * k.HGN;
   const long long Hq = p->num_q_heads, D = p->head_dim, mb = p->max_blocks_per_seq;
@@ -813,7 +813,7 @@ int decode_attn_split_partial(const da_params* p, int32_t split_tokens, int32_t 
     kk.o_part = o_part + (long long)b0 * Hq * max_splits * D;
     kk.lse_part = lse_part + (long long)b0 * Hq * max_splits;
     kk.grid = max_splits;
-    cudaError_t e = da::launch_decode(da::KIND_PAGED, kk.D, kk.KVB, use_packed(kk), kk,
+    cudaError_t e = da::launch_decode(da::KIND_PAGED_SPLIT, kk.D, kk.KVB, use_packed(kk), kk,
                                       dim3(max_splits, nb * upb), smem,
                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return DA_ERR_CUDA;

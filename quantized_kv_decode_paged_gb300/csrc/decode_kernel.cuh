@@ -223,12 +223,12 @@ __device__ __forceinline__ int plan_sequence(const KParams& p, int b, SeqPlan& e
 }
 
 // Shared-memory plan storage: 4 ints per sequence for the one-token paged
-// kernel, the whole SeqPlan for the others.
+// kernels, the whole SeqPlan for the others.
 template <int KIND>
 struct PlanStore {
   uint8_t* base;
   __device__ __forceinline__ void put(int b, const SeqPlan& e) const {
-    if constexpr (KIND == KIND_PAGED) {
+    if constexpr (one_token_paged(KIND)) {
       reinterpret_cast<SeqPlanPaged*>(base)[b] = SeqPlanPaged{e.lo, e.hi, e.t0, e.ntiles};
     } else {
       reinterpret_cast<SeqPlan*>(base)[b] = e;
@@ -236,7 +236,7 @@ struct PlanStore {
   }
   __device__ __forceinline__ SeqPlan get(int b) const {
     SeqPlan e;
-    if constexpr (KIND == KIND_PAGED) {
+    if constexpr (one_token_paged(KIND)) {
       const SeqPlanPaged s = reinterpret_cast<const SeqPlanPaged*>(base)[b];
       e.lo = s.lo;
       e.hi = s.hi;
@@ -251,7 +251,7 @@ struct PlanStore {
     return e;
   }
   __device__ __forceinline__ int ntiles(int b) const {
-    if constexpr (KIND == KIND_PAGED) {
+    if constexpr (one_token_paged(KIND)) {
       return reinterpret_cast<const SeqPlanPaged*>(base)[b].ntiles;
     } else {
       return reinterpret_cast<const SeqPlan*>(base)[b].ntiles;
@@ -366,6 +366,11 @@ __device__ __forceinline__ void seg_init(const KParams& p, const PlanStore<KIND>
                                          const int* pre, SegIter& it) {
   it.n = 0;
   it.last0 = -1;
+  if constexpr (KIND == KIND_PAGED_SPLIT) {
+    it.g = 0;
+    it.g_end = 1;
+    return;
+  }
   if (p.sched == SCHED_STREAM) {
     const long long T = pre[p.B];
     const int sg = stream_grid(p, T);
@@ -399,7 +404,7 @@ template <int KIND, int TOK>
 __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>& plan,
                                          const int* pre, SegIter& it, Seg& s) {
   const int upb = units_per_seq(p);
-  if (p.sched == SCHED_STREAM) {
+  if (KIND != KIND_PAGED_SPLIT && p.sched == SCHED_STREAM) {
     // the range's last segment first (see seg_init), then [s0, fwd_end)
     const bool last_first = it.last0 >= 0;
     const long long g = last_first ? it.last0 : it.g;
@@ -432,7 +437,7 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
     it.n++;
     return true;
   }
-  if (p.sched == SCHED_UNITS) {
+  if (KIND != KIND_PAGED_SPLIT && p.sched == SCHED_UNITS) {
     while (it.g < it.g_end) {
       const int u = (int)it.g++;
       const int b = u / upb;
@@ -455,8 +460,8 @@ __device__ __forceinline__ bool seg_next(const KParams& p, const PlanStore<KIND>
     }
     return false;
   }
-  // SCHED_SPLIT (paged only): one segment, split blockIdx.x of unit blockIdx.y
-  if constexpr (KIND != KIND_PAGED) return false;
+  // SCHED_SPLIT (its own kind): one segment, split blockIdx.x of unit blockIdx.y
+  if constexpr (KIND != KIND_PAGED_SPLIT) return false;
   if (it.n > 0) return false;
   it.n = 1;
   const int u = blockIdx.y;
@@ -1268,7 +1273,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
       const long long orow = out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h);
       dst = p.out + orow * D;
       ldst = p.lse ? p.lse + orow : nullptr;
-    } else if (KIND == KIND_PAGED && s.dest == DEST_SPLIT) {
+    } else if (KIND == KIND_PAGED_SPLIT && s.dest == DEST_SPLIT) {
       const long long pr =
           out_row<KIND>(p, s.b, slot_kv<KVB>(p, s.kvb, ks), hgs, h) * p.max_splits + s.slot;
       dst = p.o_part + pr * D;
@@ -1396,7 +1401,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
       named_bar_sync(kRedBarrier, NCW * 32);  // rows read before the buffer is written again
     }
   }
-  if (s.dest != DEST_PARTIAL) return;
+  if (KIND == KIND_PAGED_SPLIT || s.dest != DEST_PARTIAL) return;
   if (FLAT || STAGED || tg == 0) __threadfence();  // the threads that stored the partial state
   named_bar_sync(kRedBarrier, NCW * 32);
   // ---- last-arriver merge of the unit's partial states
@@ -1502,7 +1507,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   const int Hkv = p.Hkv;
 
   // Sequences with no visible key: out = 0, lse = -inf.
-  if (p.sched != SCHED_SPLIT) {
+  if (KIND != KIND_PAGED_SPLIT) {
     for (int b = blockIdx.x; b < p.B; b += p.grid) {
       if (plan.ntiles(b) != 0) continue;
       const long long rows = (long long)p.q_len * p.Hq;  // all tokens of sequence b
@@ -1523,7 +1528,7 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
   QFrag<D> q;
 
   while (seg_next<KIND, Gm::TOK>(p, plan, pre, it, s)) {
-    if (KIND == KIND_PAGED && s.i0 >= s.i1) {
+    if (KIND == KIND_PAGED_SPLIT && s.i0 >= s.i1) {
       // SPLIT with no visible key: o = 0, lse = -inf
       const int NHs = p.NH;
       for (int idx = tid; idx < KVB * NHs * D; idx += NCW * 32) {
@@ -1818,7 +1823,7 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
   // 1024-aligned base (128-byte TMA swizzle atoms), by pointer arithmetic so
   // the compiler keeps the shared address space.
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int nplan = (p.sched == SCHED_SPLIT) ? 1 : p.B;
+  const int nplan = (KIND == KIND_PAGED_SPLIT) ? 1 : p.B;
   const SmemLayout L = make_layout(KIND, D, KVB, NCW, Gm::REGION >> hgu_shift<KVB>(p), Gm::TOK,
                                    p.NH, p.Hkv, p.stages, nplan,
                                    KIND == KIND_PAGED_SPARSE ? p.sp_words : 0);
@@ -1878,7 +1883,7 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
   }
   // ---- per-sequence plan
   int fl = 0;
-  if (KIND == KIND_PAGED && p.sched == SCHED_SPLIT) {
+  if (KIND == KIND_PAGED_SPLIT) {
     if (tid == 0) {
       const int b = blockIdx.y / units_per_seq(p);
       SeqPlan e;
@@ -1903,7 +1908,7 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
     const int sf = sparse_plan<KIND, Gm::TOK, Gm::THREADS>(p, plan, sp_base, tid);
     if (sf) atomicOr(&misc->flags, sf);
   }
-  if (p.sched != SCHED_SPLIT && warp == 0) plan_prefix<KIND>(plan, pre, p.B, units_per_seq(p), tid & 31);
+  if (KIND != KIND_PAGED_SPLIT && warp == 0) plan_prefix<KIND>(plan, pre, p.B, units_per_seq(p), tid & 31);
   __syncthreads();
 
   if (warp >= NCW) {

@@ -50,6 +50,7 @@ GeoInfo decode_geo(int kind, int D, int KVB) {
     if (D == 256 && KVB == 2) return geo_info<KIND_TIERED, 256, 2>();
     return g;
   }
+  // KIND_PAGED and KIND_PAGED_SPLIT (the same geometry)
   if (D == 64 && KVB == 1) return geo_info<KIND_PAGED, 64, 1>();
   if (D == 64 && KVB == 2) return geo_info<KIND_PAGED, 64, 2>();
   if (D == 64 && KVB == 4) return geo_info<KIND_PAGED, 64, 4>();
@@ -74,6 +75,9 @@ cudaError_t launch_decode(int kind, int D, int KVB, bool packed, const KParams& 
   if (kind == KIND_PAGED_MULTI)
     return packed ? launch_paged_multi_packed(D, KVB, p, grid, smem, stream)
                   : launch_paged_multi_unpacked(D, KVB, p, grid, smem, stream);
+  if (kind == KIND_PAGED_SPLIT)
+    return packed ? launch_paged_split_packed(D, KVB, p, grid, smem, stream)
+                  : launch_paged_split_unpacked(D, KVB, p, grid, smem, stream);
   return packed ? launch_paged_packed(D, KVB, p, grid, smem, stream)
                 : launch_paged_unpacked(D, KVB, p, grid, smem, stream);
 }

@@ -18,16 +18,24 @@ constexpr uint32_t kRedBarrier = 1;      // named barrier id for the consumer wa
 // several query tokens per sequence.  TIERED: int8 cold pages (+ f16
 // scales) and an f16 hot ring.  TIERED_F16: f16 cold pages and an f16 hot ring.
 // PAGED_SPARSE: f16 pages, one query token, keys selected per query head by
-// a block-sparse CSR layout.
+// a block-sparse CSR layout.  PAGED_SPLIT: PAGED under the SPLIT schedule
+// (the split-partial entry point); PAGED runs STREAM and UNITS only, so that
+// neither kernel carries the other's code.
 enum Kind : int {
   KIND_PAGED = 0,
   KIND_TIERED = 1,
   KIND_TIERED_F16 = 2,
   KIND_PAGED_MULTI = 3,
-  KIND_PAGED_SPARSE = 4
+  KIND_PAGED_SPARSE = 4,
+  KIND_PAGED_SPLIT = 5
 };
 __host__ __device__ constexpr bool is_paged(int kind) {
-  return kind == KIND_PAGED || kind == KIND_PAGED_MULTI || kind == KIND_PAGED_SPARSE;
+  return kind == KIND_PAGED || kind == KIND_PAGED_MULTI || kind == KIND_PAGED_SPARSE ||
+         kind == KIND_PAGED_SPLIT;
+}
+// one query token, no per-head key selection: the compact per-sequence plan
+__host__ __device__ constexpr bool one_token_paged(int kind) {
+  return kind == KIND_PAGED || kind == KIND_PAGED_SPLIT;
 }
 __host__ __device__ constexpr bool is_tiered(int kind) { return !is_paged(kind); }
 __host__ __device__ constexpr bool cold_int8(int kind) { return kind == KIND_TIERED; }
@@ -222,7 +230,7 @@ __host__ __device__ inline SmemLayout make_layout(int kind, int D, int KVB, int 
   L.off_red = off;
   off += (W / 2) * red_floats(D, red_parts(kind)) * 4;
   L.off_plan = off;
-  off += B * (kind == KIND_PAGED ? (int)sizeof(SeqPlanPaged) : (int)sizeof(SeqPlan));
+  off += B * (one_token_paged(kind) ? (int)sizeof(SeqPlanPaged) : (int)sizeof(SeqPlan));
   L.off_pre = off;
   off += (B + 1) * 4;
   L.off_sparse = off;

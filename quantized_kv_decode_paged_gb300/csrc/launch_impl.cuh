@@ -49,6 +49,19 @@ cudaError_t launch_paged_pk(int D, int KVB, const KParams& p, dim3 grid, int sme
 }
 
 template <bool PK>
+cudaError_t launch_paged_split_pk(int D, int KVB, const KParams& p, dim3 grid, int smem,
+                                  cudaStream_t stream) {
+  if (D == 64 && KVB == 1) return launch_decode_impl<KIND_PAGED_SPLIT, 64, 1, PK>(p, grid, smem, stream);
+  if (D == 64 && KVB == 2) return launch_decode_impl<KIND_PAGED_SPLIT, 64, 2, PK>(p, grid, smem, stream);
+  if (D == 64 && KVB == 4) return launch_decode_impl<KIND_PAGED_SPLIT, 64, 4, PK>(p, grid, smem, stream);
+  if (D == 128 && KVB == 1) return launch_decode_impl<KIND_PAGED_SPLIT, 128, 1, PK>(p, grid, smem, stream);
+  if (D == 128 && KVB == 2) return launch_decode_impl<KIND_PAGED_SPLIT, 128, 2, PK>(p, grid, smem, stream);
+  if (D == 128 && KVB == 4) return launch_decode_impl<KIND_PAGED_SPLIT, 128, 4, PK>(p, grid, smem, stream);
+  if (D == 256 && KVB == 1) return launch_decode_impl<KIND_PAGED_SPLIT, 256, 1, PK>(p, grid, smem, stream);
+  return cudaErrorInvalidValue;
+}
+
+template <bool PK>
 cudaError_t launch_tiered_pk(int D, int KVB, const KParams& p, dim3 grid, int smem,
                              cudaStream_t stream) {
   if (D == 128 && KVB == 1) return launch_decode_impl<KIND_TIERED, 128, 1, PK>(p, grid, smem, stream);
@@ -103,6 +116,10 @@ cudaError_t launch_paged_unpacked(int D, int KVB, const KParams& p, dim3 grid, i
                                   cudaStream_t stream);
 cudaError_t launch_paged_packed(int D, int KVB, const KParams& p, dim3 grid, int smem,
                                 cudaStream_t stream);
+cudaError_t launch_paged_split_unpacked(int D, int KVB, const KParams& p, dim3 grid, int smem,
+                                        cudaStream_t stream);
+cudaError_t launch_paged_split_packed(int D, int KVB, const KParams& p, dim3 grid, int smem,
+                                      cudaStream_t stream);
 cudaError_t launch_tiered_unpacked(int D, int KVB, const KParams& p, dim3 grid, int smem,
                                    cudaStream_t stream);
 cudaError_t launch_tiered_packed(int D, int KVB, const KParams& p, dim3 grid, int smem,
