@@ -266,6 +266,7 @@ __device__ __forceinline__ void plan_prefix(const PlanStore<KIND>& plan, int* pr
   const int per = (B + 31) / 32;
   const int b0 = lane * per;
   long long sum = 0;
+#pragma unroll 1
   for (int i = 0; i < per; ++i)
     if (b0 + i < B) sum += (long long)plan.ntiles(b0 + i) * upb;
   long long incl = sum;
@@ -274,6 +275,7 @@ __device__ __forceinline__ void plan_prefix(const PlanStore<KIND>& plan, int* pr
     if (lane >= off) incl += v;
   }
   long long run = incl - sum;
+#pragma unroll 1
   for (int i = 0; i < per; ++i) {
     if (b0 + i < B) {
       pre[b0 + i] = (int)run;
@@ -1314,6 +1316,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
       }
     }
     named_bar_sync(kRedBarrier, NCW * 32);
+#pragma unroll 1
     for (int idx = tid; idx < KVB * FR * D4; idx += NCW * 32) {
       const int d4 = idx % D4, lrow = idx / D4;
       const int ks = lrow / FR, h = lrow % FR;
@@ -1431,6 +1434,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
     constexpr int D4 = D / 4;
     const int nk = c1 - c0 + 1;
     const int NHs = p.NH;  // rows per slot (the last head group's slots may use fewer)
+#pragma unroll 1
     for (int idx = tid; idx < KVB * NHs * D4; idx += NCW * 32) {
       const int d4 = idx % D4;
       const int hh = idx / D4;
@@ -1439,6 +1443,7 @@ __device__ __forceinline__ void finish_segment(const KParams& p, const Seg& s, A
       const int rowoff = ks * kHeadTile + h;
       float M = kNegInf, Wsum = 0.f;
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
       for (int k0 = 0; k0 < nk; k0 += MB) {
         float ls[MB];
         float4 ov[MB];
@@ -1508,12 +1513,15 @@ __device__ __forceinline__ void consumer_loop(const KParams& p, const PlanStore<
 
   // Sequences with no visible key: out = 0, lse = -inf.
   if (KIND != KIND_PAGED_SPLIT) {
+#pragma unroll 1
     for (int b = blockIdx.x; b < p.B; b += p.grid) {
       if (plan.ntiles(b) != 0) continue;
       const long long rows = (long long)p.q_len * p.Hq;  // all tokens of sequence b
+#pragma unroll 1
       for (long long idx = tid; idx < rows * D; idx += NCW * 32)
         p.out[(long long)b * rows * D + idx] = 0.f;
       if (p.lse)
+#pragma unroll 1
         for (long long h = tid; h < rows; h += NCW * 32) p.lse[(long long)b * rows + h] = kNegInf;
     }
   }
@@ -1738,9 +1746,11 @@ __device__ int sparse_plan(const KParams& p, const PlanStore<KIND>& plan, uint32
   // every (sequence, layout) by one thread: its CSR row's bounds, then its
   // columns, eight loads at a time, into the layout's block bitmask (which
   // only this thread writes)
+#pragma unroll 1
   for (int q = tid; q < B * nlu; q += THREADS) {
     const int b = q / nlu, l = q - b * nlu;
     uint32_t* bits = sp + (size_t)b * W + 2 * tw + l * bw;
+#pragma unroll 1
     for (int w = 0; w < bw; ++w) bits[w] = 0u;
     const SeqPlan e = plan.get(b);
     int start = 0, len = 0, f = 0;
@@ -1760,6 +1770,7 @@ __device__ int sparse_plan(const KParams& p, const PlanStore<KIND>& plan, uint32
       }
     }
     const int* cols = p.sp_col_idx + (long long)l * p.sp_nnz + start;
+#pragma unroll 1
     for (int e0 = 0; e0 < len; e0 += 8) {
       int c8[8];
 #pragma unroll
@@ -1777,6 +1788,7 @@ __device__ int sparse_plan(const KParams& p, const PlanStore<KIND>& plan, uint32
   __syncthreads();
   // tiles of [lo, hi) holding a key of a block that some layout selects: a
   // warp per 32-tile word, lane j deciding tile 32w + j
+#pragma unroll 1
   for (int q = warp; q < B * tw; q += NW) {
     const int b = q / tw, w = q - b * tw;
     const SeqPlan e = plan.get(b);
@@ -1796,6 +1808,7 @@ __device__ int sparse_plan(const KParams& p, const PlanStore<KIND>& plan, uint32
   }
   __syncthreads();
   // prefix counts and the tile count of every sequence
+#pragma unroll 1
   for (int b = tid; b < B; b += THREADS) {
     uint32_t* a = sp + (size_t)b * W;
     int run = 0;
@@ -1894,6 +1907,7 @@ __global__ void __launch_bounds__(Geo<KIND, D, KVB>::THREADS, 1)
         fl |= DEV_SPLIT_OVERFLOW;
     }
   } else {
+#pragma unroll 1
     for (int b = tid; b < p.B; b += Gm::THREADS) {
       SeqPlan e;
       const int f = plan_sequence<KIND, Gm::TOK, Gm::TOKH>(p, b, e);
